@@ -1,0 +1,228 @@
+/*
+ * pkv.h -- C ABI of the paged-KV hot path for GB300 (sm_103a).
+ *
+ * Four device computations and their host-side checks:
+ *   pkv_compute_slot_mapping   new-token positions -> flat cache slots
+ *   pkv_store_kvcache          scatter fresh K/V rows into the paged cache
+ *   pkv_paged_attention_decode one query per sequence, GQA, split-K + LSE combine
+ *   pkv_unpack_block_paged     CSR block-paged snapshot -> contiguous [T, H, d]
+ *
+ * Sources (page title -- section):
+ *   "Paged KV Cache - AI infra interview lesson": Walk the Shapes First;
+ *     Step 1: slot_mapping and store_kvcache; Step 2: paged_attention_decode.
+ *   "Block-Paged KV Cache" (Hurray format documentation): The three buffers;
+ *     Element lookup through the block table; Validating the storage invariants.
+ *
+ * Conventions shared by every entry point
+ *   - Plain pointers and sizes only.  "device" pointers must be CUDA device
+ *     (or managed) memory of the current device; "host" pointers are CPU memory.
+ *   - The caller owns every buffer.  The library never allocates, frees or
+ *     synchronises; work is enqueued on `stream` (a cudaStream_t passed as
+ *     void*, NULL = the legacy default stream) and the call returns at once.
+ *   - Shapes and arguments are checked synchronously, before anything is
+ *     enqueued; a failed check returns an error status and enqueues nothing.
+ *     pkv_last_error_string() then describes the failure (thread-local).
+ *   - Errors that depend on device data (a slot or block id out of range, a
+ *     context longer than declared) cannot be seen on the host.  The kernels
+ *     skip the offending element, apply the documented fallback and OR a bit
+ *     (PKV_ERRBIT_*) into `err_flag`, an optional device int32 that the
+ *     caller zeroes and reads back; pass NULL to ignore such errors.
+ *   - Floating-point tensors are contiguous, row-major, in one storage type
+ *     (pkv_dtype) shared by q / key / value / caches / out.  All offsets are
+ *     computed in 64-bit.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* a size, pointer or shape is invalid */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid, but not a combination this build handles */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch, tensor map) */
+    PKV_ERR_OUT_OF_RANGE = 4,  /* host-side index check failed (validators) */
+    PKV_ERR_WORKSPACE = 5      /* workspace missing or smaller than the size query says */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+/* Width of the CSR index buffers ("BlockTableIndexType" U32 / U64). */
+typedef enum pkv_index_type { PKV_U32 = 0, PKV_U64 = 1 } pkv_index_type;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PKV_ERRBIT_SLOT_RANGE   0x01 /* store: slot not -1 and outside [0, num_slots) */
+#define PKV_ERRBIT_BLOCK_RANGE  0x02 /* a used block-table entry outside [0, num_blocks) */
+#define PKV_ERRBIT_CONTEXT      0x04 /* context length < 0, > max_context_len or > table */
+#define PKV_ERRBIT_CSR_PAGE     0x08 /* unpack: a token's page lies outside its seq_ptr slice */
+#define PKV_ERRBIT_CSR_PHYS     0x10 /* unpack: physical page id >= num_pages */
+#define PKV_ERRBIT_SPAN         0x20 /* slot mapping: cu_new disagrees with [start, end) */
+#define PKV_ERRBIT_TIMEOUT      0x40 /* an internal pipeline wait gave up (never expected) */
+
+/* Text of the last error returned on this thread ("" after success). */
+const char *pkv_last_error_string(void);
+
+/* Library version string. */
+const char *pkv_version(void);
+
+/*
+ * pkv_compute_slot_mapping -- "Walk the Shapes First" and "Step 1": the slot
+ * of position p of sequence b is block_tables[b][p / block_size] * block_size
+ * + p % block_size; the mapping covers only the positions written this step.
+ *
+ *   block_tables    device int32 [num_seqs, max_blocks_per_seq], row-major;
+ *                   entries past a sequence's last block may be -1.
+ *   starts, ends    device int32 [num_seqs]: positions [starts[b], ends[b]).
+ *   cu_new          device int32 [num_seqs + 1]: sequence b's slots go to
+ *                   slot_mapping[cu_new[b] .. cu_new[b+1]); cu_new[0] == 0.
+ *   num_blocks      pool size in blocks; block_size * num_blocks < 2^31.
+ *   slot_mapping    device int32 [num_new_tokens] (output).
+ * Device errors: a position whose block is missing (-1 / beyond the row) or
+ * >= num_blocks gets slot -1 and PKV_ERRBIT_BLOCK_RANGE; a sequence whose
+ * cu_new span differs from ends-starts, or exceeds num_new_tokens, writes
+ * only what fits and sets PKV_ERRBIT_SPAN.
+ */
+pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t *starts, const int32_t *ends,
+                                    const int32_t *cu_new, int32_t num_seqs,
+                                    int32_t block_size, int32_t num_blocks,
+                                    int32_t *slot_mapping, int64_t num_new_tokens,
+                                    int32_t *err_flag, void *stream);
+
+/*
+ * pkv_store_kvcache -- "Step 1: slot_mapping and store_kvcache": with the caches
+ * viewed as [num_slots, num_kv_heads * head_dim] rows, row slot_mapping[i]
+ * receives key[i] (and value[i]); slot -1 is padding and is skipped.
+ *
+ *   key, value        device [num_tokens, num_kv_heads, head_dim]
+ *   k_cache, v_cache  device [num_blocks, block_size, num_kv_heads, head_dim],
+ *                     num_slots = num_blocks * block_size rows (modified in place)
+ *   slot_mapping      device int32 [num_tokens]; non-(-1) slots must be
+ *                     distinct (duplicates race: which row wins is undefined).
+ * Device errors: a slot that is neither -1 nor in [0, num_slots) is skipped
+ * and sets PKV_ERRBIT_SLOT_RANGE.
+ */
+pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int32_t *slot_mapping, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int64_t num_slots,
+                             pkv_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
+ * pkv_paged_attention_decode -- "Step 2: paged_attention_decode": for every
+ * sequence b (one query token) and query head h, with n = context_lens[b],
+ *   out[b,h] = softmax_t( scale * q[b,h] . K_t ) . V_t,   t = 0 .. n-1,
+ * where token t lives in cache row block_tables[b][t / block_size] *
+ * block_size + t % block_size, KV head h / (num_q_heads / num_kv_heads).
+ * Only the first ceil(n / block_size) table entries are read (later ones may
+ * be -1); the unused tail of the last block is never read.  The context is
+ * split into partitions that are reduced independently and merged with a
+ * log-sum-exp combine (flash-decoding), so long contexts fill the GPU.
+ *
+ *   out              device [num_seqs, num_q_heads, head_dim] (output, dtype)
+ *   q                device [num_seqs, num_q_heads, head_dim]
+ *   k_cache, v_cache device [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables     device int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens     device int32 [num_seqs], each in [0, max_context_len]
+ *   max_context_len  host bound on context_lens; sizes the grid and workspace
+ *   workspace        device scratch of at least
+ *                    pkv_paged_attention_decode_workspace_size(...) bytes,
+ *                    256-byte aligned; contents need not be initialised.
+ * num_q_heads must be a multiple of num_kv_heads.  Accumulation is fp32; the
+ * result is rounded once to dtype.  n == 0 gives a zero row.
+ * Device errors: a context length < 0, > max_context_len or needing more than
+ * max_blocks_per_seq blocks gives a zero row and PKV_ERRBIT_CONTEXT; a used
+ * block id outside [0, num_blocks) drops that block's tokens from the softmax
+ * and sets PKV_ERRBIT_BLOCK_RANGE.
+ */
+pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks,
+                                      int32_t max_context_len, float scale, pkv_dtype dtype,
+                                      void *workspace, size_t workspace_bytes,
+                                      int32_t *err_flag, void *stream);
+
+/* Workspace bytes pkv_paged_attention_decode needs for these sizes (0 is a
+ * valid answer).  Pure host arithmetic; never fails (returns 0 on bad sizes,
+ * which the decode call then rejects). */
+size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                 int32_t num_kv_heads, int32_t head_dim,
+                                                 int32_t block_size, int32_t max_context_len,
+                                                 pkv_dtype dtype);
+
+/*
+ * pkv_unpack_block_paged -- "The three buffers" and "Element lookup through
+ * the block table": resolve one {kv_role, layer} snapshot into its logical
+ * tensor out[total_tokens, num_heads, head_dim], element by element
+ *   flat = ((block_table[seq_ptr[s] + t / page_size] * page_size
+ *            + t % page_size) * num_heads + h) * head_dim + dim,
+ * for token t of sequence s written to row token_ptr[s] + t.  Pages that
+ * several sequences name (prefix sharing) are read, never copied in the pool.
+ * Call once per role (keys, values) over the same index buffers.
+ *
+ *   page_pool    device [num_pages, page_size, num_heads, head_dim] (paged axis 0)
+ *   block_table  device u32/u64 [nnz]; seq_ptr device u32/u64 [num_seqs + 1]
+ *   token_ptr    device int64 [num_seqs + 1]: sequence s owns output rows
+ *                token_ptr[s] .. token_ptr[s+1]-1 (the CSR buffers do not carry
+ *                per-sequence token counts); token_ptr[num_seqs] == total_tokens.
+ *   out          device [total_tokens, num_heads, head_dim] (output)
+ * Run pkv_validate_index_buffers / pkv_validate_token_ptr on the host copies
+ * first.  Device errors: rows whose page lies outside the sequence's slice
+ * are zero-filled (PKV_ERRBIT_CSR_PAGE); rows on a page id >= num_pages are
+ * zero-filled (PKV_ERRBIT_CSR_PHYS).
+ */
+pkv_status pkv_unpack_block_paged(void *out, const void *page_pool, const void *block_table,
+                                  const void *seq_ptr, pkv_index_type index_type,
+                                  const int64_t *token_ptr, int32_t num_seqs, int64_t nnz,
+                                  int32_t page_size, int64_t num_pages, int32_t num_heads,
+                                  int32_t head_dim, int64_t total_tokens, pkv_dtype dtype,
+                                  int32_t *err_flag, void *stream);
+
+/*
+ * pkv_validate_index_buffers -- "Validating the storage invariants" (host
+ * pointers): seq_ptr[0] == 0; seq_ptr non-decreasing; seq_ptr[num_seqs] ==
+ * nnz; every block_table entry < num_pages.  The empty batch (num_seqs == 0,
+ * seq_ptr == {0}) is valid.  Returns PKV_OK or PKV_ERR_OUT_OF_RANGE (with the
+ * broken invariant in pkv_last_error_string()), PKV_ERR_INVALID_ARG for NULL
+ * pointers or negative sizes.
+ */
+pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void *block_table,
+                                      pkv_index_type index_type, int64_t num_seqs, int64_t nnz,
+                                      int64_t num_pages);
+
+/*
+ * pkv_validate_token_ptr -- host check that token_ptr (host int64 [num_seqs+1])
+ * fits the snapshot: token_ptr[0] == 0, non-decreasing, token_ptr[num_seqs] ==
+ * total_tokens, and every sequence's tokens fit its pages:
+ * ceil(len_s / page_size) <= seq_ptr[s+1] - seq_ptr[s] (seq_ptr host).
+ */
+pkv_status pkv_validate_token_ptr(const int64_t *token_ptr, const void *seq_ptr,
+                                  pkv_index_type index_type, int64_t num_seqs,
+                                  int32_t page_size, int64_t total_tokens);
+
+/*
+ * pkv_block_paged_element_offset -- "Element lookup through the block table"
+ * on host pointers: writes the flat page_pool offset of (seq, token, head, dim)
+ * to *flat_out.  PKV_ERR_OUT_OF_RANGE when seq, head or dim is out of range,
+ * the token's page lies outside the sequence's slice, or the physical page is
+ * >= num_pages.
+ */
+pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, int64_t head, int64_t dim,
+                                          int32_t page_size, int64_t num_pages,
+                                          int32_t num_heads, int32_t head_dim,
+                                          const void *block_table, const void *seq_ptr,
+                                          pkv_index_type index_type, int64_t num_seqs,
+                                          int64_t *flat_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

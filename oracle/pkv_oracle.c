@@ -1,0 +1,304 @@
+/*
+ * pkv_oracle.c -- plain, slow, obviously-correct CPU oracle for the paged-KV
+ * hot path.  TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg call it; the product library never does, and
+ * this file shares no code, header, table or helper with the CUDA path.
+ *
+ * Every floating-point result is computed in IEEE binary64 from inputs widened
+ * exactly from their storage type.  Loops follow the definitions on the pages
+ * one element at a time; nothing is blocked, fused or reordered.
+ *
+ * Sources (page title -- section):
+ *   [P1] "Block-Paged KV Cache" (Hurray format documentation)
+ *        -- "The three buffers", "Element lookup through the block table",
+ *           "Validating the storage invariants".
+ *   [P3] "Paged KV Cache - AI infra interview lesson"
+ *        -- "Walk the Shapes First", "Step 1: slot_mapping and store_kvcache",
+ *           "Step 2: paged_attention_decode".
+ *
+ * Readings where the pages leave a step open are stated beside each function.
+ * Every function here is pinned by a CPU test against a value the pages print,
+ * a closed form, a library routine or brute force; none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Storage types of q / key / value / caches / page pool. */
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+
+/* ---------------------------------------------------------------------------
+ * Exact widening of the storage types to binary64.
+ * ------------------------------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_widen_f16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1F;
+    int frac = bits & 0x3FF;
+    double mag;
+    if (expo == 0) {
+        mag = ldexp((double)frac, -24);              /* zero / subnormal: frac * 2^-24 */
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp(1024.0 + (double)frac, expo - 25); /* (1 + frac/2^10) * 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* bfloat16 is the upper half of an IEEE 754 binary32. */
+double orc_widen_bf16(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int64_t idx, int dtype)
+{
+    if (dtype == ORC_F32) {
+        float f;
+        memcpy(&f, (const char *)base + idx * 4, 4);
+        return (double)f;
+    }
+    uint16_t h;
+    memcpy(&h, (const char *)base + idx * 2, 2);
+    return dtype == ORC_F16 ? orc_widen_f16(h) : orc_widen_bf16(h);
+}
+
+/* ---------------------------------------------------------------------------
+ * [P3] "Walk the Shapes First": the slot of position p of a sequence is
+ * block_table[p // bs] * bs + p % bs.  Returns -1 when the position has no
+ * block (beyond the table row, or a negative entry), which the caller reports.
+ * ------------------------------------------------------------------------- */
+int64_t orc_slot_of_position(const int32_t *bt_row, int32_t max_blocks,
+                             int64_t p, int32_t bs)
+{
+    int64_t logical_block = p / bs;
+    if (p < 0 || logical_block >= max_blocks) return -1;
+    int32_t phys = bt_row[logical_block];
+    if (phys < 0) return -1;
+    return (int64_t)phys * bs + p % bs;
+}
+
+/* [P3] "Step 1: slot_mapping and store_kvcache": the mapping covers only the
+ * tokens computed in this step, positions [start_b, end_b) of every sequence b,
+ * laid out sequence after sequence.  The oracle applies the per-position formula
+ * above (the page's range-per-block form is checked against it by the tests).
+ * Reading: a position with no valid block, or whose block id is >= num_blocks,
+ * is written as -1 and counted in the return value.  Returns the number of such
+ * errors; writes sum(end-start) entries. */
+int64_t orc_compute_slot_mapping(const int32_t *block_tables, int32_t max_blocks,
+                                 const int32_t *starts, const int32_t *ends,
+                                 int32_t num_seqs, int32_t bs, int32_t num_blocks,
+                                 int32_t *slot_mapping)
+{
+    int64_t k = 0, errors = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        const int32_t *row = block_tables + (int64_t)b * max_blocks;
+        for (int64_t p = starts[b]; p < ends[b]; ++p) {
+            int64_t slot = orc_slot_of_position(row, max_blocks, p, bs);
+            if (slot < 0 || slot >= (int64_t)num_blocks * bs) {
+                slot = -1;
+                ++errors;
+            }
+            slot_mapping[k++] = (int32_t)slot;
+        }
+    }
+    return errors;
+}
+
+/* [P3] "Step 1": the cache is viewed as [num_blocks * bs, H_kv * d] rows and
+ * row slot_mapping[i] receives token i's key (and value); a slot of -1 is
+ * padding and is not written.  Rows are moved as raw bytes.  Reading: any
+ * other slot outside [0, num_slots) is not written and is counted. */
+int64_t orc_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+                          const int32_t *slot_mapping, int64_t num_tokens,
+                          int64_t row_bytes, int64_t num_slots)
+{
+    int64_t errors = 0;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= num_slots) { ++errors; continue; }
+        memcpy((char *)k_cache + slot * row_bytes, (const char *)key + i * row_bytes, (size_t)row_bytes);
+        memcpy((char *)v_cache + slot * row_bytes, (const char *)value + i * row_bytes, (size_t)row_bytes);
+    }
+    return errors;
+}
+
+/* [P3] "Step 2: paged_attention_decode".  For sequence b with context length n:
+ * n_blk = ceil(n / bs) blocks are taken from the block-table row (entries past
+ * n_blk may be -1 and are never read); token t < n lives in row
+ * block_table[b][t // bs] * bs + t % bs of the cache [num_blocks, bs, H_kv, d];
+ * query head h reads KV head h // (Hq / H_kv); the output is
+ *     softmax_t(scale * q[b,h] . K[t]) . V[t]
+ * with the usual max subtraction.  Inputs are widened exactly, everything else
+ * is binary64.  The result is written as binary64 to out[B, Hq, d].
+ * Readings: n == 0 gives a zero row; a block id outside [0, num_blocks) inside
+ * n_blk drops that block's tokens from the softmax and is counted; a context
+ * length below 0 gives a zero row and is counted.  Returns the error count. */
+int64_t orc_paged_attention_decode(double *out, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int32_t max_blocks,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t bs, int32_t num_blocks,
+                                   double scale, int dtype)
+{
+    int64_t errors = 0;
+    int32_t group = num_q_heads / num_kv_heads;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int64_t n = context_lens[b];
+        const int32_t *row = block_tables + (int64_t)b * max_blocks;
+        if (n < 0 || (n + bs - 1) / bs > max_blocks) {
+            ++errors;
+            n = -1;
+        }
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        char *usable = (char *)malloc((size_t)(n > 0 ? n : 1));
+        if (n > 0) {
+            for (int64_t j = 0; j < (n + bs - 1) / bs; ++j)
+                if (row[j] < 0 || row[j] >= num_blocks) ++errors;
+        }
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            int32_t g = h / group;
+            double *o = out + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int32_t i = 0; i < head_dim; ++i) o[i] = 0.0;
+            if (n <= 0) continue;
+            int64_t q_base = ((int64_t)b * num_q_heads + h) * head_dim;
+            double m = -INFINITY;
+            for (int64_t t = 0; t < n; ++t) {
+                int32_t phys = row[t / bs];
+                usable[t] = (phys >= 0 && phys < num_blocks);
+                if (!usable[t]) continue;
+                int64_t cache_row = (int64_t)phys * bs + t % bs;
+                int64_t k_base = (cache_row * num_kv_heads + g) * head_dim;
+                double s = 0.0;
+                for (int32_t i = 0; i < head_dim; ++i)
+                    s += load_elem(q, q_base + i, dtype) * load_elem(k_cache, k_base + i, dtype);
+                scores[t] = scale * s;
+                if (scores[t] > m) m = scores[t];
+            }
+            if (m == -INFINITY) continue; /* no usable token */
+            double l = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                if (!usable[t]) continue;
+                scores[t] = exp(scores[t] - m);
+                l += scores[t];
+            }
+            for (int64_t t = 0; t < n; ++t) {
+                if (!usable[t]) continue;
+                int64_t cache_row = (int64_t)row[t / bs] * bs + t % bs;
+                int64_t v_base = (cache_row * num_kv_heads + g) * head_dim;
+                double p = scores[t] / l;
+                for (int32_t i = 0; i < head_dim; ++i)
+                    o[i] += p * load_elem(v_cache, v_base + i, dtype);
+            }
+        }
+        free(scores);
+        free(usable);
+    }
+    return errors;
+}
+
+/* ---------------------------------------------------------------------------
+ * [P1] CSR block-paged snapshot: page_pool [num_pages, page_size, H, d],
+ * block_table (physical page id of every logical page, sequences concatenated),
+ * seq_ptr [num_seqs + 1] delimiting each sequence's slice of block_table.
+ * Index buffers are u32 or u64 ("BlockTableIndexType").
+ * ------------------------------------------------------------------------- */
+static uint64_t load_index(const void *buf, int64_t k, int is_u64)
+{
+    if (is_u64) {
+        uint64_t v;
+        memcpy(&v, (const char *)buf + k * 8, 8);
+        return v;
+    }
+    uint32_t v;
+    memcpy(&v, (const char *)buf + k * 4, 4);
+    return v;
+}
+
+/* [P1] "Validating the storage invariants": seq_ptr[0] == 0; seq_ptr is
+ * non-decreasing; seq_ptr[num_seqs] == len(block_table); every block_table
+ * entry < num_pages.  The empty batch (num_seqs == 0, seq_ptr == [0]) is
+ * valid.  Returns 0 when all hold, else the number (1..4) of the first
+ * invariant found broken, in that order. */
+int orc_validate_index_buffers(const void *seq_ptr, const void *block_table, int is_u64,
+                               int64_t num_seqs, int64_t nnz, uint64_t num_pages)
+{
+    if (load_index(seq_ptr, 0, is_u64) != 0) return 1;
+    for (int64_t s = 0; s < num_seqs; ++s)
+        if (load_index(seq_ptr, s + 1, is_u64) < load_index(seq_ptr, s, is_u64)) return 2;
+    if (load_index(seq_ptr, num_seqs, is_u64) != (uint64_t)nnz) return 3;
+    for (int64_t k = 0; k < nnz; ++k)
+        if (load_index(block_table, k, is_u64) >= num_pages) return 4;
+    return 0;
+}
+
+/* [P1] "Element lookup through the block table":
+ *   page_in_seq = token / page_size;  offset_in_page = token % page_size;
+ *   phys_page   = block_table[seq_ptr[seq] + page_in_seq];
+ *   flat        = ((phys_page * page_size + offset_in_page) * num_heads + head) * head_dim + dim
+ * Reading of the lookup's error cases (the page returns a Result): seq out of
+ * range, page_in_seq outside the sequence's slice, phys_page >= num_pages,
+ * head or dim out of range -> -1. */
+int64_t orc_element_offset(int64_t seq, int64_t token, int64_t head, int64_t dim,
+                           int64_t page_size, uint64_t num_pages, int64_t num_heads,
+                           int64_t head_dim, const void *block_table, const void *seq_ptr,
+                           int is_u64, int64_t num_seqs)
+{
+    if (seq < 0 || seq >= num_seqs || token < 0 || head < 0 || head >= num_heads ||
+        dim < 0 || dim >= head_dim || page_size <= 0)
+        return -1;
+    uint64_t page_in_seq = (uint64_t)(token / page_size);
+    uint64_t offset_in_page = (uint64_t)(token % page_size);
+    uint64_t lo = load_index(seq_ptr, seq, is_u64);
+    uint64_t hi = load_index(seq_ptr, seq + 1, is_u64);
+    if (lo + page_in_seq >= hi) return -1;
+    uint64_t phys = load_index(block_table, (int64_t)(lo + page_in_seq), is_u64);
+    if (phys >= num_pages) return -1;
+    return (int64_t)(((phys * (uint64_t)page_size + offset_in_page) * (uint64_t)num_heads +
+                      (uint64_t)head) * (uint64_t)head_dim + (uint64_t)dim);
+}
+
+/* Unpack the snapshot into the contiguous logical tensor [total_tokens, H, d]
+ * ([P1] "The three buffers": the logical shape is [total_tokens, num_heads,
+ * head_dim]).  Reading: the CSR buffers do not say how many tokens each
+ * sequence holds, so the caller passes token_ptr [num_seqs + 1] (sequence s
+ * owns logical rows token_ptr[s] .. token_ptr[s+1]-1, in token order).  Every
+ * element is resolved independently with the lookup above and copied as raw
+ * bytes; an element whose lookup fails is written as zero bytes and counted.
+ * Aliased pages are simply read more than once. */
+int64_t orc_unpack_block_paged(void *out, const void *page_pool, const void *block_table,
+                               const void *seq_ptr, int is_u64, const int64_t *token_ptr,
+                               int64_t num_seqs, int64_t page_size, uint64_t num_pages,
+                               int64_t num_heads, int64_t head_dim, int64_t elem_bytes)
+{
+    int64_t errors = 0;
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        for (int64_t t = 0; t < token_ptr[s + 1] - token_ptr[s]; ++t) {
+            for (int64_t h = 0; h < num_heads; ++h) {
+                for (int64_t i = 0; i < head_dim; ++i) {
+                    int64_t dst = ((token_ptr[s] + t) * num_heads + h) * head_dim + i;
+                    int64_t src = orc_element_offset(s, t, h, i, page_size, num_pages, num_heads,
+                                                     head_dim, block_table, seq_ptr, is_u64,
+                                                     num_seqs);
+                    if (src < 0) {
+                        memset((char *)out + dst * elem_bytes, 0, (size_t)elem_bytes);
+                        ++errors;
+                    } else {
+                        memcpy((char *)out + dst * elem_bytes,
+                               (const char *)page_pool + src * elem_bytes, (size_t)elem_bytes);
+                    }
+                }
+            }
+        }
+    }
+    return errors;
+}
