@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -65,10 +71,10 @@ typedef enum pkv_index_type { PKV_U32 = 0, PKV_U64 = 1 } pkv_index_type;
 #define PKV_ERRBIT_TIMEOUT      0x40 /* an internal pipeline wait gave up (never expected) */
 
 /* Text of the last error returned on this thread ("" after success). */
-const char *pkv_last_error_string(void);
+PKV_API const char *pkv_last_error_string(void);
 
 /* Library version string. */
-const char *pkv_version(void);
+PKV_API const char *pkv_version(void);
 
 /*
  * pkv_compute_slot_mapping -- "Walk the Shapes First" and "Step 1": the slot
@@ -87,7 +93,7 @@ const char *pkv_version(void);
  * cu_new span differs from ends-starts, or exceeds num_new_tokens, writes
  * only what fits and sets PKV_ERRBIT_SPAN.
  */
-pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+PKV_API pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
                                     const int32_t *starts, const int32_t *ends,
                                     const int32_t *cu_new, int32_t num_seqs,
                                     int32_t block_size, int32_t num_blocks,
@@ -107,7 +113,7 @@ pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int32_t max_blo
  * Device errors: a slot that is neither -1 nor in [0, num_slots) is skipped
  * and sets PKV_ERRBIT_SLOT_RANGE.
  */
-pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+PKV_API pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
                              const int32_t *slot_mapping, int64_t num_tokens,
                              int32_t num_kv_heads, int32_t head_dim, int64_t num_slots,
                              pkv_dtype dtype, int32_t *err_flag, void *stream);
@@ -139,7 +145,7 @@ pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, 
  * block id outside [0, num_blocks) drops that block's tokens from the softmax
  * and sets PKV_ERRBIT_BLOCK_RANGE.
  */
-pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
+PKV_API pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
                                       const void *v_cache, const int32_t *block_tables,
                                       int32_t max_blocks_per_seq, const int32_t *context_lens,
                                       int32_t num_seqs, int32_t num_q_heads,
@@ -152,10 +158,21 @@ pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_ca
 /* Workspace bytes pkv_paged_attention_decode needs for these sizes (0 is a
  * valid answer).  Pure host arithmetic; never fails (returns 0 on bad sizes,
  * which the decode call then rejects). */
-size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+PKV_API size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                                  int32_t num_kv_heads, int32_t head_dim,
                                                  int32_t block_size, int32_t max_context_len,
                                                  pkv_dtype dtype);
+
+/* How pkv_paged_attention_decode will split the context for these sizes:
+ * tokens per partition, number of partitions covering max_context_len
+ * (1 = no combine pass), and whether the TMA/tensor-core path is used
+ * (fp16/bf16, head_dim 128, Hq/Hkv <= 8, block_size a multiple of 16 and
+ * 16-byte aligned pools; 0 = the CUDA-core path).  Any output may be NULL. */
+PKV_API pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t block_size, int32_t max_context_len,
+                                           pkv_dtype dtype, int32_t *partition_tokens,
+                                           int32_t *num_partitions, int32_t *fast_path);
 
 /*
  * pkv_unpack_block_paged -- "The three buffers" and "Element lookup through
@@ -178,7 +195,7 @@ size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, int32_t num_q
  * are zero-filled (PKV_ERRBIT_CSR_PAGE); rows on a page id >= num_pages are
  * zero-filled (PKV_ERRBIT_CSR_PHYS).
  */
-pkv_status pkv_unpack_block_paged(void *out, const void *page_pool, const void *block_table,
+PKV_API pkv_status pkv_unpack_block_paged(void *out, const void *page_pool, const void *block_table,
                                   const void *seq_ptr, pkv_index_type index_type,
                                   const int64_t *token_ptr, int32_t num_seqs, int64_t nnz,
                                   int32_t page_size, int64_t num_pages, int32_t num_heads,
@@ -193,7 +210,7 @@ pkv_status pkv_unpack_block_paged(void *out, const void *page_pool, const void *
  * broken invariant in pkv_last_error_string()), PKV_ERR_INVALID_ARG for NULL
  * pointers or negative sizes.
  */
-pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void *block_table,
+PKV_API pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void *block_table,
                                       pkv_index_type index_type, int64_t num_seqs, int64_t nnz,
                                       int64_t num_pages);
 
@@ -203,9 +220,18 @@ pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void *block_tab
  * total_tokens, and every sequence's tokens fit its pages:
  * ceil(len_s / page_size) <= seq_ptr[s+1] - seq_ptr[s] (seq_ptr host).
  */
-pkv_status pkv_validate_token_ptr(const int64_t *token_ptr, const void *seq_ptr,
+PKV_API pkv_status pkv_validate_token_ptr(const int64_t *token_ptr, const void *seq_ptr,
                                   pkv_index_type index_type, int64_t num_seqs,
                                   int32_t page_size, int64_t total_tokens);
+
+/*
+ * pkv_validate_block_paged_shape -- "Building a descriptor": a block-paged
+ * snapshot is rank-3 only, [total_tokens, num_heads, head_dim] (host array
+ * `shape` of `rank` entries).  PKV_OK when rank == 3, every extent is >= 0
+ * and the last two equal num_heads and head_dim; PKV_ERR_INVALID_ARG otherwise.
+ */
+PKV_API pkv_status pkv_validate_block_paged_shape(const int64_t *shape, int32_t rank,
+                                                  int32_t num_heads, int32_t head_dim);
 
 /*
  * pkv_block_paged_element_offset -- "Element lookup through the block table"
@@ -214,7 +240,7 @@ pkv_status pkv_validate_token_ptr(const int64_t *token_ptr, const void *seq_ptr,
  * the token's page lies outside the sequence's slice, or the physical page is
  * >= num_pages.
  */
-pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, int64_t head, int64_t dim,
+PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, int64_t head, int64_t dim,
                                           int32_t page_size, int64_t num_pages,
                                           int32_t num_heads, int32_t head_dim,
                                           const void *block_table, const void *seq_ptr,

@@ -58,6 +58,18 @@ double orc_widen_bf16(uint16_t bits)
     return (double)f;
 }
 
+/* orc_widen_f16 evaluated once for every bit pattern, so that full-size
+ * inputs do not pay an ldexp per element; the values are the function's. */
+static double f16_table[1 << 16];
+static int f16_table_ready = 0;
+
+static void build_f16_table(void)
+{
+    if (f16_table_ready) return;
+    for (uint32_t b = 0; b < (1u << 16); ++b) f16_table[b] = orc_widen_f16((uint16_t)b);
+    f16_table_ready = 1;
+}
+
 static double load_elem(const void *base, int64_t idx, int dtype)
 {
     if (dtype == ORC_F32) {
@@ -67,7 +79,7 @@ static double load_elem(const void *base, int64_t idx, int dtype)
     }
     uint16_t h;
     memcpy(&h, (const char *)base + idx * 2, 2);
-    return dtype == ORC_F16 ? orc_widen_f16(h) : orc_widen_bf16(h);
+    return dtype == ORC_F16 ? f16_table[h] : orc_widen_bf16(h);
 }
 
 /* ---------------------------------------------------------------------------
@@ -152,6 +164,7 @@ int64_t orc_paged_attention_decode(double *out, const void *q,
 {
     int64_t errors = 0;
     int32_t group = num_q_heads / num_kv_heads;
+    build_f16_table();
     for (int32_t b = 0; b < num_seqs; ++b) {
         int64_t n = context_lens[b];
         const int32_t *row = block_tables + (int64_t)b * max_blocks;

@@ -1,0 +1,831 @@
+// Paged decode attention: one query token per sequence, GQA, split-K over the
+// context with a log-sum-exp combine.
+//
+// "Paged KV Cache - AI infra interview lesson", "Step 2: paged_attention_decode":
+// n_blk = ceil(ctx / bs) block ids are taken from the sequence's table row
+// (later entries may be -1); K and V are gathered through them, the unused
+// tail of the last block is cut, query head h reads KV head h // (Hq / H_kv),
+// and the result is softmax(q K^T * scale) V.
+//
+// Design (GB300, sm_103a)
+// -----------------------
+// The kernel is HBM-bound: every cached K/V byte of a sequence is read once.
+// Work unit = (sequence b, group of HPC KV heads, partition j of the context).
+// One CTA per unit runs a TMA -> shared-memory pipeline:
+//   * a producer warp issues, per 16-token stage, two cp.async.bulk.tensor
+//     loads (K and V) of the box [HPC heads x 2 halves x 16 tokens x 64 dims]
+//     out of a 3-D tensor map over the pool viewed as
+//     (64 elements, num_slots rows, 2 * H_kv half-rows), 128-byte swizzled, so
+//     that the 16 tokens of one head are consecutive 128-byte rows in shared
+//     memory and every ldmatrix below is bank-conflict free;
+//   * one consumer warp per KV head keeps all G = Hq / H_kv query heads of its
+//     group in registers (as the B operand of mma.m16n8k16, G <= 8 padded to
+//     n = 8) and computes S^T = K Q^T for the 16 tokens with 8 MMAs, an online
+//     softmax on the accumulator fragment (max/sum over tokens via 3 shuffles),
+//     transposes P in registers with movmatrix and accumulates O^T += V^T P^T
+//     with 8 more MMAs (V read with ldmatrix.trans).  Each K/V byte therefore
+//     costs a handful of instructions instead of G FMAs + conversions, which
+//     keeps the SMs far from the issue limit at HBM speed.
+// mbarrier full/empty pairs hand stages between producer and consumers; all
+// waits are bounded and report PKV_ERRBIT_TIMEOUT instead of hanging.
+// A partition's output is written directly when the sequence fits in one
+// partition, otherwise as an unnormalised fp32 partial (o, max, sum) that the
+// combine kernel merges.  Shapes outside the fast path (fp32, other head
+// dims, G > 8, block sizes not a multiple of 16) run a plain CUDA-core kernel
+// with the same partitioning and the same combine.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kFastHeadDim = 128;
+constexpr int kStageTokens = 16;
+constexpr int kMaxPartition = 4096;              // tokens; bounds the per-CTA block-id list
+constexpr int kMaxStagesPerPartition = kMaxPartition / kStageTokens;
+constexpr int kTargetSms = 152;                  // GB300; fixed so the plan is device independent
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kCtaDeadlineNs = 2000000000ull;  // every wait of a CTA gives up 2 s after it started
+
+// ----------------------------------------------------------------------------- plan
+struct Plan {
+    bool fast = false;
+    int hpc = 1;          // KV heads per CTA (fast path)
+    int stages = 2;       // pipeline depth (fast path)
+    int partition = 16;   // tokens per partition
+    int nparts = 0;       // partitions covering max_context_len
+    size_t o_bytes = 0;   // fp32 partial outputs
+    size_t ml_bytes = 0;  // (max, sum) per partial
+    size_t ws_bytes = 0;
+};
+
+int env_partition_override() {
+    static int v = [] {
+        const char *s = std::getenv("PKV_DECODE_PARTITION_TOKENS");
+        return s ? std::atoi(s) : 0;
+    }();
+    return v;
+}
+
+Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt) {
+    Plan p;
+    const int G = Hq / Hkv;
+    p.fast = (dt == PKV_F16 || dt == PKV_BF16) && d == kFastHeadDim && G >= 1 && G <= 8 &&
+             bs % kStageTokens == 0;
+    p.hpc = (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
+    const int stage_bytes = p.hpc * 2 * kStageTokens * kFastHeadDim * 2;
+    p.stages = 98304 / stage_bytes;
+    if (p.stages > 8) p.stages = 8;
+    if (p.stages < 2) p.stages = 2;
+    const int64_t units = static_cast<int64_t>(B) * (p.fast ? Hkv / p.hpc : Hq);
+    // Aim for ~8 waves of 2 CTAs per SM; partitions are multiples of 64 tokens.
+    const int64_t target = static_cast<int64_t>(kTargetSms) * 2 * 8;
+    int64_t P = (static_cast<int64_t>(max_ctx) * units + target - 1) / target;
+    P = ((P + 63) / 64) * 64;
+    if (P < 256) P = 256;
+    if (env_partition_override() > 0) P = ((env_partition_override() + 15) / 16) * 16;
+    if (P > kMaxPartition) P = kMaxPartition;
+    if (P >= max_ctx) P = ((max_ctx > 0 ? max_ctx : 1) + 15) / 16 * 16;
+    if (P > kMaxPartition) P = kMaxPartition;
+    p.partition = static_cast<int>(P);
+    p.nparts = max_ctx > 0 ? static_cast<int>((max_ctx + P - 1) / P) : 0;
+    if (p.nparts > 1) {
+        const size_t rows = static_cast<size_t>(B) * Hq * p.nparts;
+        p.o_bytes = (rows * d * sizeof(float) + 255) / 256 * 256;
+        p.ml_bytes = (rows * sizeof(float2) + 255) / 256 * 256;
+        p.ws_bytes = p.o_bytes + p.ml_bytes;
+    }
+    return p;
+}
+
+// ----------------------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: false once the CTA's deadline has passed without the phase
+// completing.  A stage normally lands within microseconds, so the deadline
+// only matters if the pipeline is broken; it keeps such a CTA from hanging.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline) {
+    if (mbar_try_wait(bar, parity)) return true;
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() > deadline) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T> struct Half16;
+template <> struct Half16<__nv_bfloat16> {
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        uint32_t d;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+        return d;
+    }
+    __device__ __forceinline__ static void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+};
+template <> struct Half16<__half> {
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        uint32_t d;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+        return d;
+    }
+    __device__ __forceinline__ static void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Sequence-level validity shared by all kernels: a bad context length gives a
+// zero row (written by partition 0) and PKV_ERRBIT_CONTEXT.
+__device__ __forceinline__ bool context_ok(int ctx, int max_ctx, int bs, int max_blocks) {
+    return ctx >= 0 && ctx <= max_ctx &&
+           (static_cast<int64_t>(ctx) + bs - 1) / bs <= static_cast<int64_t>(max_blocks);
+}
+
+// ----------------------------------------------------------------------------- fast kernel
+template <int HPC, int STAGES>
+struct FastSmem {
+    static constexpr int kTileBytes = HPC * 2 * kStageTokens * 128;  // one of K / V per stage
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kTilesBytes = STAGES * kStageBytes;
+    static constexpr int kBlkOffset = kTilesBytes;
+    static constexpr int kBarOffset = kBlkOffset + kMaxStagesPerPartition * 4;
+    static constexpr int kFlagOffset = kBarOffset + 2 * STAGES * 8;
+    static constexpr int kBytes = kFlagOffset + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+template <typename T, int HPC, int STAGES>
+__global__ void __launch_bounds__((HPC + 1) * 32)
+decode_fast_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   T *__restrict__ out, const T *__restrict__ q,
+                   const int32_t *__restrict__ block_tables, int32_t max_blocks,
+                   const int32_t *__restrict__ context_lens, int32_t Hq, int32_t G, int32_t bs,
+                   int32_t num_blocks, int32_t max_ctx, int32_t partition, int32_t nparts,
+                   float scale_log2, float *__restrict__ o_part, float2 *__restrict__ ml_part,
+                   int32_t *__restrict__ err_flag) {
+    using L = FastSmem<HPC, STAGES>;
+    using H = Half16<T>;
+    const int j = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ctx = context_lens[b];
+    const int heads_per_cta = HPC * G;
+    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) {
+        if (j == 0) {
+            if (ctx != 0 && threadIdx.x == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
+            T *o = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * heads_per_cta) * kFastHeadDim;
+            for (int i = threadIdx.x; i < heads_per_cta * kFastHeadDim; i += blockDim.x) o[i] = from_f32<T>(0.f);
+        }
+        return;
+    }
+    const int t0 = j * partition;
+    if (t0 >= ctx) return;
+    // Once any CTA has reported a broken pipeline, the rest of the launch stops early.
+    if (err_flag && (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT)) return;
+    const uint64_t deadline = global_ns() + kCtaDeadlineNs;
+    const int t1 = min(t0 + partition, ctx);
+    const int nstage = (t1 - t0 + kStageTokens - 1) / kStageTokens;
+    const bool single = ctx <= partition;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *sblk = reinterpret_cast<int32_t *>(smem + L::kBlkOffset);
+    const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlagOffset);
+    const uint32_t tiles = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8 * s, 1);
+            mbar_init(bar0 + 8 * (STAGES + s), HPC);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == HPC) {  // producer warp: resolve this partition's block ids once
+        const int32_t *row = block_tables + static_cast<int64_t>(b) * max_blocks;
+        bool bad = false;
+        for (int s = lane; s < nstage; s += 32) {
+            const int pos = t0 + s * kStageTokens;
+            int32_t id = row[pos / bs];
+            if (id < 0 || id >= num_blocks) { id = -1; bad = true; }
+            sblk[s] = id;
+        }
+        if (bad && err_flag) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
+    }
+    __syncthreads();
+
+    if (warp == HPC) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int s = 0; s < nstage; ++s) {
+                const int slot = s % STAGES;
+                const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
+                if (s >= STAGES && !mbar_wait(empty, ((s / STAGES) - 1) & 1, deadline)) {
+                    *abort_flag = 1;
+                    if (err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+                    break;
+                }
+                const int id = sblk[s];
+                if (id >= 0) {
+                    const int slot_row = id * bs + (t0 + s * kStageTokens) % bs;
+                    const uint32_t dst = tiles + slot * L::kStageBytes;
+                    mbar_arrive_expect_tx(full, L::kStageBytes);
+                    tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
+                    tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full);
+                } else {
+                    mbar_arrive(full);  // nothing to load: consumers mask the whole stage
+                }
+                issued = s + 1;
+            }
+            // Drain: no bulk copy may still be writing shared memory when the CTA exits.
+            for (int s = issued - STAGES > 0 ? issued - STAGES : 0; s < issued; ++s)
+                if (!mbar_wait(bar0 + 8 * (s % STAGES), (s / STAGES) & 1, deadline) && err_flag)
+                    atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumer warp
+    const int g = lane >> 2, t = lane & 3;
+    const int hk = hg * HPC + warp;  // KV head of this warp
+    uint32_t qf[8][2];
+    {
+        const bool live = g < G;
+        const T *qrow = q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G + (live ? g : 0)) * kFastHeadDim;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+            qf[kc][0] = live ? __ldg(q32 + kc * 8 + t) : 0u;
+            qf[kc][1] = live ? __ldg(q32 + kc * 8 + 4 + t) : 0u;
+        }
+    }
+    float o[8][4];
+#pragma unroll
+    for (int dc = 0; dc < 8; ++dc)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dc][e] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    // Per-lane ldmatrix row offsets inside this warp's head (rows of 128 B,
+    // row R = (2 * warp + half) * 16 + token, chunk swizzled with R & 7).
+    const int mi = lane >> 3, r = lane & 7;
+    const uint32_t head_off = static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
+    uint32_t k_off[8], v_off[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        {   // QK: A = K[16 tokens x 16 dims]; matrices (tok 0-7|8-15) x (dims 0-7|8-15)
+            const int tok = r + 8 * (mi & 1);
+            const int c16 = 2 * c + (mi >> 1);
+            const int R = ((c16 >> 3)) * kStageTokens + tok;
+            k_off[c] = head_off + R * 128 + (((c16 & 7) ^ r) << 4);
+        }
+        {   // PV: A = V^T[16 dims x 16 tokens] via .trans; matrices (dims 0-7|8-15) x (tok 0-7|8-15)
+            const int tok = r + 8 * (mi >> 1);
+            const int c16 = 2 * c + (mi & 1);
+            const int R = ((c16 >> 3)) * kStageTokens + tok;
+            v_off[c] = head_off + R * 128 + (((c16 & 7) ^ r) << 4);
+        }
+    }
+
+    for (int s = 0; s < nstage; ++s) {
+        const int slot = s % STAGES;
+        if (!mbar_wait(bar0 + 8 * slot, (s / STAGES) & 1, deadline) || *abort_flag) {
+            if (lane == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+            return;
+        }
+        const uint32_t kt = tiles + slot * L::kStageBytes;
+        const uint32_t vt = kt + L::kTileBytes;
+        const int id = sblk[s];
+        const int pos0 = t0 + s * kStageTokens;
+        const int nvalid = id < 0 ? 0 : min(kStageTokens, t1 - pos0);
+        if (nvalid < kStageTokens) {
+            // Rows past the context (or of a skipped block) may hold anything,
+            // NaN included: zero this head's V rows so 0 * row stays 0.
+            const int nbad = kStageTokens - nvalid;
+            for (int idx = lane; idx < nbad * 16; idx += 32) {
+                const int tok = nvalid + (idx >> 4);
+                const int half = (idx >> 3) & 1;
+                const int chunk = idx & 7;
+                const uint32_t addr = vt + head_off + (half * kStageTokens + tok) * 128 + chunk * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+            }
+            __syncwarp();
+        }
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+            uint32_t a[4];
+            ldsm_x4(kt + k_off[kc], a);
+            H::mma(sc, a, qf[kc][0], qf[kc][1]);
+        }
+        // scores in log2 units; masked tokens -> -inf
+        const bool vg = g < nvalid, vg8 = g + 8 < nvalid;
+        const float x0 = vg ? sc[0] * scale_log2 : -INFINITY;
+        const float x1 = vg ? sc[1] * scale_log2 : -INFINITY;
+        const float x2 = vg8 ? sc[2] * scale_log2 : -INFINITY;
+        const float x3 = vg8 ? sc[3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float p0 = fast_exp2(x0 - base0), p1 = fast_exp2(x1 - base1);
+        const float p2 = fast_exp2(x2 - base0), p3 = fast_exp2(x3 - base1);
+        const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 = l0 * a0 + (p0 + p2);
+        l1 = l1 * a1 + (p1 + p3);
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            o[dc][0] *= a0;
+            o[dc][1] *= a1;
+            o[dc][2] *= a0;
+            o[dc][3] *= a1;
+        }
+        const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            uint32_t a[4];
+            ldsm_x4_trans(vt + v_off[dc], a);
+            H::mma(o[dc], a, pb0, pb1);
+        }
+        if (nvalid < kStageTokens) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));
+    }
+
+    // row sums over the 16 token lanes of each head column
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    }
+    const int hA = 2 * t, hB = 2 * t + 1;  // head columns of this lane
+    const int64_t qhead0 = static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G;
+    if (single) {
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            const int d0 = dc * 16 + g;
+            if (hA < G) {
+                T *dst = out + (qhead0 + hA) * kFastHeadDim;
+                dst[d0] = from_f32<T>(o[dc][0] * inv0);
+                dst[d0 + 8] = from_f32<T>(o[dc][2] * inv0);
+            }
+            if (hB < G) {
+                T *dst = out + (qhead0 + hB) * kFastHeadDim;
+                dst[d0] = from_f32<T>(o[dc][1] * inv1);
+                dst[d0 + 8] = from_f32<T>(o[dc][3] * inv1);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            const int d0 = dc * 16 + g;
+            if (hA < G) {
+                float *dst = o_part + ((qhead0 + hA) * nparts + j) * kFastHeadDim;
+                dst[d0] = o[dc][0];
+                dst[d0 + 8] = o[dc][2];
+            }
+            if (hB < G) {
+                float *dst = o_part + ((qhead0 + hB) * nparts + j) * kFastHeadDim;
+                dst[d0] = o[dc][1];
+                dst[d0 + 8] = o[dc][3];
+            }
+        }
+        if (g == 0) {
+            if (hA < G) ml_part[(qhead0 + hA) * nparts + j] = make_float2(m0, l0);
+            if (hB < G) ml_part[(qhead0 + hB) * nparts + j] = make_float2(m1, l1);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- generic kernel
+constexpr int kGenThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, float *scratch, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, sh);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = scratch[0];
+    for (int w = 1; w < kGenThreads / 32; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
+    return v;
+}
+
+// One CTA per (partition, query head, sequence): scores of the partition in
+// shared memory, fp32 throughout, exact exp2f.
+template <typename T>
+__global__ void __launch_bounds__(kGenThreads)
+decode_generic_kernel(T *__restrict__ out, const T *__restrict__ q, const T *__restrict__ k_cache,
+                      const T *__restrict__ v_cache, const int32_t *__restrict__ block_tables,
+                      int32_t max_blocks, const int32_t *__restrict__ context_lens, int32_t Hq,
+                      int32_t Hkv, int32_t d, int32_t bs, int32_t num_blocks, int32_t max_ctx,
+                      int32_t partition, int32_t nparts, float scale_log2,
+                      float *__restrict__ o_part, float2 *__restrict__ ml_part,
+                      int32_t *__restrict__ err_flag) {
+    const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int ctx = context_lens[b];
+    T *orow = out + (static_cast<int64_t>(b) * Hq + h) * d;
+    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) {
+        if (j == 0) {
+            if (ctx != 0 && threadIdx.x == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
+            for (int i = threadIdx.x; i < d; i += kGenThreads) orow[i] = from_f32<T>(0.f);
+        }
+        return;
+    }
+    const int t0 = j * partition;
+    if (t0 >= ctx) return;
+    const int t1 = min(t0 + partition, ctx);
+    const int n = t1 - t0;
+    const int g = h / (Hq / Hkv);
+    extern __shared__ float gsm[];
+    float *qs = gsm;              // [d]
+    float *sc = gsm + d;          // [partition]
+    float *scratch = sc + partition;  // [32]
+    const int32_t *row = block_tables + static_cast<int64_t>(b) * max_blocks;
+    for (int i = threadIdx.x; i < d; i += kGenThreads) qs[i] = to_f32(q[(static_cast<int64_t>(b) * Hq + h) * d + i]);
+    __syncthreads();
+    bool bad = false;
+    for (int k = threadIdx.x; k < n; k += kGenThreads) {
+        const int pos = t0 + k;
+        const int32_t id = row[pos / bs];
+        if (id < 0 || id >= num_blocks) { sc[k] = -INFINITY; bad = true; continue; }
+        const T *kr = k_cache + ((static_cast<int64_t>(id) * bs + pos % bs) * Hkv + g) * d;
+        float acc = 0.f;
+        for (int i = 0; i < d; ++i) acc = fmaf(qs[i], to_f32(kr[i]), acc);
+        sc[k] = acc * scale_log2;
+    }
+    if (bad && err_flag) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
+    float mx = -INFINITY;
+    for (int k = threadIdx.x; k < n; k += kGenThreads) mx = fmaxf(mx, sc[k]);
+    mx = block_reduce(mx, scratch, true);
+    float lsum = 0.f;
+    for (int k = threadIdx.x; k < n; k += kGenThreads) {
+        const float p = mx == -INFINITY ? 0.f : exp2f(sc[k] - mx);
+        sc[k] = p;
+        lsum += p;
+    }
+    lsum = block_reduce(lsum, scratch, false);  // also orders the sc[] writes before the reads below
+    for (int i = threadIdx.x; i < d; i += kGenThreads) {
+        float acc = 0.f;
+        for (int k = 0; k < n; ++k) {
+            const float p = sc[k];
+            if (p == 0.f) continue;
+            const int pos = t0 + k;
+            const int32_t id = row[pos / bs];
+            acc = fmaf(p, to_f32(v_cache[((static_cast<int64_t>(id) * bs + pos % bs) * Hkv + g) * d + i]), acc);
+        }
+        if (ctx <= partition) {
+            orow[i] = from_f32<T>(lsum > 0.f ? acc / lsum : 0.f);
+        } else {
+            o_part[((static_cast<int64_t>(b) * Hq + h) * nparts + j) * d + i] = acc;
+        }
+    }
+    if (ctx > partition && threadIdx.x == 0)
+        ml_part[(static_cast<int64_t>(b) * Hq + h) * nparts + j] = make_float2(mx, lsum);
+}
+
+// ----------------------------------------------------------------------------- combine
+// out = sum_j w_j o_j / sum_j w_j,  w_j = l_j * 2^(m_j - max_j m_j)  (m in log2 units)
+template <typename T>
+__global__ void __launch_bounds__(128)
+combine_kernel(T *__restrict__ out, const float *__restrict__ o_part, const float2 *__restrict__ ml_part,
+               const int32_t *__restrict__ context_lens, int32_t Hq, int32_t d, int32_t bs,
+               int32_t max_blocks, int32_t max_ctx, int32_t partition, int32_t nparts) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int ctx = context_lens[b];
+    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx <= partition) return;  // written by the main kernel
+    const int np = (ctx + partition - 1) / partition;
+    const int64_t row = static_cast<int64_t>(b) * Hq + h;
+    const float2 *ml = ml_part + row * nparts;
+    float M = -INFINITY;
+    for (int k = 0; k < np; ++k) M = fmaxf(M, ml[k].x);
+    float Lsum = 0.f;
+    for (int k = 0; k < np; ++k) Lsum += M == -INFINITY ? 0.f : ml[k].y * exp2f(ml[k].x - M);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        float acc = 0.f;
+        if (M != -INFINITY)
+            for (int k = 0; k < np; ++k) {
+                const float w = exp2f(ml[k].x - M);
+                acc = fmaf(w, o_part[(row * nparts + k) * d + i], acc);
+            }
+        out[row * d + i] = from_f32<T>(acc * inv);
+    }
+}
+
+// ----------------------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Pool [num_slots, Hkv, 128] viewed as (64 elements, num_slots, 2*Hkv half-rows).
+pkv_status make_kv_map(CUtensorMap *map, const void *pool, CUtensorMapDataType type, int64_t num_slots,
+                       int Hkv, int hpc) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled entry point unavailable");
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_slots), static_cast<cuuint64_t>(2 * Hkv)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hkv) * kFastHeadDim * 2, 128};
+    const cuuint32_t box[3] = {64, kStageTokens, static_cast<cuuint32_t>(2 * hpc)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, type, 3, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+// cudaFuncSetAttribute once per (kernel, device); `done` is the caller's
+// per-kernel bitmask of devices already configured.
+template <typename K>
+cudaError_t ensure_smem(K kernel, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+struct DecodeArgs {
+    void *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables;
+    int32_t max_blocks;
+    const int32_t *context_lens;
+    int32_t B, Hq, Hkv, d, bs, num_blocks, max_ctx;
+    float scale;
+    float *o_part;
+    float2 *ml_part;
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+template <typename T, int HPC, int STAGES>
+pkv_status launch_fast(const DecodeArgs &a, const Plan &p) {
+    using L = FastSmem<HPC, STAGES>;
+    CUtensorMap mk, mv;
+    pkv_status st = make_kv_map(&mk, a.k_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    if (st != PKV_OK) return st;
+    st = make_kv_map(&mv, a.v_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    if (st != PKV_OK) return st;
+    auto kern = decode_fast_kernel<T, HPC, STAGES>;
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = ensure_smem(kern, L::kAlloc, configured);
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
+    // At least one partition, so that zero-length contexts still get their zero rows.
+    dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hkv / HPC, a.B);
+    kern<<<grid, (HPC + 1) * 32, L::kAlloc, a.stream>>>(
+        mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q), a.block_tables, a.max_blocks,
+        a.context_lens, a.Hq, a.Hq / a.Hkv, a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts,
+        a.scale * kLog2e, a.o_part, a.ml_part, a.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+template <typename T>
+pkv_status launch_fast_any(const DecodeArgs &a, const Plan &p) {
+    switch (p.hpc) {
+    case 4: return launch_fast<T, 4, 3>(a, p);
+    case 2: return launch_fast<T, 2, 6>(a, p);
+    default: return launch_fast<T, 1, 8>(a, p);
+    }
+}
+
+template <typename T>
+pkv_status launch_generic_and_combine(const DecodeArgs &a, const Plan &p, bool run_main) {
+    if (run_main) {
+        const size_t smem = (static_cast<size_t>(a.d) + p.partition + 32) * sizeof(float);
+        auto kern = decode_generic_kernel<T>;
+        static std::atomic<uint64_t> configured{0};
+        cudaError_t e = ensure_smem(kern, static_cast<int>(48 * 1024), configured);
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
+        dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hq, a.B);
+        kern<<<grid, kGenThreads, smem, a.stream>>>(
+            static_cast<T *>(a.out), static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache),
+            static_cast<const T *>(a.v_cache), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hkv, a.d,
+            a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part, a.ml_part, a.err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    }
+    if (p.nparts > 1) {
+        dim3 grid(a.Hq, a.B);
+        combine_kernel<T><<<grid, 128, 0, a.stream>>>(static_cast<T *>(a.out), a.o_part, a.ml_part,
+                                                      a.context_lens, a.Hq, a.d, a.bs, a.max_blocks,
+                                                      a.max_ctx, p.partition, p.nparts);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                            int32_t num_kv_heads, int32_t head_dim,
+                                                            int32_t block_size, int32_t max_context_len,
+                                                            pkv_dtype dtype) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        head_dim <= 0 || block_size <= 0 || max_context_len < 0 || dtype_bytes(dtype) == 0)
+        return 0;
+    return make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype).ws_bytes;
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim,
+                                                      int32_t block_size, int32_t max_context_len,
+                                                      pkv_dtype dtype, int32_t *partition_tokens,
+                                                      int32_t *num_partitions, int32_t *fast_path) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        head_dim <= 0 || block_size <= 0 || max_context_len < 0 || dtype_bytes(dtype) == 0)
+        return set_error(PKV_ERR_INVALID_ARG, "decode plan: bad sizes");
+    Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
+    if (partition_tokens) *partition_tokens = p.partition;
+    if (num_partitions) *num_partitions = p.nparts;
+    if (fast_path) *fast_path = p.fast ? 1 : 0;
+    return ok();
+}
+
+extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *block_tables,
+                                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                                 int32_t num_seqs, int32_t num_q_heads,
+                                                 int32_t num_kv_heads, int32_t head_dim,
+                                                 int32_t block_size, int32_t num_blocks,
+                                                 int32_t max_context_len, float scale, pkv_dtype dtype,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int32_t *err_flag, void *stream) {
+    const int64_t es = dtype_bytes(dtype);
+    if (es == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || max_context_len < 0 || max_blocks_per_seq < 0)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: bad sizes");
+    if (num_q_heads % num_kv_heads)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                         num_q_heads, num_kv_heads);
+    if (head_dim > 1024) return set_error(PKV_ERR_UNSUPPORTED, "decode: head_dim > 1024");
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: num_blocks * block_size >= 2^31");
+    if (num_seqs > 65535) return set_error(PKV_ERR_UNSUPPORTED, "decode: more than 65535 sequences in one call");
+    if (num_seqs == 0) return ok();
+    if (!out || !q || !context_lens || (max_blocks_per_seq > 0 && !block_tables) ||
+        (num_blocks > 0 && (!k_cache || !v_cache)))
+        return set_error(PKV_ERR_INVALID_ARG, "decode: NULL pointer");
+    Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
+    if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
+        return set_error(PKV_ERR_WORKSPACE, "decode: workspace needs %zu bytes (256-byte aligned), got %zu",
+                         p.ws_bytes, workspace_bytes);
+    if (!aligned(out, es) || !aligned(q, es) || (k_cache && !aligned(k_cache, es)) || (v_cache && !aligned(v_cache, es)))
+        return set_error(PKV_ERR_INVALID_ARG, "decode: buffers not aligned to the element size");
+    // The fast path additionally wants 16-byte aligned pools (TMA) and 4-byte aligned q.
+    const bool fast = p.fast && num_blocks > 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4);
+    DecodeArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                 num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
+                 p.ws_bytes ? static_cast<float *>(workspace) : nullptr,
+                 p.ws_bytes ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.o_bytes) : nullptr,
+                 err_flag, static_cast<cudaStream_t>(stream)};
+    pkv_status st;
+    if (fast) {
+        st = dtype == PKV_BF16 ? launch_fast_any<__nv_bfloat16>(a, p) : launch_fast_any<__half>(a, p);
+        if (st != PKV_OK) return st;
+        st = dtype == PKV_BF16 ? launch_generic_and_combine<__nv_bfloat16>(a, p, false)
+                               : launch_generic_and_combine<__half>(a, p, false);
+    } else {
+        switch (dtype) {
+        case PKV_BF16: st = launch_generic_and_combine<__nv_bfloat16>(a, p, true); break;
+        case PKV_F16: st = launch_generic_and_combine<__half>(a, p, true); break;
+        default: st = launch_generic_and_combine<float>(a, p, true); break;
+        }
+    }
+    if (st != PKV_OK) return st;
+    return ok();
+}

@@ -25,3 +25,33 @@ def load_golden(name):
 
     with open(os.path.join(ROOT, "tests", "golden", name)) as f:
         return json.load(f)
+
+
+def build_product_library():
+    """Run pagedattention_decode_pkv_gb300/build.py by path: importing it as a
+    submodule would load the package (and a stale libpkv.so) first."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "pagedattention_decode_pkv_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_pkv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build_library()
+
+
+@pytest.fixture(scope="session")
+def pkv():
+    """The product binding; builds libpkv.so in-tree first if needed (nvcc, sm_103a)."""
+    build_product_library()
+    import pagedattention_decode_pkv_gb300 as mod
+
+    return mod
+
+
+@pytest.fixture(scope="session")
+def cuda_dev(pkv):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")

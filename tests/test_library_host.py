@@ -1,0 +1,142 @@
+"""Host-side checks of libpkv.so that need no GPU: every symbol the header
+declares is exported, the host validators agree with the pages' printed cases,
+and argument checks fail synchronously before any CUDA work is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from conftest import ROOT, load_golden
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return sorted(set(re.findall(r"PKV_API[^;(]*?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported(pkv):
+    names = _declared_symbols()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(pkv.LIBRARY_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(names) >= {"pkv_compute_slot_mapping", "pkv_store_kvcache", "pkv_paged_attention_decode",
+                          "pkv_unpack_block_paged"}
+
+
+def test_version(pkv):
+    assert "sm_103a" in pkv.pkv_version()
+
+
+def test_validator_printed_cases(pkv):
+    g = load_golden("validator_cases.json")
+    for c in g["cases"]:
+        for idx in (torch.int32, torch.int64):
+            if c["valid"]:
+                pkv.pkv_validate_index_buffers(c["seq_ptr"], c["block_table"], g["num_pages"], idx)
+            else:
+                with pytest.raises(pkv.PkvError) as e:
+                    pkv.pkv_validate_index_buffers(c["seq_ptr"], c["block_table"], g["num_pages"], idx)
+                assert e.value.status == pkv.PKV_ERR_OUT_OF_RANGE
+
+
+@pytest.mark.parametrize("seq_ptr,block_table", [([1, 2, 3], [0, 1, 0]), ([0, 2, 1], [0, 1, 0]),
+                                                  ([0, 2, 2], [0, 1, 0]), ([0, 2, 3], [0, 1, 9])])
+def test_validator_rejects_each_invariant(pkv, seq_ptr, block_table):
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_validate_index_buffers(seq_ptr, block_table, 5)
+
+
+def test_element_offset_printed_example(pkv):
+    g = load_golden("element_offset_example.json")
+    args = (g["page_size"], g["num_pages"], g["num_heads"], g["head_dim"], g["block_table"], g["seq_ptr"])
+    for idx in (torch.int32, torch.int64):
+        for lk in g["lookups"]:
+            assert pkv.pkv_block_paged_element_offset(lk["seq"], lk["token"], lk["head"], lk["dim"], *args,
+                                                      index_dtype=idx) == lk["flat"]
+        for a, b in g["aliased"]:
+            assert pkv.pkv_block_paged_element_offset(a["seq"], a["token"], a["head"], a["dim"], *args) == \
+                pkv.pkv_block_paged_element_offset(b["seq"], b["token"], b["head"], b["dim"], *args)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_block_paged_element_offset(1, 4, 0, 0, *args)  # beyond seq 1's single page
+
+
+def test_element_offset_matches_oracle_everywhere(pkv, orc):
+    g = torch.Generator().manual_seed(11)
+    ps, npg, H, d = 4, 9, 3, 5
+    lens = [7, 1, 12, 4]
+    pages = [torch.randint(0, npg, ((n + ps - 1) // ps,), generator=g).tolist() for n in lens]
+    seq_ptr = [0]
+    for p in pages:
+        seq_ptr.append(seq_ptr[-1] + len(p))
+    bt = [x for p in pages for x in p]
+    for s, n in enumerate(lens):
+        for t in range(n + ps):  # includes tokens past the sequence's pages
+            for h in range(H):
+                for i in range(d):
+                    want = orc.element_offset(s, t, h, i, ps, npg, H, d, bt, seq_ptr)
+                    if want < 0:
+                        with pytest.raises(pkv.PkvError):
+                            pkv.pkv_block_paged_element_offset(s, t, h, i, ps, npg, H, d, bt, seq_ptr)
+                    else:
+                        assert pkv.pkv_block_paged_element_offset(s, t, h, i, ps, npg, H, d, bt, seq_ptr) == want
+
+
+def test_token_ptr_and_shape_checks(pkv):
+    pkv.pkv_validate_token_ptr([0, 5, 9], [0, 2, 3], 4, 9)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_validate_token_ptr([0, 9, 9], [0, 2, 3], 4, 9)   # 9 tokens need 3 pages, seq 0 has 2
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_validate_token_ptr([0, 5, 8], [0, 2, 3], 4, 9)   # does not end at total_tokens
+    pkv.pkv_validate_block_paged_shape([9, 2, 8], 2, 8)         # the page's rank-3 example
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_validate_block_paged_shape([9, 2], 2, 8)        # rank-2 is refused
+
+
+def test_decode_argument_errors_are_synchronous(pkv):
+    lib = pkv._lib
+    # Hq not a multiple of Hkv: rejected before anything touches a device.
+    st = lib.pkv_paged_attention_decode(None, None, None, None, None, 1, None, 2, 6, 4, 128, 16, 10, 64,
+                                        1.0, pkv.PKV_BF16, None, 0, None, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    assert b"multiple" in lib.pkv_last_error_string()
+    st = lib.pkv_paged_attention_decode(None, None, None, None, None, 1, None, 2, 8, 4, 128, 16, 10, 64,
+                                        1.0, 7, None, 0, None, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # NULL pointers with work to do
+    st = lib.pkv_paged_attention_decode(None, None, None, None, None, 1, None, 2, 8, 4, 128, 16, 10, 64,
+                                        1.0, pkv.PKV_BF16, None, 0, None, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    # empty batch is a no-op
+    st = lib.pkv_paged_attention_decode(None, None, None, None, None, 0, None, 0, 8, 4, 128, 16, 10, 64,
+                                        1.0, pkv.PKV_BF16, None, 0, None, None)
+    assert st == pkv.PKV_OK
+    assert lib.pkv_store_kvcache(None, None, None, None, None, 3, 2, 4, 16, pkv.PKV_F32, None, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_store_kvcache(None, None, None, None, None, 0, 2, 4, 16, pkv.PKV_F32, None, None) == pkv.PKV_OK
+    assert lib.pkv_compute_slot_mapping(None, 4, None, None, None, 2, 0, 8, None, 0, None, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_unpack_block_paged(None, None, None, None, 2, None, 1, 1, 4, 5, 2, 8, 9, pkv.PKV_BF16, None,
+                                      None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_workspace_size_and_plan(pkv):
+    # one partition -> no workspace; long contexts -> partials for every (seq, head, partition)
+    assert pkv.pkv_paged_attention_decode_workspace_size(4, 8, 8, 128, 16, 100, torch.bfloat16) == 0
+    p, n, fast = pkv.pkv_paged_attention_decode_plan(8, 32, 8, 128, 16, 32768, torch.bfloat16)
+    assert fast and p % 16 == 0 and n == -(-32768 // p) and n > 1
+    ws = pkv.pkv_paged_attention_decode_workspace_size(8, 32, 8, 128, 16, 32768, torch.bfloat16)
+    assert ws >= 8 * 32 * n * (128 * 4 + 8)
+    assert not pkv.pkv_paged_attention_decode_plan(2, 4, 2, 8, 4, 64, torch.float32)[2]   # CUDA-core path
+    assert not pkv.pkv_paged_attention_decode_plan(2, 32, 2, 128, 16, 64, torch.bfloat16)[2]  # G = 16 > 8
+    assert pkv.pkv_paged_attention_decode_workspace_size(2, 6, 4, 128, 16, 64, torch.bfloat16) == 0  # invalid
+
+
+def test_binding_refuses_cpu_tensors(pkv):
+    t = torch.zeros(2, 2, 4)
+    with pytest.raises(ValueError):
+        pkv.pkv_paged_attention_decode(t, torch.zeros(1, 4, 2, 4), torch.zeros(1, 4, 2, 4),
+                                       torch.zeros(2, 1, dtype=torch.int32), torch.ones(2, dtype=torch.int32),
+                                       1.0, 4)
