@@ -106,7 +106,8 @@ def test_slot_mapping_errors(pkv, orc, cuda_dev):
                                           (torch.bfloat16, 1, 8, 256)])
 def test_store_parity(pkv, orc, cuda_dev, dtype, H, d, bs):
     g = torch.Generator().manual_seed(H * 1000 + d)
-    nb, N = 24, 150
+    N = 150
+    nb = max(24, (2 * N + bs - 1) // bs)
     kc = torch.randn(nb, bs, H, d, generator=g).to(dtype)
     vc = torch.randn(nb, bs, H, d, generator=g).to(dtype)
     key = torch.randn(N, H, d, generator=g).to(dtype)
