@@ -1,0 +1,528 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV hot path on GB300.
+
+One step = one pass of the whole hot path over one decode batch of the chosen
+workload, through the C ABI (libpkv.so):
+  1. pkv_compute_slot_mapping  -- slot of every sequence's new token (position ctx-1)
+  2. pkv_store_kvcache         -- scatter the new K/V rows into the paged caches
+  3. pkv_paged_attention_decode -- one query per sequence over its whole paged
+                                  context (main pass + split-K combine)
+  4. pkv_unpack_block_paged x2 -- the batch's cache read as a CSR block-paged
+                                  snapshot, unpacked for the key and value roles
+
+`value` is the step's algorithmic HBM bytes divided by the device time of
+the step (GB/s, inputs resident in HBM).  `e2e` is the same metric when
+every step also copies its per-step inputs from pinned host memory and reads
+the attention output back.  `roofline` is the decode-attention call
+(the dominant kernel) against the measured HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+For N > 1 launch under torch.distributed.run: every rank runs its own
+replica of the workload (independent sequences, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import pkv_workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attention KV GB/s and % of GB300 HBM roofline; decode tokens/s"
+DEFAULT_CONFIG = "llama2-7b-layer-fp16"
+DECODE_CONFIGS = ["llama2-7b-layer-fp16", "qwen3-0.6b-gqa-bf16", "long-gqa-8k-bf16", "long-gqa-32k-bf16"]
+DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
+HBM_FALLBACK_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=DECODE_CONFIGS, default=DEFAULT_CONFIG)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0,
+                    help="wall-clock budget of the oracle CPU-baseline sample")
+    ap.add_argument("--skip-cpu-baseline", action="store_true",
+                    help="omit the oracle timing (for profiler runs)")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a host scalar over ranks (timing only; nothing on the data path)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- accounting
+def step_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> dict:
+    """Algorithmic HBM bytes of one step, per kernel (what the computation must
+    move at minimum; split-K partials are implementation overhead, not counted)."""
+    es = torch.tensor([], dtype=cfg.dtype).element_size()
+    B = int(ctx.numel())
+    T = int(ctx.to(torch.int64).sum())
+    row = cfg.num_kv_heads * cfg.head_dim * es
+    q_bytes = B * cfg.num_q_heads * cfg.head_dim * es
+    return {
+        "slot_mapping": B * (4 * 4 + 4),                     # starts, ends, cu_new, table entry; slot out
+        "store_kvcache": B * 4 + 2 * B * row * 2,            # slots; K and V rows read and written
+        "paged_attention_decode": T * 2 * row + 2 * q_bytes + nnz * 4 + B * 4,  # KV once, q, out, tables
+        "unpack_k": 2 * T * row + nnz * 4 + (B + 1) * 12,    # rows read and written, index buffers
+        "unpack_v": 2 * T * row + nnz * 4 + (B + 1) * 12,
+    }
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def profiled_traffic(kernel_key: str, units: float):
+    """DRAM bytes per launch from a committed ncu summary, scaled to `units`,
+    or None when the summary was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel_key]
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if sha != rec["source_sha256"]:
+            return None
+        return rec["dram_bytes_per_unit"] * units
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.device_index = device_index
+
+    def _gpu_selector(self):
+        try:
+            u = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            return vis.split(",")[self.device_index] if vis else str(self.device_index)
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "100", "-i", self._gpu_selector()]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if inside else self.samples
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples_in_timed_region": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [v for v in (num(p[0]) for _, p in used) if v is not None]
+        smax = [v for v in (num(p[1]) for _, p in used) if v is not None]
+        reasons = set()
+        for _, p in used:
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"],
+                                 p[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        power = [v for v in (num(p[2]) for _, p in used) if v is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples_in_timed_region": len(inside),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- the step
+class DecodeStep:
+    """Device buffers and C-ABI argument tuples of one hot-path step."""
+
+    def __init__(self, pkv, cfg: wl.DecodeConfig, seed: int, device):
+        self.pkv, self.cfg, self.device = pkv, cfg, device
+        self.batch = b = wl.decode_batch(cfg, seed=seed, device=device)
+        self.snap = wl.decode_batch_snapshot(b)
+        B, bs = cfg.batch, cfg.block_size
+        self.B = B
+        self.nb = b.extra["num_blocks"]
+        self.slots = torch.empty(B, dtype=torch.int32, device=device)
+        self.out = torch.empty_like(b.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        H, d = cfg.num_kv_heads, cfg.head_dim
+        self.unpacked_k = torch.empty(self.snap.total_tokens, H, d, dtype=cfg.dtype, device=device)
+        self.unpacked_v = torch.empty_like(self.unpacked_k)
+        self.ws_bytes = pkv.pkv_paged_attention_decode_workspace_size(B, cfg.num_q_heads, H, d, bs,
+                                                                      b.max_context_len, cfg.dtype)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.plan = pkv.pkv_paged_attention_decode_plan(B, cfg.num_q_heads, H, d, bs, b.max_context_len, cfg.dtype)
+        self.dt = pkv._DTYPE[cfg.dtype]
+        self.bytes = step_bytes(cfg, b.context_lens.cpu(), self.snap.nnz)
+        self.launches_per_step = 1 + 1 + (2 if self.plan[1] > 1 else 1) + 2
+
+    def run(self, stream_ptr, events=None):
+        """Enqueue one step; events (6 per step) bracket the kernels if given."""
+        L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        ok = 0
+        rec(0)
+        ok |= L.pkv_compute_slot_mapping(p(b.block_tables), b.block_tables.shape[1], p(b.starts), p(b.ends),
+                                         p(b.cu_new), self.B, c.block_size, self.nb, p(self.slots), self.B,
+                                         p(self.err), stream_ptr)
+        rec(1)
+        ok |= L.pkv_store_kvcache(p(b.new_key), p(b.new_value), p(b.k_cache), p(b.v_cache), p(self.slots), self.B,
+                                  c.num_kv_heads, c.head_dim, self.nb * c.block_size, self.dt, p(self.err),
+                                  stream_ptr)
+        rec(2)
+        ok |= L.pkv_paged_attention_decode(p(self.out), p(b.q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
+                                           b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads,
+                                           c.num_kv_heads, c.head_dim, c.block_size, self.nb, b.max_context_len,
+                                           b.scale, self.dt, p(self.workspace), self.workspace.numel(),
+                                           p(self.err), stream_ptr)
+        rec(3)
+        s = self.snap
+        for pool, dst in ((b.k_cache, self.unpacked_k), (b.v_cache, self.unpacked_v)):
+            ok |= L.pkv_unpack_block_paged(p(dst), p(pool), p(s.block_table), p(s.seq_ptr), self.pkv.PKV_U32,
+                                           p(s.token_ptr), self.B, s.nnz, c.block_size, self.nb, c.num_kv_heads,
+                                           c.head_dim, s.total_tokens, self.dt, p(self.err), stream_ptr)
+            rec(4 if dst is self.unpacked_k else 5)
+        if ok != 0:
+            raise RuntimeError("pkv call failed: " + L.pkv_last_error_string().decode())
+
+    # per-step host inputs for the end-to-end measurement
+    def host_inputs(self):
+        b, s = self.batch, self.snap
+        dev_tensors = [b.q, b.new_key, b.new_value, b.block_tables, b.context_lens, b.starts, b.ends, b.cu_new,
+                       s.block_table, s.seq_ptr, s.token_ptr]
+        host = [t.cpu().pin_memory() for t in dev_tensors]
+        return list(zip(host, dev_tensors))
+
+
+def time_device(step: DecodeStep, steps: int, warmup: int, world: int, stream, sampler):
+    ptr = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step.run(ptr)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        for i in range(steps):
+            step.run(ptr, evs[i])
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier(world)
+    total_ms = evs[0][0].elapsed_time(evs[-1][5])
+    names = ["slot_mapping", "store_kvcache", "paged_attention_decode", "unpack_k", "unpack_v"]
+    per = {n: statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, n in enumerate(names)}
+    return total_ms, per, (t_wall0, t_wall1)
+
+
+def time_e2e(step: DecodeStep, steps: int, world: int, stream):
+    pairs = step.host_inputs()
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    err_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = out_host.numel() * out_host.element_size() + 4
+    ptr = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        def one():
+            for h, d in pairs:
+                d.copy_(h, non_blocking=True)
+            step.run(ptr)
+            out_host.copy_(step.out, non_blocking=True)
+            err_host.copy_(step.err, non_blocking=True)
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+# ----------------------------------------------------------------------------- oracle sample
+def oracle_sample_inputs(batch: wl.DecodeBatch, seqs):
+    """The chosen sequences with only the blocks they use, on the CPU (block
+    ids renumbered into a compact pool); plus their CSR view."""
+    cfg, bs = batch.cfg, batch.cfg.block_size
+    ctx = batch.context_lens.cpu()[seqs]
+    tables = batch.block_tables.cpu()[seqs]
+    nblk = [(int(c) + bs - 1) // bs for c in ctx]
+    used = torch.cat([tables[i, :n] for i, n in enumerate(nblk)]).to(torch.int64)
+    remap = {int(x): i for i, x in enumerate(used.tolist())}
+    new_tables = torch.full((len(seqs), max(nblk)), -1, dtype=torch.int32)
+    for i, n in enumerate(nblk):
+        new_tables[i, :n] = torch.tensor([remap[int(x)] for x in tables[i, :n]], dtype=torch.int32)
+    kc = batch.k_cache[used.to(batch.k_cache.device)].cpu()
+    vc = batch.v_cache[used.to(batch.v_cache.device)].cpu()
+    seq_ptr = torch.zeros(len(seqs) + 1, dtype=torch.int64)
+    seq_ptr[1:] = torch.cumsum(torch.tensor(nblk), 0)
+    token_ptr = torch.zeros(len(seqs) + 1, dtype=torch.int64)
+    token_ptr[1:] = torch.cumsum(ctx.to(torch.int64), 0)
+    csr_bt = torch.cat([new_tables[i, :n] for i, n in enumerate(nblk)])
+    return dict(q=batch.q.cpu()[seqs], kc=kc, vc=vc, tables=new_tables, ctx=ctx,
+                starts=batch.starts.cpu()[seqs], ends=batch.ends.cpu()[seqs],
+                key=batch.new_key.cpu()[seqs], value=batch.new_value.cpu()[seqs], nb=len(used),
+                seq_ptr=seq_ptr.to(torch.int32), token_ptr=token_ptr, csr_bt=csr_bt, nnz=len(used))
+
+
+def oracle_step(orc, s, cfg, scale):
+    """The step's computations, done by the oracle on one sample."""
+    slots, _ = orc.compute_slot_mapping(s["tables"], s["starts"], s["ends"], cfg.block_size, s["nb"])
+    kc, vc, _ = orc.store_kvcache(s["key"], s["value"], s["kc"], s["vc"], slots)
+    orc.paged_attention_decode(s["q"], kc, vc, s["tables"], s["ctx"], scale)
+    for pool in (kc, vc):
+        orc.unpack_block_paged(pool, s["csr_bt"], s["seq_ptr"], s["token_ptr"], index_dtype=torch.int32)
+
+
+def cpu_sample_run(batch, budget_s: float, start_seq: int = 0, max_seqs: int | None = None):
+    """Run the oracle over sequences start_seq, start_seq+1, ... until the
+    budget is spent; returns (GB/s, seconds, number of sequences, bytes)."""
+    import oracle as orc
+
+    orc.build()
+    cfg, B = batch.cfg, batch.cfg.batch
+    done, t_total, nbytes = 0, 0.0, 0
+    while t_total < budget_s and (max_seqs is None or done < max_seqs) and done < B:
+        seq = [(start_seq + done) % B]
+        s = oracle_sample_inputs(batch, seq)
+        t0 = time.perf_counter()
+        oracle_step(orc, s, cfg, batch.scale)
+        t_total += time.perf_counter() - t0
+        nbytes += sum(step_bytes(cfg, s["ctx"], s["nnz"]).values())
+        done += 1
+    return nbytes / t_total / 1e9, t_total, done, nbytes
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return 0
+    cfg = wl.CONFIGS[args.config]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    batch = wl.decode_batch(cfg, seed=args.seed, device=device)
+    seqs_per_step = 2
+    for w in range(args.warmup):
+        cpu_sample_run(batch, 1e9, start_seq=w * seqs_per_step, max_seqs=seqs_per_step)
+    t, nbytes = 0.0, 0
+    for i in range(args.steps):
+        _, dt, _, nb = cpu_sample_run(batch, 1e9, start_seq=(args.warmup + i) * seqs_per_step,
+                                      max_seqs=seqs_per_step)
+        t += dt
+        nbytes += nb
+    value = nbytes / t / 1e9
+    sample = (f"{seqs_per_step} sequences of the {cfg.name} batch per step (slot mapping, store, decode "
+              f"attention, K/V unpack of those sequences), single-threaded C oracle in binary64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
+        "data": "synthetic (seeded N(0,1), random block permutation)",
+        "config": {"workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
+                   "l2": "bounded CPU sample; no GPU work"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import pagedattention_decode_pkv_gb300 as pkv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = wl.CONFIGS[args.config]
+    step = DecodeStep(pkv, cfg, seed=args.seed + rank, device=device)
+    stream = torch.cuda.Stream(device)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, per, (tw0, tw1) = time_device(step, args.steps, max(args.warmup, 3), world, stream, sampler)
+    clocks = sampler.summary(tw0, tw1)
+    sampler.stop()
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    if err:
+        raise RuntimeError(f"device error bits {err:#x} during the benchmark")
+
+    e2e_ms, h2d, d2h = time_e2e(step, args.steps, world, stream)
+
+    step_total_bytes = sum(step.bytes.values())
+    total_ms_max = reduce_max(total_ms, world, device)
+    e2e_ms_max = reduce_max(e2e_ms, world, device)
+    all_bytes = reduce_sum(step_total_bytes * args.steps, world, device)
+    value = all_bytes / (total_ms_max * 1e-3) / 1e9
+    e2e_value = all_bytes / (e2e_ms_max * 1e-3) / 1e9
+
+    peak, peak_kind = measured_hbm_peak()
+    attn_ms = per["paged_attention_decode"]
+    attn_gbs = step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9
+    units = int(step.batch.context_lens.to(torch.int64).sum())  # tokens of context per launch
+    traffic = profiled_traffic("paged_attention_decode", units)
+    decode_ms = per["slot_mapping"] + per["store_kvcache"] + attn_ms
+    decode_tok_s = reduce_sum(cfg.batch / (decode_ms * 1e-3), world, device)
+
+    cpu_baseline = None
+    if world == 1 and not args.skip_cpu_baseline:
+        gbs, secs, nseq, nbytes = cpu_sample_run(step.batch, args.cpu_budget_s)
+        cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": f"first {nseq} of {cfg.batch} sequences of the batch, whole step per sequence "
+                                  f"({nbytes / 1e9:.3f} GB of step bytes in {secs:.1f} s), single-threaded C "
+                                  f"oracle in binary64"}
+
+    if rank != 0:
+        return 0
+    kernel_us = {k: round(v * 1e3, 2) for k, v in per.items()}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
+        "data": "synthetic (seeded N(0,1) K/V/q, random non-contiguous block permutation)",
+        "config": {
+            "workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
+            "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+            "block_size": cfg.block_size, "context_tokens": units, "max_context_len": step.batch.max_context_len,
+            "decode_partition_tokens": step.plan[0], "decode_partitions": step.plan[1],
+            "tensor_core_path": step.plan[2],
+            "step": "slot mapping + store_kvcache + paged_attention_decode (+combine) + unpack K and V",
+            "step_bytes": step_total_bytes,
+            "l2": f"inputs larger than L2: {step.bytes['paged_attention_decode'] / 1e9:.2f} GB of KV per step "
+                  f"vs 129 MB L2; no flush",
+            "parallelism": f"replicas x{world} (independent sequences per rank, no data-path collective)",
+        },
+        "decode_tokens_per_s": round(decode_tok_s, 1),
+        "kernel_us": kernel_us,
+        "kernel_gbs": {k: round(step.bytes[k] / (per[k] * 1e-3) / 1e9, 1) for k in per},
+        "roofline": {"kernel": "pkv_paged_attention_decode (main pass + combine)", "bound": "hbm",
+                     "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_8000_nominal": round(attn_gbs / 8000.0, 4),
+                     "traffic": None if traffic is None else round(traffic)},
+        "cpu_baseline": cpu_baseline,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_init(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

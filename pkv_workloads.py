@@ -321,3 +321,32 @@ def tiny_trace(seed: int = 0, device="cpu") -> TinyTrace:
     k0 = torch.zeros(cfg.num_blocks, bs, H, d).to(device)
     v0 = torch.zeros(cfg.num_blocks, bs, H, d).to(device)
     return TinyTrace(cfg=cfg, steps=steps, k_cache0=k0, v_cache0=v0)
+
+
+@dataclass
+class BatchSnapshot:
+    """A decode batch's cache described as a CSR block-paged snapshot (one per
+    role over the same index buffers): block_table concatenates each
+    sequence's ceil(ctx / bs) block ids, seq_ptr delimits the slices and
+    token_ptr the sequences' rows of the logical [total_tokens, Hkv, d]."""
+    block_table: torch.Tensor  # int32 [nnz]
+    seq_ptr: torch.Tensor      # int32 [B+1]
+    token_ptr: torch.Tensor    # int64 [B+1]
+    total_tokens: int
+    nnz: int
+
+
+def decode_batch_snapshot(batch: DecodeBatch) -> BatchSnapshot:
+    bs = batch.cfg.block_size
+    ctx = batch.context_lens.cpu().to(torch.int64)
+    tables = batch.block_tables.cpu()
+    nblk = [(int(c) + bs - 1) // bs for c in ctx]
+    ids = [tables[b, :n] for b, n in enumerate(nblk)]
+    block_table = torch.cat(ids) if ids else torch.zeros(0, dtype=torch.int32)
+    seq_ptr = torch.zeros(len(nblk) + 1, dtype=torch.int64)
+    seq_ptr[1:] = torch.cumsum(torch.tensor(nblk, dtype=torch.int64), 0)
+    token_ptr = torch.zeros(len(nblk) + 1, dtype=torch.int64)
+    token_ptr[1:] = torch.cumsum(ctx, 0)
+    dev = batch.block_tables.device
+    return BatchSnapshot(block_table=block_table.to(torch.int32).to(dev), seq_ptr=seq_ptr.to(torch.int32).to(dev),
+                         token_ptr=token_ptr.to(dev), total_tokens=int(token_ptr[-1]), nnz=int(seq_ptr[-1]))
