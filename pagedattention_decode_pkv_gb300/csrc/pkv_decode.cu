@@ -595,12 +595,24 @@ decode_generic_kernel(T *__restrict__ out, const T *__restrict__ q, const T *__r
 }
 
 // ----------------------------------------------------------------------------- combine
-// out = sum_j w_j o_j / sum_j w_j,  w_j = l_j * 2^(m_j - max_j m_j)  (m in log2 units)
-template <typename T>
-__global__ void __launch_bounds__(128)
+// out = sum_k w_k o_k / sum_k w_k,  w_k = l_k * 2^(m_k - M), M = max_k m_k (m in log2 units).
+// One CTA per (query head, sequence).  The weights are computed once into
+// shared memory; partitions are then spread over the four warps and the head
+// dimension over the lanes (DPL dims per lane, coalesced), with four
+// partitions' loads in flight per thread before they are accumulated.
+constexpr int kCombineThreads = 128;
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombineUnroll = 4;
+
+template <typename T, int DPL>
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(T *__restrict__ out, const float *__restrict__ o_part, const float2 *__restrict__ ml_part,
                const int32_t *__restrict__ context_lens, int32_t Hq, int32_t d, int32_t bs,
                int32_t max_blocks, int32_t max_ctx, int32_t partition, int32_t nparts) {
+    extern __shared__ float csm[];
+    float *w = csm;                        // [nparts]
+    float *red = csm + nparts;             // [kCombineWarps][DPL * 32]
+    __shared__ float scratch[32];
     const int h = blockIdx.x, b = blockIdx.y;
     const int ctx = context_lens[b];
     if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx <= partition) return;  // written by the main kernel
@@ -608,19 +620,77 @@ combine_kernel(T *__restrict__ out, const float *__restrict__ o_part, const floa
     const int64_t row = static_cast<int64_t>(b) * Hq + h;
     const float2 *ml = ml_part + row * nparts;
     float M = -INFINITY;
-    for (int k = 0; k < np; ++k) M = fmaxf(M, ml[k].x);
-    float Lsum = 0.f;
-    for (int k = 0; k < np; ++k) Lsum += M == -INFINITY ? 0.f : ml[k].y * exp2f(ml[k].x - M);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        float acc = 0.f;
-        if (M != -INFINITY)
-            for (int k = 0; k < np; ++k) {
-                const float w = exp2f(ml[k].x - M);
-                acc = fmaf(w, o_part[(row * nparts + k) * d + i], acc);
-            }
-        out[row * d + i] = from_f32<T>(acc * inv);
+    for (int k = threadIdx.x; k < np; k += kCombineThreads) M = fmaxf(M, ml[k].x);
+    M = block_reduce(M, scratch, true);
+    float L = 0.f;
+    for (int k = threadIdx.x; k < np; k += kCombineThreads) {
+        const float2 v = ml[k];
+        const float e = M == -INFINITY ? 0.f : exp2f(v.x - M);
+        w[k] = e;
+        L += v.y * e;
     }
+    L = block_reduce(L, scratch, false);  // its barriers also publish w[]
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *base = o_part + row * nparts * static_cast<int64_t>(d);
+    float acc[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+    for (int k0 = warp; k0 < np; k0 += kCombineWarps * kCombineUnroll) {
+        float v[kCombineUnroll][DPL];
+#pragma unroll
+        for (int u = 0; u < kCombineUnroll; ++u) {
+            const int k = k0 + u * kCombineWarps;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) {
+                const int i = lane + 32 * j;
+                v[u][j] = (k < np && i < d) ? __ldg(base + static_cast<int64_t>(k) * d + i) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCombineUnroll; ++u) {
+            const int k = k0 + u * kCombineWarps;
+            const float wk = k < np ? w[k] : 0.f;
+#pragma unroll
+            for (int j = 0; j < DPL; ++j) acc[j] = fmaf(wk, v[u][j], acc[j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) red[warp * DPL * 32 + lane + 32 * j] = acc[j];
+    __syncthreads();
+    for (int i = threadIdx.x; i < d; i += kCombineThreads) {
+        float sacc = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kCombineWarps; ++ww) sacc += red[ww * DPL * 32 + i];
+        out[row * d + i] = from_f32<T>(sacc * inv);
+    }
+}
+
+template <typename T, int DPL>
+cudaError_t launch_combine_dpl(T *out, const float *o_part, const float2 *ml, const int32_t *ctx, int Hq, int B,
+                               int d, int bs, int max_blocks, int max_ctx, int partition, int nparts,
+                               cudaStream_t s) {
+    const size_t smem = (static_cast<size_t>(nparts) + kCombineWarps * DPL * 32) * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(combine_kernel<T, DPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    combine_kernel<T, DPL><<<dim3(Hq, B), kCombineThreads, smem, s>>>(out, o_part, ml, ctx, Hq, d, bs, max_blocks,
+                                                                      max_ctx, partition, nparts);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine(T *out, const float *o_part, const float2 *ml, const int32_t *ctx, int Hq, int B, int d,
+                           int bs, int max_blocks, int max_ctx, int partition, int nparts, cudaStream_t s) {
+    if (d <= 32) return launch_combine_dpl<T, 1>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+    if (d <= 64) return launch_combine_dpl<T, 2>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+    if (d <= 128) return launch_combine_dpl<T, 4>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+    if (d <= 256) return launch_combine_dpl<T, 8>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+    if (d <= 512) return launch_combine_dpl<T, 16>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+    return launch_combine_dpl<T, 32>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -735,11 +805,8 @@ pkv_status launch_generic_and_combine(const DecodeArgs &a, const Plan &p, bool r
         if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     }
     if (p.nparts > 1) {
-        dim3 grid(a.Hq, a.B);
-        combine_kernel<T><<<grid, 128, 0, a.stream>>>(static_cast<T *>(a.out), a.o_part, a.ml_part,
-                                                      a.context_lens, a.Hq, a.d, a.bs, a.max_blocks,
-                                                      a.max_ctx, p.partition, p.nparts);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_combine<T>(static_cast<T *>(a.out), a.o_part, a.ml_part, a.context_lens, a.Hq, a.B,
+                                          a.d, a.bs, a.max_blocks, a.max_ctx, p.partition, p.nparts, a.stream);
         if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     }
     return PKV_OK;
