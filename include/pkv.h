@@ -175,6 +175,44 @@ PKV_API pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num
                                            int32_t *num_partitions, int32_t *fast_path);
 
 /*
+ * pkv_paged_attention_decode_static_ws -- the same computation and arguments
+ * as pkv_paged_attention_decode, minus the workspace: this variant allocates
+ * nothing and needs nothing allocated for it.  (No counterpart on the pages;
+ * it exists for callers, not for the method.)
+ *
+ * Who needs it: code that cannot allocate device memory where it runs
+ * attention.  One example is a plugin inside an inference engine, whose enqueue
+ * hook may only use memory the engine handed it.  Another is a service that
+ * reserves a fixed memory budget at start-up and must not call cudaMalloc
+ * afterwards.  Such callers still pass q, the caches, the tables and out; the
+ * split-K scratch comes from a fixed region built into the library instead.
+ *
+ * The region is PKV_STATIC_WORKSPACE_BYTES (16 MiB) of device memory that
+ * every GPU loading the library holds until the process exits.  Sizes whose
+ * pkv_paged_attention_decode_workspace_size exceeds it are rejected with
+ * PKV_ERR_WORKSPACE before anything is enqueued; use the workspace variant
+ * for those.
+ *
+ * The first call on each device looks up the region's device address
+ * (cudaGetSymbolAddress) with that device current.  Make that first call
+ * before any stream capture.
+ *
+ * All calls share the one region, and it keeps whatever the last call left
+ * there.  Nothing in it has to start at zero: every call writes each scratch
+ * value before reading it.  Calls whose GPU work overlaps (for example on two
+ * streams at once) race on the region and give wrong results; serialise
+ * them.  The function calls no cudaMalloc/cudaFree and no allocating library
+ * routine.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+PKV_API pkv_status pkv_paged_attention_decode_static_ws(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+    pkv_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
  * pkv_unpack_block_paged -- "The three buffers" and "Element lookup through
  * the block table": resolve one {kv_role, layer} snapshot into its logical
  * tensor out[total_tokens, num_heads, head_dim], element by element

@@ -44,6 +44,8 @@ _SIGS = {
     "pkv_store_kvcache": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_paged_attention_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
+    "pkv_paged_attention_decode_static_ws": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                              _i32, _i32, _f32, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_paged_attention_decode_workspace_size": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int], _sz),
     "pkv_paged_attention_decode_plan": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp],
                                         ctypes.c_int),

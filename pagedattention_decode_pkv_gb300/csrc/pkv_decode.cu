@@ -896,3 +896,66 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
     if (st != PKV_OK) return st;
     return ok();
 }
+
+// ----------------------------------------------------------------------------- no-allocation variant
+// Decode attention for callers that cannot allocate device memory where they
+// run (an engine plugin that may only use memory it was handed, a service with
+// a fixed budget reserved at start-up).  The split-K scratch lives in this
+// fixed region instead of a caller workspace; every GPU that loads the library
+// holds it until exit.  All calls share it: nothing in it must start at zero
+// (each call writes every scratch value before reading it), and calls whose GPU
+// work overlaps race on it.
+static __device__ __align__(256) unsigned char g_pkv_static_workspace[PKV_STATIC_WORKSPACE_BYTES];
+
+namespace pkv {
+namespace {
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_ws_mutex;
+void *g_static_ws_addr[kMaxStaticDevices] = {};
+
+// Device address of the region on the current device, looked up once per
+// device with that device current (host code cannot use the symbol itself).
+pkv_status static_workspace_address(void **addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "static workspace: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxStaticDevices)
+        return set_error(PKV_ERR_UNSUPPORTED, "static workspace: device index %d >= %d", dev, kMaxStaticDevices);
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (!g_static_ws_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_pkv_static_workspace);
+        if (e != cudaSuccess || !p)
+            return set_error(PKV_ERR_CUDA, "static workspace: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_static_ws_addr[dev] = p;
+    }
+    *addr = g_static_ws_addr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_attention_decode_static_ws(
+    void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+    float scale, pkv_dtype dtype, int32_t *err_flag, void *stream) {
+    const size_t need = pkv_paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                                  block_size, max_context_len, dtype);
+    if (need > PKV_STATIC_WORKSPACE_BYTES)
+        return set_error(PKV_ERR_WORKSPACE,
+                         "decode (static workspace): these sizes need %zu bytes of scratch, more than the "
+                         "library's built-in %u bytes; call pkv_paged_attention_decode with a workspace",
+                         need, (unsigned)PKV_STATIC_WORKSPACE_BYTES);
+    void *ws = nullptr;
+    if (need > 0) {
+        pkv_status st = static_workspace_address(&ws);
+        if (st != PKV_OK) return st;
+    }
+    return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                      max_context_len, scale, dtype, ws, need > 0 ? PKV_STATIC_WORKSPACE_BYTES : 0,
+                                      err_flag, stream);
+}
