@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "pkv_internal.h"
+#include "pkv_pdl.cuh"
 
 namespace pkv {
 namespace {
@@ -54,10 +55,15 @@ constexpr int kMaxStagesPerPartition = kMaxPartition / kStageTokens;
 constexpr int kTargetSms = 152;                  // GB300; fixed so the plan is device independent
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kCtaDeadlineNs = 2000000000ull;  // every wait of a CTA gives up 2 s after it started
+constexpr int kMaxStreamSeqs = 1024;   // work-balanced schedule: sequences per call (shared-memory bound)
+constexpr int kMaxStreamCtas = 512;    // work-balanced schedule: CTAs per launch (sizes the workspace)
+constexpr int kMinStreamStages = 4;    // work-balanced schedule: fewest stages a working CTA streams
 
 // ----------------------------------------------------------------------------- plan
 struct Plan {
     bool fast = false;
+    bool stream = false;  // fast path with the work-balanced one-wave schedule
+    int64_t units = 0;    // (sequence, head group) units of the work-balanced schedule
     int hpc = 1;          // KV heads per CTA (fast path)
     int stages = 2;       // pipeline depth (fast path)
     int partition = 16;   // tokens per partition
@@ -75,16 +81,33 @@ int env_partition_override() {
     return v;
 }
 
-Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt) {
+// generic_only: plan the CUDA-core kernel (used when the fast path's pointer
+// alignment does not hold at call time); max_parts > 0 caps the partitions so
+// that the partials fit a workspace sized for another plan.
+Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt, bool generic_only = false,
+               int64_t max_parts = 0) {
     Plan p;
     const int G = Hq / Hkv;
-    p.fast = (dt == PKV_F16 || dt == PKV_BF16) && d == kFastHeadDim && G >= 1 && G <= 8 &&
+    p.fast = !generic_only && (dt == PKV_F16 || dt == PKV_BF16) && d == kFastHeadDim && G >= 1 && G <= 8 &&
              bs % kStageTokens == 0;
     p.hpc = (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
     const int stage_bytes = p.hpc * 2 * kStageTokens * kFastHeadDim * 2;
     p.stages = 98304 / stage_bytes;
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) p.stages = 2;
+    p.stream = p.fast && B <= kMaxStreamSeqs;
+    if (p.stream) {
+        // Pieces: at most one per (unit, CTA) boundary, i.e. units + CTAs.
+        const int64_t HG = Hkv / p.hpc, HU = Hq / HG;
+        p.units = static_cast<int64_t>(B) * HG;
+        const size_t pieces = static_cast<size_t>(p.units + kMaxStreamCtas);
+        p.o_bytes = (pieces * HU * d * sizeof(float) + 255) / 256 * 256;
+        p.ml_bytes = (pieces * HU * sizeof(float2) + 255) / 256 * 256;
+        p.ws_bytes = p.o_bytes + p.ml_bytes + (2 * static_cast<size_t>(p.units) * sizeof(int32_t) + 255) / 256 * 256;
+        p.partition = 0;
+        p.nparts = 0;
+        return p;
+    }
     const int64_t units = static_cast<int64_t>(B) * (p.fast ? Hkv / p.hpc : Hq);
     // Aim for ~8 waves of 2 CTAs per SM; partitions are multiples of 64 tokens.
     const int64_t target = static_cast<int64_t>(kTargetSms) * 2 * 8;
@@ -92,6 +115,8 @@ Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt)
     P = ((P + 63) / 64) * 64;
     if (P < 256) P = 256;
     if (env_partition_override() > 0) P = ((env_partition_override() + 15) / 16) * 16;
+    if (max_parts > 0 && (static_cast<int64_t>(max_ctx) + P - 1) / P > max_parts)
+        P = ((static_cast<int64_t>(max_ctx) + max_parts - 1) / max_parts + 15) / 16 * 16;
     if (P > kMaxPartition) P = kMaxPartition;
     if (P >= max_ctx) P = ((max_ctx > 0 ? max_ctx : 1) + 15) / 16 * 16;
     if (P > kMaxPartition) P = kMaxPartition;
@@ -262,6 +287,8 @@ decode_fast_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                    int32_t *__restrict__ err_flag) {
     using L = FastSmem<HPC, STAGES>;
     using H = Half16<T>;
+    pdl_wait();
+    pdl_trigger();
     const int j = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ctx = context_lens[b];
@@ -532,6 +559,8 @@ decode_generic_kernel(T *__restrict__ out, const T *__restrict__ q, const T *__r
                       int32_t partition, int32_t nparts, float scale_log2,
                       float *__restrict__ o_part, float2 *__restrict__ ml_part,
                       int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
     const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int ctx = context_lens[b];
     T *orow = out + (static_cast<int64_t>(b) * Hq + h) * d;
@@ -613,6 +642,8 @@ combine_kernel(T *__restrict__ out, const float *__restrict__ o_part, const floa
     float *w = csm;                        // [nparts]
     float *red = csm + nparts;             // [kCombineWarps][DPL * 32]
     __shared__ float scratch[32];
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y;
     const int ctx = context_lens[b];
     if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx <= partition) return;  // written by the main kernel
@@ -677,9 +708,8 @@ cudaError_t launch_combine_dpl(T *out, const float *o_part, const float2 *ml, co
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    combine_kernel<T, DPL><<<dim3(Hq, B), kCombineThreads, smem, s>>>(out, o_part, ml, ctx, Hq, d, bs, max_blocks,
-                                                                      max_ctx, partition, nparts);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<T, DPL>, dim3(Hq, B), dim3(kCombineThreads), smem, s, out, o_part, ml, ctx, Hq,
+                      d, bs, max_blocks, max_ctx, partition, nparts);
 }
 
 template <typename T>
@@ -691,6 +721,448 @@ cudaError_t launch_combine(T *out, const float *o_part, const float2 *ml, const 
     if (d <= 256) return launch_combine_dpl<T, 8>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
     if (d <= 512) return launch_combine_dpl<T, 16>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
     return launch_combine_dpl<T, 32>(out, o_part, ml, ctx, Hq, B, d, bs, max_blocks, max_ctx, partition, nparts, s);
+}
+
+// ----------------------------------------------------------------------------- work-balanced kernel
+// One wave of CTAs (every SM holds two).  The work of the launch is the
+// flattened list of 16-token stages over (sequence b, head group hg, stage st),
+// sequences in order, head groups in order, stages in order; CTA c streams the
+// contiguous slice [c*W/C, (c+1)*W/C) of that list, so every CTA moves the same
+// number of K/V bytes whatever the mix of context lengths.  A (b, hg) unit that
+// lies wholly inside one CTA is written straight to `out`; a unit split over
+// several CTAs leaves one unnormalised piece per CTA at piece index unit + c,
+// merged by stream_combine_kernel.  The producer warp maps stages to blocks 32
+// at a time, one chunk ahead of the TMA issue, and hands each stage's (b, hg,
+// position, valid rows, flags) to the consumers through shared memory.
+constexpr int kFlagFirst = 1 << 8;   // first stage of a piece: reset the running softmax
+constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
+constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
+
+template <int HPC, int STAGES>
+struct StreamSmem {
+    static constexpr int kTileBytes = HPC * 2 * kStageTokens * 128;
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kTilesBytes = STAGES * kStageBytes;
+    static constexpr int kCtxOffset = kTilesBytes;                        // int32 effective ctx per sequence
+    static constexpr int kPrefOffset = kCtxOffset + 4 * kMaxStreamSeqs;   // int64 stage prefix per sequence
+    static constexpr int kInfoOffset = kPrefOffset + 8 * (kMaxStreamSeqs + 16);
+    static constexpr int kBarOffset = kInfoOffset + 16 * STAGES;
+    static constexpr int kFlagOffset = kBarOffset + 16 * STAGES;
+    static constexpr int kBytes = kFlagOffset + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+};
+
+// Flattened stage s (< W) -> sequence b, head group hg, stage st of the sequence.
+__device__ __forceinline__ void locate_stage(const int64_t *pref, int B, int HG, int64_t s, int &b, int &hg,
+                                             int &st) {
+    int lo = 0, hi = B - 1;  // largest b with HG * pref[b] <= s (it has at least one stage)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(HG) * pref[mid] <= s) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const int64_t n = pref[b + 1] - pref[b];
+    const int64_t off = s - static_cast<int64_t>(HG) * pref[b];
+    hg = static_cast<int>(off / n);
+    st = static_cast<int>(off - hg * n);
+}
+
+template <typename T, int HPC, int STAGES>
+__global__ void __launch_bounds__((HPC + 1) * 32)
+decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
+                     int32_t max_blocks, const int32_t *__restrict__ context_lens, int32_t B, int32_t Hq,
+                     int32_t G, int32_t HG, int32_t bs, int32_t num_blocks, int32_t max_ctx, float scale_log2,
+                     float *__restrict__ o_piece, float2 *__restrict__ ml_piece, int32_t *__restrict__ unit_first,
+                     int32_t *__restrict__ unit_last, int32_t *__restrict__ err_flag) {
+    using L = StreamSmem<HPC, STAGES>;
+    using H = Half16<T>;
+    const int c = blockIdx.x, C = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *cx = reinterpret_cast<int32_t *>(smem + L::kCtxOffset);
+    int64_t *pref = reinterpret_cast<int64_t *>(smem + L::kPrefOffset);
+    int4 *info = reinterpret_cast<int4 *>(smem + L::kInfoOffset);
+    const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlagOffset);
+    const uint32_t tiles = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(bar0 + 8 * i, 1);
+            mbar_init(bar0 + 8 * (STAGES + i), HPC);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0)  // a broken pipeline elsewhere in the launch stops this CTA early
+        *abort_flag = (err_flag && (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT)) ? 1 : 0;
+    const uint64_t deadline = global_ns() + kCtaDeadlineNs;
+
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        const int ctx = context_lens[b];
+        cx[b] = context_ok(ctx, max_ctx, bs, max_blocks) ? ctx : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of stages per sequence
+        const int chunk = (B + 31) / 32;
+        const int lo = min(lane * chunk, B), hi = min(lo + chunk, B);
+        int64_t sum = 0;
+        for (int b = lo; b < hi; ++b) sum += (cx[b] + kStageTokens - 1) / kStageTokens;
+        int64_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int64_t run = incl - sum;
+        for (int b = lo; b < hi; ++b) {
+            pref[b] = run;
+            run += (cx[b] + kStageTokens - 1) / kStageTokens;
+        }
+        if (lane == 31) pref[B] = incl;
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+    const int64_t W = static_cast<int64_t>(HG) * pref[B];
+    // Working CTAs: at most one per kMinStreamStages stages, so every working CTA's
+    // slice is non-empty and each split unit's pieces come from consecutive CTAs.
+    int64_t Cw = W / kMinStreamStages;
+    if (Cw > C) Cw = C;
+    if (Cw < 1) Cw = 1;
+    const int64_t s0 = c < Cw ? W * c / Cw : 0, s1 = c < Cw ? W * (c + 1) / Cw : 0;
+
+    // Sequences with nothing to stream (empty or invalid context) get zero rows
+    // from CTA b mod C.
+    for (int b = c; b < B; b += C) {
+        if (cx[b] > 0) continue;
+        if (threadIdx.x == 0 && context_lens[b] != 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
+        T *o = out + static_cast<int64_t>(b) * Hq * kFastHeadDim;
+        for (int i = threadIdx.x; i < Hq * kFastHeadDim; i += blockDim.x) o[i] = from_f32<T>(0.f);
+    }
+    const int64_t nst = s1 - s0;
+    if (nst <= 0) return;
+
+    if (warp == HPC) {
+        // ------------------------------------------------------------ producer warp
+        bool bad = false;
+        // Stage i of this CTA, described by lane i % 32 of the chunk that holds it.
+        auto describe = [&](int64_t i, int &b, int &hg, int &pos0, int &meta, int &id) {
+            b = hg = pos0 = meta = 0;
+            id = -1;
+            if (i >= nst) return;
+            int st;
+            locate_stage(pref, B, HG, s0 + i, b, hg, st);
+            const int ctx = cx[b];
+            const int n = (ctx + kStageTokens - 1) / kStageTokens;
+            pos0 = st * kStageTokens;
+            id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];
+            if (id < 0 || id >= num_blocks) {
+                id = -1;
+                bad = true;
+            }
+            int flags = 0;
+            if (i == 0 || st == 0) flags |= kFlagFirst;
+            if (i == nst - 1 || st == n - 1) flags |= kFlagLast;
+            const int64_t u0 = static_cast<int64_t>(HG) * pref[b] + static_cast<int64_t>(hg) * n;
+            if (u0 >= s0 && u0 + n <= s1) flags |= kFlagWhole;
+            meta = (id < 0 ? 0 : min(kStageTokens, ctx - pos0)) | flags;
+            const int64_t u = static_cast<int64_t>(b) * HG + hg;
+            if (st == 0) unit_first[u] = c;
+            if (st == n - 1) unit_last[u] = c;
+        };
+        int cb, chg, cpos, cmeta, cid, nb, nhg, npos, nmeta, nid;
+        describe(lane, cb, chg, cpos, cmeta, cid);
+        bool aborted = false;
+        int64_t issued = 0;
+        const int64_t nchunks = (nst + 31) / 32;
+        for (int64_t k = 0; k < nchunks && !aborted; ++k) {
+            describe((k + 1) * 32 + lane, nb, nhg, npos, nmeta, nid);  // one chunk ahead
+            const int cnt = static_cast<int>(min(static_cast<int64_t>(32), nst - k * 32));
+            for (int j = 0; j < cnt; ++j) {
+                const int64_t i = k * 32 + j;
+                const int slot = static_cast<int>(i % STAGES);
+                const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
+                int ok = 1;
+                if (lane == 0 && i >= STAGES) ok = mbar_wait(empty, ((i / STAGES) - 1) & 1, deadline) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    aborted = true;
+                    break;
+                }
+                const int b = __shfl_sync(0xffffffffu, cb, j), hg = __shfl_sync(0xffffffffu, chg, j);
+                const int pos0 = __shfl_sync(0xffffffffu, cpos, j), meta = __shfl_sync(0xffffffffu, cmeta, j);
+                const int id = __shfl_sync(0xffffffffu, cid, j);
+                if (lane == 0) {
+                    info[slot] = make_int4(b, hg, pos0, meta);
+                    if (id >= 0) {
+                        const int slot_row = id * bs + pos0 % bs;
+                        const uint32_t dst = tiles + slot * L::kStageBytes;
+                        mbar_arrive_expect_tx(full, L::kStageBytes);
+                        tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
+                        tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full);
+                    } else {
+                        mbar_arrive(full);  // nothing to load: the consumers mask the whole stage
+                    }
+                }
+                issued = i + 1;
+                __syncwarp();
+            }
+            cb = nb; chg = nhg; cpos = npos; cmeta = nmeta; cid = nid;
+        }
+        if (lane == 0) {
+            if (aborted) {
+                *abort_flag = 1;
+                if (err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+            }
+            // No bulk copy may still be writing shared memory when the CTA exits.
+            for (int64_t i = issued - STAGES > 0 ? issued - STAGES : 0; i < issued; ++i)
+                if (!mbar_wait(bar0 + 8 * (i % STAGES), (i / STAGES) & 1, deadline) && err_flag)
+                    atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+        }
+        if (bad && err_flag) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumer warp
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, r = lane & 7;
+    const uint32_t head_off = static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
+    uint32_t k_off[8], v_off[8];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        {
+            const int tok = r + 8 * (mi & 1);
+            const int c16 = 2 * cc + (mi >> 1);
+            k_off[cc] = head_off + ((c16 >> 3) * kStageTokens + tok) * 128 + (((c16 & 7) ^ r) << 4);
+        }
+        {
+            const int tok = r + 8 * (mi >> 1);
+            const int c16 = 2 * cc + (mi & 1);
+            v_off[cc] = head_off + ((c16 >> 3) * kStageTokens + tok) * 128 + (((c16 & 7) ^ r) << 4);
+        }
+    }
+    uint32_t qf[8][2];
+    float o[8][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int64_t i = 0; i < nst; ++i) {
+        const int slot = static_cast<int>(i % STAGES);
+        if (!mbar_wait(bar0 + 8 * slot, (i / STAGES) & 1, deadline) || *abort_flag) {
+            if (lane == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+            return;
+        }
+        const int4 inf = info[slot];
+        const int b = inf.x, hg = inf.y, meta = inf.w;
+        const int nvalid = meta & 0xff;
+        const int hk = hg * HPC + warp;
+        if (meta & kFlagFirst) {
+            const bool live = g < G;
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+                q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G + (live ? g : 0)) * kFastHeadDim);
+#pragma unroll
+            for (int kc = 0; kc < 8; ++kc) {
+                qf[kc][0] = live ? __ldg(q32 + kc * 8 + t) : 0u;
+                qf[kc][1] = live ? __ldg(q32 + kc * 8 + 4 + t) : 0u;
+            }
+#pragma unroll
+            for (int dc = 0; dc < 8; ++dc)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[dc][e] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+        const uint32_t kt = tiles + slot * L::kStageBytes;
+        const uint32_t vt = kt + L::kTileBytes;
+        if (nvalid < kStageTokens) {
+            // Rows past the context (or of a skipped block) may hold anything,
+            // NaN included: zero this head's V rows so that 0 * row stays 0.
+            const int nbad = kStageTokens - nvalid;
+            for (int idx = lane; idx < nbad * 16; idx += 32) {
+                const int tok = nvalid + (idx >> 4);
+                const int half = (idx >> 3) & 1;
+                const int chunk = idx & 7;
+                const uint32_t addr = vt + head_off + (half * kStageTokens + tok) * 128 + chunk * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+            }
+            __syncwarp();
+        }
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+            uint32_t a[4];
+            ldsm_x4(kt + k_off[kc], a);
+            H::mma(sc, a, qf[kc][0], qf[kc][1]);
+        }
+        const bool vg = g < nvalid, vg8 = g + 8 < nvalid;
+        const float x0 = vg ? sc[0] * scale_log2 : -INFINITY;
+        const float x1 = vg ? sc[1] * scale_log2 : -INFINITY;
+        const float x2 = vg8 ? sc[2] * scale_log2 : -INFINITY;
+        const float x3 = vg8 ? sc[3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float p0 = fast_exp2(x0 - base0), p1 = fast_exp2(x1 - base1);
+        const float p2 = fast_exp2(x2 - base0), p3 = fast_exp2(x3 - base1);
+        const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 = l0 * a0 + (p0 + p2);
+        l1 = l1 * a1 + (p1 + p3);
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            o[dc][0] *= a0;
+            o[dc][1] *= a1;
+            o[dc][2] *= a0;
+            o[dc][3] *= a1;
+        }
+        const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+#pragma unroll
+        for (int dc = 0; dc < 8; ++dc) {
+            uint32_t a[4];
+            ldsm_x4_trans(vt + v_off[dc], a);
+            H::mma(o[dc], a, pb0, pb1);
+        }
+        if (nvalid < kStageTokens) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));
+
+        if (meta & kFlagLast) {
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+                l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+            }
+            const int hA = 2 * t, hB = 2 * t + 1;
+            if (meta & kFlagWhole) {
+                const int64_t qhead0 = static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G;
+                const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+                for (int dc = 0; dc < 8; ++dc) {
+                    const int d0 = dc * 16 + g;
+                    if (hA < G) {
+                        T *dst = out + (qhead0 + hA) * kFastHeadDim;
+                        dst[d0] = from_f32<T>(o[dc][0] * inv0);
+                        dst[d0 + 8] = from_f32<T>(o[dc][2] * inv0);
+                    }
+                    if (hB < G) {
+                        T *dst = out + (qhead0 + hB) * kFastHeadDim;
+                        dst[d0] = from_f32<T>(o[dc][1] * inv1);
+                        dst[d0 + 8] = from_f32<T>(o[dc][3] * inv1);
+                    }
+                }
+            } else {
+                const int64_t piece = (static_cast<int64_t>(b) * HG + hg + c) * HPC + warp;  // * G + head
+#pragma unroll
+                for (int dc = 0; dc < 8; ++dc) {
+                    const int d0 = dc * 16 + g;
+                    if (hA < G) {
+                        float *dst = o_piece + (piece * G + hA) * kFastHeadDim;
+                        dst[d0] = o[dc][0];
+                        dst[d0 + 8] = o[dc][2];
+                    }
+                    if (hB < G) {
+                        float *dst = o_piece + (piece * G + hB) * kFastHeadDim;
+                        dst[d0] = o[dc][1];
+                        dst[d0 + 8] = o[dc][3];
+                    }
+                }
+                if (g == 0) {
+                    if (hA < G) ml_piece[piece * G + hA] = make_float2(m0, l0);
+                    if (hB < G) ml_piece[piece * G + hB] = make_float2(m1, l1);
+                }
+            }
+        }
+    }
+}
+
+// Merges the pieces of every split unit.  One CTA per (query head of the unit,
+// unit): every warp derives the max and the weight sum over all pieces (lanes
+// over pieces), then accumulates its share of the pieces (k = warp, warp + 4,
+// ...) with lanes over the 128 dims as float4; the four partial sums meet in
+// shared memory.
+template <typename T>
+__global__ void __launch_bounds__(128)
+stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, const float2 *__restrict__ ml_piece,
+                      const int32_t *__restrict__ unit_first, const int32_t *__restrict__ unit_last,
+                      const int32_t *__restrict__ context_lens, int32_t Hq, int32_t HG, int32_t HU, int32_t bs,
+                      int32_t max_blocks, int32_t max_ctx, int32_t num_ctas) {
+    __shared__ float4 red[4][32];
+    pdl_wait();
+    pdl_trigger();
+    const int u = blockIdx.x, j = blockIdx.y;
+    const int b = u / HG, hg = u - b * HG;
+    const int ctx = context_lens[b];
+    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) return;
+    const int f = unit_first[u], l = unit_last[u];
+    if (f >= l) return;  // the whole unit sat in one CTA, which wrote the output
+    if (f < 0 || l >= num_ctas) return;  // only after an aborted main pass (PKV_ERRBIT_TIMEOUT is set)
+    const int np = l - f + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t first = (static_cast<int64_t>(u) + f) * HU + j;  // piece k at first + k * HU
+    float M = -INFINITY;
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, ml_piece[first + static_cast<int64_t>(k) * HU].x);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int k = lane; k < np; k += 32) {
+            const float2 v = ml_piece[first + static_cast<int64_t>(k) * HU];
+            Lsum += v.y * exp2f(v.x - M);
+        }
+        for (int k0 = warp; k0 < np; k0 += 4 * 4) {
+            float4 v[4];
+            float w[4];
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const int k = k0 + 4 * uu;
+                if (k < np) {
+                    const int64_t row = first + static_cast<int64_t>(k) * HU;
+                    w[uu] = exp2f(ml_piece[row].x - M);
+                    v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + row * kFastHeadDim) + lane);
+                } else {
+                    w[uu] = 0.f;
+                    v[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                acc.x = fmaf(w[uu], v[uu].x, acc.x);
+                acc.y = fmaf(w[uu], v[uu].y, acc.y);
+                acc.z = fmaf(w[uu], v[uu].z, acc.z);
+                acc.w = fmaf(w[uu], v[uu].w, acc.w);
+            }
+        }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, sh);
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = red[0][lane];
+#pragma unroll
+        for (int ww = 1; ww < 4; ++ww) {
+            t.x += red[ww][lane].x;
+            t.y += red[ww][lane].y;
+            t.z += red[ww][lane].z;
+            t.w += red[ww][lane].w;
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        T *dst = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * HU + j) * kFastHeadDim + 4 * lane;
+        dst[0] = from_f32<T>(t.x * inv);
+        dst[1] = from_f32<T>(t.y * inv);
+        dst[2] = from_f32<T>(t.z * inv);
+        dst[3] = from_f32<T>(t.w * inv);
+    }
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -752,9 +1224,90 @@ struct DecodeArgs {
     float scale;
     float *o_part;
     float2 *ml_part;
+    int32_t *unit_first, *unit_last;  // work-balanced schedule only
     int32_t *err;
     cudaStream_t stream;
 };
+
+// CTAs of the one-wave work-balanced grid on the current device:
+// (resident CTAs per SM) x (SMs), capped by the workspace bound.
+template <typename K>
+int stream_ctas(K kernel, int threads, int smem, std::atomic<int> *per_device) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int c = per_device[dev].load(std::memory_order_acquire);
+    if (c > 0) return c;
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    c = per_sm * sms;
+    if (c > kMaxStreamCtas) c = kMaxStreamCtas;
+    if (c > 0) per_device[dev].store(c, std::memory_order_release);
+    return c;
+}
+
+template <typename T, int HPC, int STAGES>
+struct StreamLaunch {
+    static std::atomic<int> ctas[64];
+    static std::atomic<uint64_t> configured;
+    static int grid() {
+        using L = StreamSmem<HPC, STAGES>;
+        if (ensure_smem(decode_stream_kernel<T, HPC, STAGES>, L::kAlloc, configured) != cudaSuccess) return 0;
+        return stream_ctas(decode_stream_kernel<T, HPC, STAGES>, (HPC + 1) * 32, L::kAlloc, ctas);
+    }
+};
+template <typename T, int HPC, int STAGES> std::atomic<int> StreamLaunch<T, HPC, STAGES>::ctas[64];
+template <typename T, int HPC, int STAGES> std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES>::configured{0};
+
+template <typename T, int HPC, int STAGES>
+pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
+    using L = StreamSmem<HPC, STAGES>;
+    CUtensorMap mk, mv;
+    pkv_status st = make_kv_map(&mk, a.k_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    if (st != PKV_OK) return st;
+    st = make_kv_map(&mv, a.v_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    if (st != PKV_OK) return st;
+    const int C = StreamLaunch<T, HPC, STAGES>::grid();
+    if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
+    const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
+    cudaError_t e = launch_pdl(decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
+                               a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
+                               a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
+                               a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_first, a.unit_last, a.err);
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    e = launch_pdl(stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G), dim3(128), 0, a.stream,
+                   static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
+                   static_cast<const float2 *>(a.ml_part), static_cast<const int32_t *>(a.unit_first),
+                   static_cast<const int32_t *>(a.unit_last), a.context_lens, a.Hq, HG, HPC * G, a.bs,
+                   a.max_blocks, a.max_ctx, C);
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+template <typename T>
+pkv_status launch_stream_any(const DecodeArgs &a, const Plan &p) {
+    switch (p.hpc) {
+    case 4: return launch_stream<T, 4, 3>(a, p);
+    case 2: return launch_stream<T, 2, 6>(a, p);
+    default: return launch_stream<T, 1, 8>(a, p);
+    }
+}
+
+int stream_grid_for(pkv_dtype dt, int hpc) {
+    if (dt == PKV_BF16) {
+        switch (hpc) {
+        case 4: return StreamLaunch<__nv_bfloat16, 4, 3>::grid();
+        case 2: return StreamLaunch<__nv_bfloat16, 2, 6>::grid();
+        default: return StreamLaunch<__nv_bfloat16, 1, 8>::grid();
+        }
+    }
+    switch (hpc) {
+    case 4: return StreamLaunch<__half, 4, 3>::grid();
+    case 2: return StreamLaunch<__half, 2, 6>::grid();
+    default: return StreamLaunch<__half, 1, 8>::grid();
+    }
+}
 
 template <typename T, int HPC, int STAGES>
 pkv_status launch_fast(const DecodeArgs &a, const Plan &p) {
@@ -770,11 +1323,10 @@ pkv_status launch_fast(const DecodeArgs &a, const Plan &p) {
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
     // At least one partition, so that zero-length contexts still get their zero rows.
     dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hkv / HPC, a.B);
-    kern<<<grid, (HPC + 1) * 32, L::kAlloc, a.stream>>>(
-        mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q), a.block_tables, a.max_blocks,
-        a.context_lens, a.Hq, a.Hq / a.Hkv, a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts,
-        a.scale * kLog2e, a.o_part, a.ml_part, a.err);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, grid, dim3((HPC + 1) * 32), L::kAlloc, a.stream, mk, mv, static_cast<T *>(a.out),
+                   static_cast<const T *>(a.q), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hq / a.Hkv,
+                   a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part, a.ml_part,
+                   a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
@@ -797,11 +1349,11 @@ pkv_status launch_generic_and_combine(const DecodeArgs &a, const Plan &p, bool r
         cudaError_t e = ensure_smem(kern, static_cast<int>(48 * 1024), configured);
         if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
         dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hq, a.B);
-        kern<<<grid, kGenThreads, smem, a.stream>>>(
-            static_cast<T *>(a.out), static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache),
-            static_cast<const T *>(a.v_cache), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hkv, a.d,
-            a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part, a.ml_part, a.err);
-        e = cudaGetLastError();
+        e = launch_pdl(kern, grid, dim3(kGenThreads), smem, a.stream, static_cast<T *>(a.out),
+                       static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache),
+                       static_cast<const T *>(a.v_cache), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hkv,
+                       a.d, a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part,
+                       a.ml_part, a.err);
         if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     }
     if (p.nparts > 1) {
@@ -837,7 +1389,7 @@ extern "C" pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t 
         return set_error(PKV_ERR_INVALID_ARG, "decode plan: bad sizes");
     Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
     if (partition_tokens) *partition_tokens = p.partition;
-    if (num_partitions) *num_partitions = p.nparts;
+    if (num_partitions) *num_partitions = p.stream ? stream_grid_for(dtype, p.hpc) : p.nparts;
     if (fast_path) *fast_path = p.fast ? 1 : 0;
     return ok();
 }
@@ -875,13 +1427,29 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
         return set_error(PKV_ERR_INVALID_ARG, "decode: buffers not aligned to the element size");
     // The fast path additionally wants 16-byte aligned pools (TMA) and 4-byte aligned q.
     const bool fast = p.fast && num_blocks > 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4);
+    if (p.fast && !fast) {
+        // CUDA-core fallback with partitions that fit the workspace sized for the fast plan.
+        const int64_t per_part = static_cast<int64_t>(num_seqs) * num_q_heads * (head_dim * 4 + 8);
+        const int64_t max_parts = p.ws_bytes > 512 ? (static_cast<int64_t>(p.ws_bytes) - 512) / per_part : 1;
+        p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype, true,
+                      max_parts > 0 ? max_parts : 1);
+        if (p.ws_bytes > workspace_bytes)
+            return set_error(PKV_ERR_WORKSPACE, "decode: unaligned pools need the CUDA-core path, whose partials "
+                                                "(%zu bytes) do not fit the workspace (%zu bytes)",
+                             p.ws_bytes, workspace_bytes);
+    }
+    char *ws = static_cast<char *>(workspace);
     DecodeArgs a{out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                  num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
-                 p.ws_bytes ? static_cast<float *>(workspace) : nullptr,
-                 p.ws_bytes ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.o_bytes) : nullptr,
+                 p.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr,
+                 p.ws_bytes ? reinterpret_cast<float2 *>(ws + p.o_bytes) : nullptr,
+                 p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes) : nullptr,
+                 p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes) + p.units : nullptr,
                  err_flag, static_cast<cudaStream_t>(stream)};
     pkv_status st;
-    if (fast) {
+    if (fast && p.stream) {
+        st = dtype == PKV_BF16 ? launch_stream_any<__nv_bfloat16>(a, p) : launch_stream_any<__half>(a, p);
+    } else if (fast) {
         st = dtype == PKV_BF16 ? launch_fast_any<__nv_bfloat16>(a, p) : launch_fast_any<__half>(a, p);
         if (st != PKV_OK) return st;
         st = dtype == PKV_BF16 ? launch_generic_and_combine<__nv_bfloat16>(a, p, false)

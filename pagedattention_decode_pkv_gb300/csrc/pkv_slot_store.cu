@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "pkv_internal.h"
+#include "pkv_pdl.cuh"
 
 namespace pkv {
 namespace {
@@ -27,6 +28,8 @@ slot_mapping_kernel(const int32_t *__restrict__ block_tables, int32_t max_blocks
                     const int32_t *__restrict__ cu_new, int32_t block_size, int32_t num_blocks,
                     int32_t *__restrict__ slot_mapping, int64_t num_new_tokens,
                     int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     const int32_t start = starts[b], end = ends[b];
     const int64_t out0 = cu_new[b], out1 = cu_new[b + 1];
@@ -76,6 +79,8 @@ store_kvcache_kernel(const char *__restrict__ key, const char *__restrict__ valu
                      char *__restrict__ k_cache, char *__restrict__ v_cache,
                      const int32_t *__restrict__ slot_mapping, int64_t num_tokens,
                      int64_t row_bytes, int64_t num_slots, int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
     using V = typename VecType<VEC>::T;
     constexpr int64_t kSeg = 32LL * kStoreUnroll * VEC;
     const int lane = threadIdx.x & 31;
@@ -149,10 +154,9 @@ extern "C" pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int3
     if (!starts || !ends || !cu_new || (max_blocks_per_seq > 0 && !block_tables) ||
         (num_new_tokens > 0 && !slot_mapping))
         return set_error(PKV_ERR_INVALID_ARG, "slot mapping: NULL pointer");
-    slot_mapping_kernel<<<num_seqs, kSlotThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        block_tables, max_blocks_per_seq, starts, ends, cu_new, block_size, num_blocks,
-        slot_mapping, num_new_tokens, err_flag);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(slot_mapping_kernel, dim3(num_seqs), dim3(kSlotThreads), 0,
+                               static_cast<cudaStream_t>(stream), block_tables, max_blocks_per_seq, starts, ends,
+                               cu_new, block_size, num_blocks, slot_mapping, num_new_tokens, err_flag);
     if (e != cudaSuccess)
         return set_error(PKV_ERR_CUDA, "slot mapping launch: %s", cudaGetErrorString(e));
     return ok();
@@ -190,13 +194,13 @@ extern "C" pkv_status pkv_store_kvcache(const void *key, const void *value, void
     auto vc = static_cast<char *>(v_cache);
     auto kk = static_cast<const char *>(key);
     auto vv = static_cast<const char *>(value);
+    cudaError_t e;
     switch (vec) {
-    case 16: store_kvcache_kernel<16><<<grid, kStoreThreads, 0, s>>>(kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    case 8: store_kvcache_kernel<8><<<grid, kStoreThreads, 0, s>>>(kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    case 4: store_kvcache_kernel<4><<<grid, kStoreThreads, 0, s>>>(kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    default: store_kvcache_kernel<2><<<grid, kStoreThreads, 0, s>>>(kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 16: e = launch_pdl(store_kvcache_kernel<16>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 8: e = launch_pdl(store_kvcache_kernel<8>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 4: e = launch_pdl(store_kvcache_kernel<4>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    default: e = launch_pdl(store_kvcache_kernel<2>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "store launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include "pkv_internal.h"
+#include "pkv_pdl.cuh"
 
 namespace pkv {
 namespace {
@@ -38,6 +39,8 @@ unpack_kernel(char *__restrict__ out, const char *__restrict__ pool,
               const int64_t *__restrict__ token_ptr, int64_t nnz, int32_t page_size,
               int64_t num_pages, int64_t row_bytes, int64_t total_tokens,
               int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
     using V = typename UVec<VEC>::T;
     const int s = blockIdx.y;
     const uint64_t lo = seq_ptr[s], hi = seq_ptr[s + 1];
@@ -93,13 +96,13 @@ cudaError_t launch_unpack(int vec, dim3 grid, cudaStream_t s, char *out, const c
                           int32_t *err) {
     auto b = static_cast<const IDX *>(bt);
     auto q = static_cast<const IDX *>(sp);
+    const dim3 block(kUnpackThreads);
     switch (vec) {
-    case 16: unpack_kernel<IDX, 16><<<grid, kUnpackThreads, 0, s>>>(out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err); break;
-    case 8: unpack_kernel<IDX, 8><<<grid, kUnpackThreads, 0, s>>>(out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err); break;
-    case 4: unpack_kernel<IDX, 4><<<grid, kUnpackThreads, 0, s>>>(out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err); break;
-    default: unpack_kernel<IDX, 2><<<grid, kUnpackThreads, 0, s>>>(out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err); break;
+    case 16: return launch_pdl(unpack_kernel<IDX, 16>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    case 8: return launch_pdl(unpack_kernel<IDX, 8>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    case 4: return launch_pdl(unpack_kernel<IDX, 4>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    default: return launch_pdl(unpack_kernel<IDX, 2>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

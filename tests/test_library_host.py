@@ -123,12 +123,17 @@ def test_decode_argument_errors_are_synchronous(pkv):
 
 
 def test_workspace_size_and_plan(pkv):
-    # one partition -> no workspace; long contexts -> partials for every (seq, head, partition)
-    assert pkv.pkv_paged_attention_decode_workspace_size(4, 8, 8, 128, 16, 100, torch.bfloat16) == 0
+    # CUDA-core path: one partition -> no workspace
+    assert pkv.pkv_paged_attention_decode_workspace_size(4, 8, 8, 64, 16, 100, torch.float32) == 0
+    # tensor-core path, work-balanced schedule (partition 0): room for one piece per (unit, CTA) boundary
     p, n, fast = pkv.pkv_paged_attention_decode_plan(8, 32, 8, 128, 16, 32768, torch.bfloat16)
-    assert fast and p % 16 == 0 and n == -(-32768 // p) and n > 1
+    assert fast and p == 0
     ws = pkv.pkv_paged_attention_decode_workspace_size(8, 32, 8, 128, 16, 32768, torch.bfloat16)
-    assert ws >= 8 * 32 * n * (128 * 4 + 8)
+    units, heads_per_unit = 8 * 2, 16
+    assert ws >= (units + 512) * heads_per_unit * (128 * 4 + 8) + 2 * units * 4
+    # more than 1024 sequences: tensor-core path with fixed partitions of the context
+    p, n, fast = pkv.pkv_paged_attention_decode_plan(2000, 32, 8, 128, 16, 32768, torch.bfloat16)
+    assert fast and p % 16 == 0 and p > 0 and n == -(-32768 // p)
     assert not pkv.pkv_paged_attention_decode_plan(2, 4, 2, 8, 4, 64, torch.float32)[2]   # CUDA-core path
     assert not pkv.pkv_paged_attention_decode_plan(2, 32, 2, 128, 16, 64, torch.bfloat16)[2]  # G = 16 > 8
     assert pkv.pkv_paged_attention_decode_workspace_size(2, 6, 4, 128, 16, 64, torch.bfloat16) == 0  # invalid
