@@ -708,7 +708,7 @@ cudaError_t launch_combine_dpl(T *out, const float *o_part, const float2 *ml, co
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(combine_kernel<T, DPL>, dim3(Hq, B), dim3(kCombineThreads), smem, s, out, o_part, ml, ctx, Hq,
+    return launch_pdl(kPdlCombine, combine_kernel<T, DPL>, dim3(Hq, B), dim3(kCombineThreads), smem, s, out, o_part, ml, ctx, Hq,
                       d, bs, max_blocks, max_ctx, partition, nparts);
 }
 
@@ -1271,12 +1271,12 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
     const int C = StreamLaunch<T, HPC, STAGES>::grid();
     if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
     const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
-    cudaError_t e = launch_pdl(decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
+    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
                                a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_first, a.unit_last, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    e = launch_pdl(stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G), dim3(128), 0, a.stream,
+    e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G), dim3(128), 0, a.stream,
                    static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
                    static_cast<const float2 *>(a.ml_part), static_cast<const int32_t *>(a.unit_first),
                    static_cast<const int32_t *>(a.unit_last), a.context_lens, a.Hq, HG, HPC * G, a.bs,
@@ -1323,7 +1323,7 @@ pkv_status launch_fast(const DecodeArgs &a, const Plan &p) {
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
     // At least one partition, so that zero-length contexts still get their zero rows.
     dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hkv / HPC, a.B);
-    e = launch_pdl(kern, grid, dim3((HPC + 1) * 32), L::kAlloc, a.stream, mk, mv, static_cast<T *>(a.out),
+    e = launch_pdl(kPdlDecode, kern, grid, dim3((HPC + 1) * 32), L::kAlloc, a.stream, mk, mv, static_cast<T *>(a.out),
                    static_cast<const T *>(a.q), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hq / a.Hkv,
                    a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part, a.ml_part,
                    a.err);
@@ -1349,7 +1349,7 @@ pkv_status launch_generic_and_combine(const DecodeArgs &a, const Plan &p, bool r
         cudaError_t e = ensure_smem(kern, static_cast<int>(48 * 1024), configured);
         if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: smem attribute: %s", cudaGetErrorString(e));
         dim3 grid(p.nparts > 0 ? p.nparts : 1, a.Hq, a.B);
-        e = launch_pdl(kern, grid, dim3(kGenThreads), smem, a.stream, static_cast<T *>(a.out),
+        e = launch_pdl(kPdlDecode, kern, grid, dim3(kGenThreads), smem, a.stream, static_cast<T *>(a.out),
                        static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache),
                        static_cast<const T *>(a.v_cache), a.block_tables, a.max_blocks, a.context_lens, a.Hq, a.Hkv,
                        a.d, a.bs, a.num_blocks, a.max_ctx, p.partition, p.nparts, a.scale * kLog2e, a.o_part,

@@ -18,9 +18,21 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Launch `kernel` on `stream` with programmatic stream serialization allowed.
+// Which launches allow programmatic dependent launch (the kernels always
+// execute pdl_wait(), which is a no-op without it).  Measured on GB300 over a
+// whole decode step (slot mapping, store, attention + combine, unpack K/V):
+// chaining everything but the unpack is fastest; letting the many-wave unpack
+// grid start early as well cost ~9 % of the step.
+constexpr bool kPdlSlotMapping = true;
+constexpr bool kPdlStore = true;
+constexpr bool kPdlDecode = true;
+constexpr bool kPdlCombine = true;
+constexpr bool kPdlUnpack = false;
+
+// Launch `kernel` on `stream`, with programmatic stream serialization allowed
+// when `pdl` is set.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -31,7 +43,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

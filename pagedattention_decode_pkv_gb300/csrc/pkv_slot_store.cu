@@ -154,7 +154,7 @@ extern "C" pkv_status pkv_compute_slot_mapping(const int32_t *block_tables, int3
     if (!starts || !ends || !cu_new || (max_blocks_per_seq > 0 && !block_tables) ||
         (num_new_tokens > 0 && !slot_mapping))
         return set_error(PKV_ERR_INVALID_ARG, "slot mapping: NULL pointer");
-    cudaError_t e = launch_pdl(slot_mapping_kernel, dim3(num_seqs), dim3(kSlotThreads), 0,
+    cudaError_t e = launch_pdl(kPdlSlotMapping, slot_mapping_kernel, dim3(num_seqs), dim3(kSlotThreads), 0,
                                static_cast<cudaStream_t>(stream), block_tables, max_blocks_per_seq, starts, ends,
                                cu_new, block_size, num_blocks, slot_mapping, num_new_tokens, err_flag);
     if (e != cudaSuccess)
@@ -196,10 +196,10 @@ extern "C" pkv_status pkv_store_kvcache(const void *key, const void *value, void
     auto vv = static_cast<const char *>(value);
     cudaError_t e;
     switch (vec) {
-    case 16: e = launch_pdl(store_kvcache_kernel<16>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    case 8: e = launch_pdl(store_kvcache_kernel<8>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    case 4: e = launch_pdl(store_kvcache_kernel<4>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
-    default: e = launch_pdl(store_kvcache_kernel<2>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 16: e = launch_pdl(kPdlStore, store_kvcache_kernel<16>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 8: e = launch_pdl(kPdlStore, store_kvcache_kernel<8>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    case 4: e = launch_pdl(kPdlStore, store_kvcache_kernel<4>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
+    default: e = launch_pdl(kPdlStore, store_kvcache_kernel<2>, dim3(grid), dim3(kStoreThreads), 0, s, kk, vv, kc, vc, slot_mapping, num_tokens, row_bytes, num_slots, err_flag); break;
     }
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "store launch: %s", cudaGetErrorString(e));
     return ok();

@@ -98,10 +98,10 @@ cudaError_t launch_unpack(int vec, dim3 grid, cudaStream_t s, char *out, const c
     auto q = static_cast<const IDX *>(sp);
     const dim3 block(kUnpackThreads);
     switch (vec) {
-    case 16: return launch_pdl(unpack_kernel<IDX, 16>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
-    case 8: return launch_pdl(unpack_kernel<IDX, 8>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
-    case 4: return launch_pdl(unpack_kernel<IDX, 4>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
-    default: return launch_pdl(unpack_kernel<IDX, 2>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    case 16: return launch_pdl(kPdlUnpack, unpack_kernel<IDX, 16>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    case 8: return launch_pdl(kPdlUnpack, unpack_kernel<IDX, 8>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    case 4: return launch_pdl(kPdlUnpack, unpack_kernel<IDX, 4>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
+    default: return launch_pdl(kPdlUnpack, unpack_kernel<IDX, 2>, grid, block, 0, s, out, pool, b, q, tp, nnz, ps, np, row_bytes, total, err);
     }
 }
 
