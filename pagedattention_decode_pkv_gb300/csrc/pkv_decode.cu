@@ -55,15 +55,19 @@ constexpr int kMaxStagesPerPartition = kMaxPartition / kStageTokens;
 constexpr int kTargetSms = 152;                  // GB300; fixed so the plan is device independent
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kCtaDeadlineNs = 2000000000ull;  // every wait of a CTA gives up 2 s after it started
-constexpr int kMaxStreamSeqs = 1024;   // work-balanced schedule: sequences per call (shared-memory bound)
+constexpr int kMaxStreamSeqs = 512;    // work-balanced schedule: sequences per call (shared-memory bound)
 constexpr int kMaxStreamCtas = 512;    // work-balanced schedule: CTAs per launch (sizes the workspace)
 constexpr int kMinStreamStages = 4;    // work-balanced schedule: fewest stages a working CTA streams
+constexpr int kChunkStages = 4;        // work-balanced schedule: dynamic-tail chunk (64 tokens)
+constexpr int kTailDenominator = 8;    // work-balanced schedule: the dynamic tail is 1/8 of the stages
 
 // ----------------------------------------------------------------------------- plan
 struct Plan {
     bool fast = false;
     bool stream = false;  // fast path with the work-balanced one-wave schedule
     int64_t units = 0;    // (sequence, head group) units of the work-balanced schedule
+    int64_t max_chunks = 0, max_segments = 0;  // dynamic-tail chunks / piece slots (bounds)
+    size_t unit_bytes = 0;
     int hpc = 1;          // KV heads per CTA (fast path)
     int stages = 2;       // pipeline depth (fast path)
     int partition = 16;   // tokens per partition
@@ -89,7 +93,7 @@ Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt,
     Plan p;
     const int G = Hq / Hkv;
     p.fast = !generic_only && (dt == PKV_F16 || dt == PKV_BF16) && d == kFastHeadDim && G >= 1 && G <= 8 &&
-             bs % kStageTokens == 0;
+             bs % kStageTokens == 0 && bs <= 32768;
     p.hpc = (Hkv % 4 == 0) ? 4 : (Hkv % 2 == 0) ? 2 : 1;
     const int stage_bytes = p.hpc * 2 * kStageTokens * kFastHeadDim * 2;
     p.stages = 98304 / stage_bytes;
@@ -97,13 +101,19 @@ Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt,
     if (p.stages < 2) p.stages = 2;
     p.stream = p.fast && B <= kMaxStreamSeqs;
     if (p.stream) {
-        // Pieces: at most one per (unit, CTA) boundary, i.e. units + CTAs.
+        // Pieces: at most one per (unit, segment) boundary; segments are the
+        // static slices (at most kMaxStreamCtas) and the dynamic-tail chunks.
         const int64_t HG = Hkv / p.hpc, HU = Hq / HG;
         p.units = static_cast<int64_t>(B) * HG;
-        const size_t pieces = static_cast<size_t>(p.units + kMaxStreamCtas);
+        const int64_t w_max = p.units * ((static_cast<int64_t>(max_ctx) + kStageTokens - 1) / kStageTokens);
+        p.max_chunks = w_max / kTailDenominator / kChunkStages + 1;
+        // static slots [0, kMaxStreamCtas + units), dynamic slots after them
+        p.max_segments = 2 * p.units + kMaxStreamCtas + p.max_chunks;  // piece slots
+        const size_t pieces = static_cast<size_t>(p.max_segments);
         p.o_bytes = (pieces * HU * d * sizeof(float) + 255) / 256 * 256;
         p.ml_bytes = (pieces * HU * sizeof(float2) + 255) / 256 * 256;
-        p.ws_bytes = p.o_bytes + p.ml_bytes + (2 * static_cast<size_t>(p.units) * sizeof(int32_t) + 255) / 256 * 256;
+        p.unit_bytes = (static_cast<size_t>(p.units) * sizeof(int4) + 255) / 256 * 256;
+        p.ws_bytes = p.o_bytes + p.ml_bytes + p.unit_bytes + 256;  // + Cw and the chunk counter
         p.partition = 0;
         p.nparts = 0;
         return p;
@@ -725,15 +735,22 @@ cudaError_t launch_combine(T *out, const float *o_part, const float2 *ml, const 
 
 // ----------------------------------------------------------------------------- work-balanced kernel
 // One wave of CTAs (every SM holds two).  The work of the launch is the
-// flattened list of 16-token stages over (sequence b, head group hg, stage st),
-// sequences in order, head groups in order, stages in order; CTA c streams the
-// contiguous slice [c*W/C, (c+1)*W/C) of that list, so every CTA moves the same
-// number of K/V bytes whatever the mix of context lengths.  A (b, hg) unit that
-// lies wholly inside one CTA is written straight to `out`; a unit split over
-// several CTAs leaves one unnormalised piece per CTA at piece index unit + c,
-// merged by stream_combine_kernel.  The producer warp maps stages to blocks 32
-// at a time, one chunk ahead of the TMA issue, and hands each stage's (b, hg,
-// position, valid rows, flags) to the consumers through shared memory.
+// flattened list of 16-token stages over (sequence b, head group hg, stage st):
+// sequences in order, head groups in order, stages in order; W stages in all.
+//  * Static part: the first 7/8 of the list is cut into equal contiguous
+//    slices, one per working CTA ("segment" c), so every CTA moves the same
+//    number of K/V bytes whatever the mix of context lengths.
+//  * Dynamic tail: the last 1/8 is cut into chunks of kChunkStages stages
+//    ("segment" C + k) that CTAs take from an atomic counter as they finish
+//    their slice.  SMs do not all get the same share of HBM bandwidth (the
+//    slow ones are the same from launch to launch), and the tail absorbs that.
+// A (b, hg) unit that lies wholly inside one segment is written straight to
+// `out`; a unit split over several segments leaves one unnormalised piece per
+// segment at slot (segment + unit), merged by stream_combine_kernel.  The
+// producer warp describes up to 32 stages at a time, one batch ahead of the
+// TMA issue (block-id loads and chunk grabs in flight meanwhile), and hands
+// each stage's (b, hg, valid rows, flags, segment) to the consumers through
+// shared memory.
 constexpr int kFlagFirst = 1 << 8;   // first stage of a piece: reset the running softmax
 constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
 constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
@@ -745,36 +762,44 @@ struct StreamSmem {
     static constexpr int kTilesBytes = STAGES * kStageBytes;
     static constexpr int kCtxOffset = kTilesBytes;                        // int32 effective ctx per sequence
     static constexpr int kPrefOffset = kCtxOffset + 4 * kMaxStreamSeqs;   // int64 stage prefix per sequence
-    static constexpr int kInfoOffset = kPrefOffset + 8 * (kMaxStreamSeqs + 16);
+    static constexpr int kSPrefOffset = kPrefOffset + 8 * (kMaxStreamSeqs + 16);  // int64 static-part prefix
+    static constexpr int kInfoOffset = kSPrefOffset + 8 * (kMaxStreamSeqs + 16);
     static constexpr int kBarOffset = kInfoOffset + 16 * STAGES;
     static constexpr int kFlagOffset = kBarOffset + 16 * STAGES;
     static constexpr int kBytes = kFlagOffset + 16;
     static constexpr int kAlloc = kBytes + 1024;
 };
 
-// Flattened stage s (< W) -> sequence b, head group hg, stage st of the sequence.
-__device__ __forceinline__ void locate_stage(const int64_t *pref, int B, int HG, int64_t s, int &b, int &hg,
-                                             int &st) {
-    int lo = 0, hi = B - 1;  // largest b with HG * pref[b] <= s (it has at least one stage)
+// Tail stages of a sequence with n stages: whole chunks, about 1/8 of n.
+__device__ __forceinline__ int64_t tail_stages(int64_t n) {
+    return n / kTailDenominator / kChunkStages * kChunkStages;
+}
+
+// Stage s (< HG * pre(B)) of a region whose per-sequence prefix is pre(b) ->
+// sequence b, head group hg, index st inside that sequence's part.
+template <typename Pre>
+__device__ __forceinline__ void locate_stage(Pre pre, int B, int HG, int64_t s, int &b, int &hg, int &st) {
+    int lo = 0, hi = B - 1;  // largest b with HG * pre(b) <= s (its part is not empty)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int64_t>(HG) * pref[mid] <= s) lo = mid; else hi = mid - 1;
+        if (static_cast<int64_t>(HG) * pre(mid) <= s) lo = mid; else hi = mid - 1;
     }
     b = lo;
-    const int64_t n = pref[b + 1] - pref[b];
-    const int64_t off = s - static_cast<int64_t>(HG) * pref[b];
+    const int64_t n = pre(b + 1) - pre(b);
+    const int64_t off = s - static_cast<int64_t>(HG) * pre(b);
     hg = static_cast<int>(off / n);
     st = static_cast<int>(off - hg * n);
 }
 
 template <typename T, int HPC, int STAGES>
-__global__ void __launch_bounds__((HPC + 1) * 32)
+__global__ void __launch_bounds__((HPC + 1) * 32, 2)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                      int32_t max_blocks, const int32_t *__restrict__ context_lens, int32_t B, int32_t Hq,
                      int32_t G, int32_t HG, int32_t bs, int32_t num_blocks, int32_t max_ctx, float scale_log2,
-                     float *__restrict__ o_piece, float2 *__restrict__ ml_piece, int32_t *__restrict__ unit_first,
-                     int32_t *__restrict__ unit_last, int32_t *__restrict__ err_flag) {
+                     float *__restrict__ o_piece, float2 *__restrict__ ml_piece, int4 *__restrict__ unit_info,
+                     int32_t *__restrict__ ws_meta, uint32_t *__restrict__ chunk_ctr,
+                     int32_t *__restrict__ err_flag) {
     using L = StreamSmem<HPC, STAGES>;
     using H = Half16<T>;
     const int c = blockIdx.x, C = gridDim.x;
@@ -783,10 +808,14 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t *cx = reinterpret_cast<int32_t *>(smem + L::kCtxOffset);
     int64_t *pref = reinterpret_cast<int64_t *>(smem + L::kPrefOffset);
+    int64_t *spref = reinterpret_cast<int64_t *>(smem + L::kSPrefOffset);
     int4 *info = reinterpret_cast<int4 *>(smem + L::kInfoOffset);
     const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlagOffset);
     const uint32_t tiles = smem_u32(smem);
+    auto pre_all = [&](int b) { return pref[b]; };
+    auto pre_static = [&](int b) { return spref[b]; };
+    auto pre_tail = [&](int b) { return pref[b] - spref[b]; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -797,42 +826,60 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
     pdl_wait();
     pdl_trigger();
-    if (threadIdx.x == 0)  // a broken pipeline elsewhere in the launch stops this CTA early
-        *abort_flag = (err_flag && (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT)) ? 1 : 0;
     const uint64_t deadline = global_ns() + kCtaDeadlineNs;
-
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int ctx = context_lens[b];
         cx[b] = context_ok(ctx, max_ctx, bs, max_blocks) ? ctx : 0;
     }
+    if (threadIdx.x == 0)  // a broken pipeline elsewhere in the launch stops this CTA early
+        *abort_flag = (err_flag && (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT)) ? 1 : 0;
     __syncthreads();
-    if (warp == 0) {  // exclusive prefix of stages per sequence
+    if (warp == 0) {  // exclusive prefixes of stages and of static-part stages per sequence
         const int chunk = (B + 31) / 32;
         const int lo = min(lane * chunk, B), hi = min(lo + chunk, B);
-        int64_t sum = 0;
-        for (int b = lo; b < hi; ++b) sum += (cx[b] + kStageTokens - 1) / kStageTokens;
-        int64_t incl = sum;
+        int64_t sum = 0, ssum = 0;
+        for (int b = lo; b < hi; ++b) {
+            const int64_t n = (cx[b] + kStageTokens - 1) / kStageTokens;
+            sum += n;
+            ssum += n - tail_stages(n);
+        }
+        int64_t incl = sum, sincl = ssum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int64_t sv = __shfl_up_sync(0xffffffffu, sincl, o);
+            if (lane >= o) {
+                incl += v;
+                sincl += sv;
+            }
         }
-        int64_t run = incl - sum;
+        int64_t run = incl - sum, srun = sincl - ssum;
         for (int b = lo; b < hi; ++b) {
             pref[b] = run;
-            run += (cx[b] + kStageTokens - 1) / kStageTokens;
+            spref[b] = srun;
+            const int64_t n = (cx[b] + kStageTokens - 1) / kStageTokens;
+            run += n;
+            srun += n - tail_stages(n);
         }
-        if (lane == 31) pref[B] = incl;
+        if (lane == 31) {
+            pref[B] = incl;
+            spref[B] = sincl;
+        }
     }
     __syncthreads();
     if (*abort_flag) return;
     const int64_t W = static_cast<int64_t>(HG) * pref[B];
-    // Working CTAs: at most one per kMinStreamStages stages, so every working CTA's
-    // slice is non-empty and each split unit's pieces come from consecutive CTAs.
-    int64_t Cw = W / kMinStreamStages;
+    const int64_t Wst = static_cast<int64_t>(HG) * spref[B];  // static region
+    const int64_t K = (W - Wst) / kChunkStages;                // dynamic chunks
+    const int64_t U = static_cast<int64_t>(B) * HG;
+    const int64_t dyn_base = kMaxStreamCtas + U;              // first dynamic piece slot
+    // Working CTAs of the static part: at most one per kMinStreamStages stages,
+    // so every static slice is non-empty.
+    int64_t Cw = Wst / kMinStreamStages;
     if (Cw > C) Cw = C;
-    if (Cw < 1) Cw = 1;
-    const int64_t s0 = c < Cw ? W * c / Cw : 0, s1 = c < Cw ? W * (c + 1) / Cw : 0;
+    if (Cw < 1) Cw = Wst > 0 ? 1 : 0;
+    const int64_t s0 = c < Cw ? Wst * c / Cw : 0, s1 = c < Cw ? Wst * (c + 1) / Cw : 0;
+    if (c == 0 && threadIdx.x == 0) ws_meta[0] = static_cast<int32_t>(Cw);
 
     // Sequences with nothing to stream (empty or invalid context) get zero rows
     // from CTA b mod C.
@@ -842,47 +889,102 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         T *o = out + static_cast<int64_t>(b) * Hq * kFastHeadDim;
         for (int i = threadIdx.x; i < Hq * kFastHeadDim; i += blockDim.x) o[i] = from_f32<T>(0.f);
     }
-    const int64_t nst = s1 - s0;
-    if (nst <= 0) return;
+    if (W == 0) return;
 
     if (warp == HPC) {
         // ------------------------------------------------------------ producer warp
+        // A batch = up to 32 consecutive stages [sb, se) of one segment [lo, hi).
         bool bad = false;
-        // Stage i of this CTA, described by lane i % 32 of the chunk that holds it.
-        auto describe = [&](int64_t i, int &b, int &hg, int &pos0, int &meta, int &id) {
-            b = hg = pos0 = meta = 0;
+        // Stage sb + lane of a batch [sb, se) that lies in segment [lo, hi) of
+        // the static region (seg = c) or of the dynamic region (seg = C + k).
+        auto describe = [&](int64_t sb, int64_t se, int64_t lo, int64_t hi, int seg, int &b, int &hg,
+                            int &meta, int &id, int &slot_of_piece) {
+            b = hg = meta = slot_of_piece = 0;
             id = -1;
-            if (i >= nst) return;
-            int st;
-            locate_stage(pref, B, HG, s0 + i, b, hg, st);
+            const int64_t sf = sb + lane;
+            if (sf >= se) return;
+            const bool dyn = seg >= C;
+            int sp;  // index inside the sequence's part
+            if (dyn) locate_stage(pre_tail, B, HG, sf, b, hg, sp);
+            else locate_stage(pre_static, B, HG, sf, b, hg, sp);
             const int ctx = cx[b];
-            const int n = (ctx + kStageTokens - 1) / kStageTokens;
-            pos0 = st * kStageTokens;
-            id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];
-            if (id < 0 || id >= num_blocks) {
-                id = -1;
-                bad = true;
-            }
-            int flags = 0;
-            if (i == 0 || st == 0) flags |= kFlagFirst;
-            if (i == nst - 1 || st == n - 1) flags |= kFlagLast;
-            const int64_t u0 = static_cast<int64_t>(HG) * pref[b] + static_cast<int64_t>(hg) * n;
-            if (u0 >= s0 && u0 + n <= s1) flags |= kFlagWhole;
-            meta = (id < 0 ? 0 : min(kStageTokens, ctx - pos0)) | flags;
+            const int64_t n = pref[b + 1] - pref[b];
+            const int64_t ns = spref[b + 1] - spref[b], nt = n - ns;
+            const int st = dyn ? static_cast<int>(ns) + sp : sp;  // stage inside the unit
+            const int pos0 = st * kStageTokens;
+            id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];  // checked when issued
             const int64_t u = static_cast<int64_t>(b) * HG + hg;
-            if (st == 0) unit_first[u] = c;
-            if (st == n - 1) unit_last[u] = c;
+            int flags = 0;
+            if (sf == lo || (!dyn && sp == 0)) flags |= kFlagFirst;
+            if (sf == hi - 1 || (!dyn && sp == ns - 1)) flags |= kFlagLast;
+            if (!dyn) {
+                const int64_t u0 = static_cast<int64_t>(HG) * spref[b] + static_cast<int64_t>(hg) * ns;
+                if (nt == 0 && u0 >= lo && u0 + ns <= hi) flags |= kFlagWhole;
+                slot_of_piece = static_cast<int>(seg + u);
+                if (sp == 0) unit_info[u].x = seg;
+                if (sp == ns - 1) {  // the unit's static part ends here: record its chunk range too
+                    const int64_t t0 = static_cast<int64_t>(HG) * pre_tail(b) + static_cast<int64_t>(hg) * nt;
+                    unit_info[u].y = seg;
+                    unit_info[u].z = static_cast<int>(t0 / kChunkStages);
+                    unit_info[u].w = static_cast<int>(nt / kChunkStages);
+                }
+            } else {
+                slot_of_piece = static_cast<int>(dyn_base + (seg - C) + u);
+            }
+            meta = min(kStageTokens, ctx - pos0) | flags | (pos0 % bs) << 16;
         };
-        int cb, chg, cpos, cmeta, cid, nb, nhg, npos, nmeta, nid;
-        describe(lane, cb, chg, cpos, cmeta, cid);
+        // batch bookkeeping (warp-uniform)
+        int64_t c_sb = 0, c_se = 0, c_lo = 0, c_hi = 0;
+        int c_seg = -1;
+        int cb = 0, chg = 0, cmeta = 0, cid = -1, cslot = 0;  // this lane's stage of the current batch
+        int64_t static_next = s0;                   // next static stage not yet batched
+        uint32_t k_reg = 0xffffffffu;               // lane 0: ticket of a grabbed chunk not yet batched
+        bool pending_valid = false;
+        // Grab the chunk after the next batch: a ticket from the counter (zeroed
+        // before the launch), read only at the next batch boundary.
+        auto prefetch_grab = [&]() {
+            if (static_next >= s1 && !pending_valid) {
+                if (lane == 0) k_reg = atomicAdd(chunk_ctr, 1u);
+                pending_valid = true;
+            }
+        };
+        // the next batch: static stages first, then dynamic chunks
+        auto next_batch = [&](int64_t &sb, int64_t &se, int64_t &lo, int64_t &hi, int &seg) -> bool {
+            if (static_next < s1) {
+                sb = static_next;
+                se = min(static_next + 32, s1);
+                lo = s0;
+                hi = s1;
+                seg = c;
+                static_next = se;
+                return true;
+            }
+            prefetch_grab();
+            const uint32_t k = __shfl_sync(0xffffffffu, k_reg, 0);
+            pending_valid = false;
+            if (k >= K) return false;
+            sb = static_cast<int64_t>(k) * kChunkStages;  // in the dynamic region
+            se = sb + kChunkStages;
+            lo = sb;
+            hi = se;
+            seg = C + static_cast<int>(k);
+            return true;
+        };
+        int64_t n_sb, n_se, n_lo, n_hi;
+        int n_seg;
+        bool have = next_batch(c_sb, c_se, c_lo, c_hi, c_seg);
+        if (have) describe(c_sb, c_se, c_lo, c_hi, c_seg, cb, chg, cmeta, cid, cslot);
         bool aborted = false;
         int64_t issued = 0;
-        const int64_t nchunks = (nst + 31) / 32;
-        for (int64_t k = 0; k < nchunks && !aborted; ++k) {
-            describe((k + 1) * 32 + lane, nb, nhg, npos, nmeta, nid);  // one chunk ahead
-            const int cnt = static_cast<int>(min(static_cast<int64_t>(32), nst - k * 32));
+        while (have && !aborted) {
+            // one batch ahead: describe the next batch (its block-id loads stay in flight)
+            int nb = 0, nhg = 0, nmeta = 0, nid = -1, nslot = 0;
+            const bool have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
+            if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
+            prefetch_grab();
+            const int cnt = static_cast<int>(c_se - c_sb);
             for (int j = 0; j < cnt; ++j) {
-                const int64_t i = k * 32 + j;
+                const int64_t i = issued;
                 const int slot = static_cast<int>(i % STAGES);
                 const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
                 int ok = 1;
@@ -893,12 +995,18 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     break;
                 }
                 const int b = __shfl_sync(0xffffffffu, cb, j), hg = __shfl_sync(0xffffffffu, chg, j);
-                const int pos0 = __shfl_sync(0xffffffffu, cpos, j), meta = __shfl_sync(0xffffffffu, cmeta, j);
-                const int id = __shfl_sync(0xffffffffu, cid, j);
+                int meta = __shfl_sync(0xffffffffu, cmeta, j);
+                int id = __shfl_sync(0xffffffffu, cid, j);
+                const int pslot = __shfl_sync(0xffffffffu, cslot, j);
                 if (lane == 0) {
-                    info[slot] = make_int4(b, hg, pos0, meta);
+                    if (id < 0 || id >= num_blocks) {  // skip the block: its rows count as masked
+                        id = -1;
+                        bad = true;
+                        meta &= ~0xff;
+                    }
+                    info[slot] = make_int4(b, hg, meta & 0xffff, pslot);
                     if (id >= 0) {
-                        const int slot_row = id * bs + pos0 % bs;
+                        const int slot_row = id * bs + (meta >> 16);
                         const uint32_t dst = tiles + slot * L::kStageBytes;
                         mbar_arrive_expect_tx(full, L::kStageBytes);
                         tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
@@ -910,17 +1018,32 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 issued = i + 1;
                 __syncwarp();
             }
-            cb = nb; chg = nhg; cpos = npos; cmeta = nmeta; cid = nid;
+            have = have_next;
+            c_sb = n_sb; c_se = n_se; c_lo = n_lo; c_hi = n_hi; c_seg = n_seg;
+            cb = nb; chg = nhg; cmeta = nmeta; cid = nid; cslot = nslot;
         }
         if (lane == 0) {
+            if (!aborted) {
+                // Tell the consumers there is no more work: a stage with b = -1.
+                // They consume every real stage before it, so every bulk copy has
+                // landed by the time they leave.
+                const int64_t i = issued;
+                const int slot = static_cast<int>(i % STAGES);
+                if (i < STAGES || mbar_wait(bar0 + 8 * (STAGES + slot), ((i / STAGES) - 1) & 1, deadline)) {
+                    info[slot] = make_int4(-1, 0, 0, 0);
+                    mbar_arrive(bar0 + 8 * slot);
+                } else {
+                    aborted = true;
+                }
+            }
             if (aborted) {
                 *abort_flag = 1;
                 if (err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+                // No bulk copy may still be writing shared memory when the CTA exits.
+                for (int64_t i = issued - STAGES > 0 ? issued - STAGES : 0; i < issued; ++i)
+                    if (!mbar_wait(bar0 + 8 * (i % STAGES), (i / STAGES) & 1, deadline) && err_flag)
+                        atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
             }
-            // No bulk copy may still be writing shared memory when the CTA exits.
-            for (int64_t i = issued - STAGES > 0 ? issued - STAGES : 0; i < issued; ++i)
-                if (!mbar_wait(bar0 + 8 * (i % STAGES), (i / STAGES) & 1, deadline) && err_flag)
-                    atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
         }
         if (bad && err_flag) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
         return;
@@ -945,27 +1068,40 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
     }
     uint32_t qf[8][2];
+    int q_b = -1, q_hg = -1;  // whose query heads qf holds
+    auto load_q = [&](int b, int hg) {
+        const int hk = hg * HPC + warp;
+        const bool live = g < G;
+        const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
+            q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G + (live ? g : 0)) * kFastHeadDim);
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+            qf[kc][0] = live ? __ldg(q32 + kc * 8 + t) : 0u;
+            qf[kc][1] = live ? __ldg(q32 + kc * 8 + 4 + t) : 0u;
+        }
+        q_b = b;
+        q_hg = hg;
+    };
+    if (s0 < s1) {  // the first stage of the static slice is known now: fetch its queries early
+        int b, hg, st;
+        locate_stage(pre_static, B, HG, s0, b, hg, st);
+        load_q(b, hg);
+    }
     float o[8][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    for (int64_t i = 0; i < nst; ++i) {
+    for (int64_t i = 0;; ++i) {
         const int slot = static_cast<int>(i % STAGES);
         if (!mbar_wait(bar0 + 8 * slot, (i / STAGES) & 1, deadline) || *abort_flag) {
             if (lane == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
             return;
         }
         const int4 inf = info[slot];
-        const int b = inf.x, hg = inf.y, meta = inf.w;
+        const int b = inf.x, hg = inf.y, meta = inf.z, pslot = inf.w;
+        if (b < 0) break;  // no more work
         const int nvalid = meta & 0xff;
         const int hk = hg * HPC + warp;
         if (meta & kFlagFirst) {
-            const bool live = g < G;
-            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
-                q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G + (live ? g : 0)) * kFastHeadDim);
-#pragma unroll
-            for (int kc = 0; kc < 8; ++kc) {
-                qf[kc][0] = live ? __ldg(q32 + kc * 8 + t) : 0u;
-                qf[kc][1] = live ? __ldg(q32 + kc * 8 + 4 + t) : 0u;
-            }
+            if (b != q_b || hg != q_hg) load_q(b, hg);
 #pragma unroll
             for (int dc = 0; dc < 8; ++dc)
 #pragma unroll
@@ -1060,7 +1196,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     }
                 }
             } else {
-                const int64_t piece = (static_cast<int64_t>(b) * HG + hg + c) * HPC + warp;  // * G + head
+                const int64_t piece = static_cast<int64_t>(pslot) * HPC + warp;  // * G + head
 #pragma unroll
                 for (int dc = 0; dc < 8; ++dc) {
                     const int d0 = dc * 16 + g;
@@ -1084,17 +1220,19 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
 }
 
-// Merges the pieces of every split unit.  One CTA per (query head of the unit,
-// unit): every warp derives the max and the weight sum over all pieces (lanes
-// over pieces), then accumulates its share of the pieces (k = warp, warp + 4,
-// ...) with lanes over the 128 dims as float4; the four partial sums meet in
+// Merges the pieces of every split unit.  One CTA per (unit, query head of the
+// unit).  unit_info[u] = (first static slice, last static slice, first chunk,
+// chunk count) gives the unit's pieces: slot (c + u) for its static slices and
+// (dyn_base + k + u) for its chunks.  Every warp derives the max and the weight
+// sum over all pieces (lanes over pieces), then accumulates its share of the
+// pieces with lanes over the 128 dims as float4; the four partial sums meet in
 // shared memory.
 template <typename T>
 __global__ void __launch_bounds__(128)
 stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, const float2 *__restrict__ ml_piece,
-                      const int32_t *__restrict__ unit_first, const int32_t *__restrict__ unit_last,
-                      const int32_t *__restrict__ context_lens, int32_t Hq, int32_t HG, int32_t HU, int32_t bs,
-                      int32_t max_blocks, int32_t max_ctx, int32_t num_ctas) {
+                      const int4 *__restrict__ unit_info, const int32_t *__restrict__ context_lens, int32_t Hq,
+                      int32_t HG, int32_t HU, int32_t bs, int32_t max_blocks, int32_t max_ctx, int32_t num_ctas,
+                      int64_t dyn_base, int64_t max_slots) {
     __shared__ float4 red[4][32];
     pdl_wait();
     pdl_trigger();
@@ -1102,31 +1240,36 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
     const int b = u / HG, hg = u - b * HG;
     const int ctx = context_lens[b];
     if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) return;
-    const int f = unit_first[u], l = unit_last[u];
-    if (f >= l) return;  // the whole unit sat in one CTA, which wrote the output
-    if (f < 0 || l >= num_ctas) return;  // only after an aborted main pass (PKV_ERRBIT_TIMEOUT is set)
-    const int np = l - f + 1;
+    const int4 ui = unit_info[u];
+    const int f = ui.x, l = ui.y, k0 = ui.z, nk = ui.w;
+    if (f == l && nk == 0) return;  // one piece: the main kernel wrote the output
+    // only after an aborted main pass (PKV_ERRBIT_TIMEOUT is set) can these fail
+    if (f < 0 || l < f || l >= num_ctas || k0 < 0 || nk < 0 || dyn_base + k0 + nk + u > max_slots) return;
+    const int n_static = l - f + 1;
+    const int np = n_static + nk;
+    auto slot_of = [&](int k) -> int64_t {
+        return k < n_static ? static_cast<int64_t>(f + k) + u : dyn_base + k0 + (k - n_static) + u;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t first = (static_cast<int64_t>(u) + f) * HU + j;  // piece k at first + k * HU
     float M = -INFINITY;
-    for (int k = lane; k < np; k += 32) M = fmaxf(M, ml_piece[first + static_cast<int64_t>(k) * HU].x);
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, ml_piece[slot_of(k) * HU + j].x);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
     float Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
         for (int k = lane; k < np; k += 32) {
-            const float2 v = ml_piece[first + static_cast<int64_t>(k) * HU];
+            const float2 v = ml_piece[slot_of(k) * HU + j];
             Lsum += v.y * exp2f(v.x - M);
         }
-        for (int k0 = warp; k0 < np; k0 += 4 * 4) {
+        for (int k0w = warp; k0w < np; k0w += 4 * 4) {
             float4 v[4];
             float w[4];
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu) {
-                const int k = k0 + 4 * uu;
+                const int k = k0w + 4 * uu;
                 if (k < np) {
-                    const int64_t row = first + static_cast<int64_t>(k) * HU;
+                    const int64_t row = slot_of(k) * HU + j;
                     w[uu] = exp2f(ml_piece[row].x - M);
                     v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + row * kFastHeadDim) + lane);
                 } else {
@@ -1148,20 +1291,20 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
     red[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {
-        float4 t = red[0][lane];
+        float4 tt = red[0][lane];
 #pragma unroll
         for (int ww = 1; ww < 4; ++ww) {
-            t.x += red[ww][lane].x;
-            t.y += red[ww][lane].y;
-            t.z += red[ww][lane].z;
-            t.w += red[ww][lane].w;
+            tt.x += red[ww][lane].x;
+            tt.y += red[ww][lane].y;
+            tt.z += red[ww][lane].z;
+            tt.w += red[ww][lane].w;
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         T *dst = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * HU + j) * kFastHeadDim + 4 * lane;
-        dst[0] = from_f32<T>(t.x * inv);
-        dst[1] = from_f32<T>(t.y * inv);
-        dst[2] = from_f32<T>(t.z * inv);
-        dst[3] = from_f32<T>(t.w * inv);
+        dst[0] = from_f32<T>(tt.x * inv);
+        dst[1] = from_f32<T>(tt.y * inv);
+        dst[2] = from_f32<T>(tt.z * inv);
+        dst[3] = from_f32<T>(tt.w * inv);
     }
 }
 
@@ -1224,7 +1367,9 @@ struct DecodeArgs {
     float scale;
     float *o_part;
     float2 *ml_part;
-    int32_t *unit_first, *unit_last;  // work-balanced schedule only
+    int4 *unit_info;  // work-balanced schedule only
+    int32_t *ws_meta;
+    uint32_t *chunk_ctr;
     int32_t *err;
     cudaStream_t stream;
 };
@@ -1271,16 +1416,19 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
     const int C = StreamLaunch<T, HPC, STAGES>::grid();
     if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
     const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
-    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
+    cudaError_t e = cudaMemsetAsync(a.chunk_ctr, 0, sizeof(uint32_t), a.stream);  // dynamic-tail tickets
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: counter reset: %s", cudaGetErrorString(e));
+    e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
                                a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
-                               a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_first, a.unit_last, a.err);
+                               a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
+                               a.chunk_ctr, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G), dim3(128), 0, a.stream,
                    static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
-                   static_cast<const float2 *>(a.ml_part), static_cast<const int32_t *>(a.unit_first),
-                   static_cast<const int32_t *>(a.unit_last), a.context_lens, a.Hq, HG, HPC * G, a.bs,
-                   a.max_blocks, a.max_ctx, C);
+                   static_cast<const float2 *>(a.ml_part), static_cast<const int4 *>(a.unit_info), a.context_lens,
+                   a.Hq, HG, HPC * G, a.bs, a.max_blocks, a.max_ctx, C,
+                   static_cast<int64_t>(kMaxStreamCtas + p.units), static_cast<int64_t>(p.max_segments));
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
@@ -1443,8 +1591,9 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
                  num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale,
                  p.ws_bytes ? reinterpret_cast<float *>(ws) : nullptr,
                  p.ws_bytes ? reinterpret_cast<float2 *>(ws + p.o_bytes) : nullptr,
-                 p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes) : nullptr,
-                 p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes) + p.units : nullptr,
+                 p.stream ? reinterpret_cast<int4 *>(ws + p.o_bytes + p.ml_bytes) : nullptr,
+                 p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes) : nullptr,
+                 p.stream ? reinterpret_cast<uint32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes + 8) : nullptr,
                  err_flag, static_cast<cudaStream_t>(stream)};
     pkv_status st;
     if (fast && p.stream) {
