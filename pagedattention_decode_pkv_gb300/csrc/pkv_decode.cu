@@ -60,6 +60,7 @@ constexpr int kMaxStreamCtas = 512;    // work-balanced schedule: CTAs per launc
 constexpr int kMinStreamStages = 4;    // work-balanced schedule: fewest stages a working CTA streams
 constexpr int kChunkStages = 4;        // work-balanced schedule: dynamic-tail chunk (64 tokens)
 constexpr int kTailDenominator = 8;    // work-balanced schedule: the dynamic tail is 1/8 of the stages
+constexpr int kGrabAhead = 2;          // work-balanced schedule: claim the next chunk this many stages early
 
 // ----------------------------------------------------------------------------- plan
 struct Plan {
@@ -543,6 +544,23 @@ decode_fast_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 // ----------------------------------------------------------------------------- generic kernel
 constexpr int kGenThreads = 128;
 
+template <int NWARPS>
+__device__ __forceinline__ float block_reduce_n(float v, float *scratch, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, sh);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = scratch[0];
+#pragma unroll
+    for (int w = 1; w < NWARPS; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
+    return v;
+}
+
 __device__ __forceinline__ float block_reduce(float v, float *scratch, bool is_max) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -826,6 +844,11 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
     pdl_wait();
     pdl_trigger();
+    // Chunk tickets start at 0.  Only CTA 0 resets the counter; a CTA that grabs
+    // before the reset can only cause chunks to be processed twice, which writes
+    // the same piece twice with identical values, and CTA 0 keeps grabbing after
+    // its reset until every chunk has been handed out again.
+    if (c == 0 && threadIdx.x == 0) atomicExch(chunk_ctr, 0u);
     const uint64_t deadline = global_ns() + kCtaDeadlineNs;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int ctx = context_lens[b];
@@ -938,17 +961,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         int c_seg = -1;
         int cb = 0, chg = 0, cmeta = 0, cid = -1, cslot = 0;  // this lane's stage of the current batch
         int64_t static_next = s0;                   // next static stage not yet batched
-        uint32_t k_reg = 0xffffffffu;               // lane 0: ticket of a grabbed chunk not yet batched
-        bool pending_valid = false;
-        // Grab the chunk after the next batch: a ticket from the counter (zeroed
-        // before the launch), read only at the next batch boundary.
-        auto prefetch_grab = [&]() {
-            if (static_next >= s1 && !pending_valid) {
-                if (lane == 0) k_reg = atomicAdd(chunk_ctr, 1u);
-                pending_valid = true;
-            }
-        };
-        // the next batch: static stages first, then dynamic chunks
+        // the next batch: static stages first, then chunks of the dynamic region
+        // (a ticket from the counter)
         auto next_batch = [&](int64_t &sb, int64_t &se, int64_t &lo, int64_t &hi, int &seg) -> bool {
             if (static_next < s1) {
                 sb = static_next;
@@ -959,9 +973,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 static_next = se;
                 return true;
             }
-            prefetch_grab();
-            const uint32_t k = __shfl_sync(0xffffffffu, k_reg, 0);
-            pending_valid = false;
+            uint32_t k = 0;
+            if (lane == 0) k = atomicAdd(chunk_ctr, 1u);
+            k = __shfl_sync(0xffffffffu, k, 0);
             if (k >= K) return false;
             sb = static_cast<int64_t>(k) * kChunkStages;  // in the dynamic region
             se = sb + kChunkStages;
@@ -970,20 +984,31 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             seg = C + static_cast<int>(k);
             return true;
         };
-        int64_t n_sb, n_se, n_lo, n_hi;
-        int n_seg;
+        int64_t n_sb = 0, n_se = 0, n_lo = 0, n_hi = 0;
+        int n_seg = 0;
         bool have = next_batch(c_sb, c_se, c_lo, c_hi, c_seg);
         if (have) describe(c_sb, c_se, c_lo, c_hi, c_seg, cb, chg, cmeta, cid, cslot);
         bool aborted = false;
         int64_t issued = 0;
         while (have && !aborted) {
-            // one batch ahead: describe the next batch (its block-id loads stay in flight)
+            // Static batches are described one batch ahead (their block-id loads
+            // stay in flight meanwhile); a dynamic chunk is claimed only when
+            // kGrabAhead stages of the current batch remain, so that chunks go to
+            // the CTAs that actually run out of work.
             int nb = 0, nhg = 0, nmeta = 0, nid = -1, nslot = 0;
-            const bool have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
-            if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
-            prefetch_grab();
+            bool have_next = false, decided = false;
+            if (static_next < s1) {
+                have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
+                describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
+                decided = true;
+            }
             const int cnt = static_cast<int>(c_se - c_sb);
             for (int j = 0; j < cnt; ++j) {
+                if (!decided && cnt - j <= kGrabAhead) {
+                    have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
+                    if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
+                    decided = true;
+                }
                 const int64_t i = issued;
                 const int slot = static_cast<int>(i % STAGES);
                 const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
@@ -1220,20 +1245,27 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
 }
 
-// Merges the pieces of every split unit.  One CTA per (unit, query head of the
-// unit).  unit_info[u] = (first static slice, last static slice, first chunk,
-// chunk count) gives the unit's pieces: slot (c + u) for its static slices and
-// (dyn_base + k + u) for its chunks.  Every warp derives the max and the weight
-// sum over all pieces (lanes over pieces), then accumulates its share of the
-// pieces with lanes over the 128 dims as float4; the four partial sums meet in
-// shared memory.
+// Merges the pieces of every split unit.  One CTA of 8 warps per (unit, query
+// head of the unit).  unit_info[u] = (first static slice, last static slice,
+// first chunk, chunk count) gives the unit's pieces: slot (c + u) for its
+// static slices and (dyn_base + k + u) for its chunks.  The (max, sum) pairs of
+// all pieces are read in one round (threads over pieces) and turned into
+// weights in shared memory; then warp w loads pieces w, w + 8, ... (lanes over
+// the 128 dims as float4), all of them in flight at once, and the eight partial
+// sums meet in shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeInFlight = 8;  // pieces per warp per round
+
 template <typename T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeThreads)
 stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, const float2 *__restrict__ ml_piece,
                       const int4 *__restrict__ unit_info, const int32_t *__restrict__ context_lens, int32_t Hq,
                       int32_t HG, int32_t HU, int32_t bs, int32_t max_blocks, int32_t max_ctx, int32_t num_ctas,
                       int64_t dyn_base, int64_t max_slots) {
-    __shared__ float4 red[4][32];
+    extern __shared__ float wsm[];                 // weight of every piece
+    __shared__ float4 red[kMergeWarps][32];
+    __shared__ float scratch[32];
     pdl_wait();
     pdl_trigger();
     const int u = blockIdx.x, j = blockIdx.y;
@@ -1247,53 +1279,51 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
     if (f < 0 || l < f || l >= num_ctas || k0 < 0 || nk < 0 || dyn_base + k0 + nk + u > max_slots) return;
     const int n_static = l - f + 1;
     const int np = n_static + nk;
-    auto slot_of = [&](int k) -> int64_t {
-        return k < n_static ? static_cast<int64_t>(f + k) + u : dyn_base + k0 + (k - n_static) + u;
+    auto row_of = [&](int k) -> int64_t {
+        const int64_t slot = k < n_static ? static_cast<int64_t>(f + k) + u : dyn_base + k0 + (k - n_static) + u;
+        return slot * HU + j;
     };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float M = -INFINITY;
-    for (int k = lane; k < np; k += 32) M = fmaxf(M, ml_piece[slot_of(k) * HU + j].x);
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+    for (int k = threadIdx.x; k < np; k += kMergeThreads) {
+        const float2 v = ml_piece[row_of(k)];
+        wsm[2 * k] = v.x;
+        wsm[2 * k + 1] = v.y;
+        M = fmaxf(M, v.x);
+    }
+    M = block_reduce_n<kMergeWarps>(M, scratch, true);
     float Lsum = 0.f;
+    for (int k = threadIdx.x; k < np; k += kMergeThreads) {
+        const float w = M == -INFINITY ? 0.f : exp2f(wsm[2 * k] - M);
+        Lsum += w * wsm[2 * k + 1];
+        wsm[2 * k] = w;
+    }
+    Lsum = block_reduce_n<kMergeWarps>(Lsum, scratch, false);  // its barriers also publish the weights
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int k = lane; k < np; k += 32) {
-            const float2 v = ml_piece[slot_of(k) * HU + j];
-            Lsum += v.y * exp2f(v.x - M);
+    for (int k0w = warp; k0w < np; k0w += kMergeWarps * kMergeInFlight) {
+        float4 v[kMergeInFlight];
+#pragma unroll
+        for (int uu = 0; uu < kMergeInFlight; ++uu) {
+            const int k = k0w + kMergeWarps * uu;
+            v[uu] = k < np ? __ldg(reinterpret_cast<const float4 *>(o_piece + row_of(k) * kFastHeadDim) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int k0w = warp; k0w < np; k0w += 4 * 4) {
-            float4 v[4];
-            float w[4];
 #pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                const int k = k0w + 4 * uu;
-                if (k < np) {
-                    const int64_t row = slot_of(k) * HU + j;
-                    w[uu] = exp2f(ml_piece[row].x - M);
-                    v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + row * kFastHeadDim) + lane);
-                } else {
-                    w[uu] = 0.f;
-                    v[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int uu = 0; uu < 4; ++uu) {
-                acc.x = fmaf(w[uu], v[uu].x, acc.x);
-                acc.y = fmaf(w[uu], v[uu].y, acc.y);
-                acc.z = fmaf(w[uu], v[uu].z, acc.z);
-                acc.w = fmaf(w[uu], v[uu].w, acc.w);
-            }
+        for (int uu = 0; uu < kMergeInFlight; ++uu) {
+            const int k = k0w + kMergeWarps * uu;
+            const float w = k < np ? wsm[2 * k] : 0.f;
+            acc.x = fmaf(w, v[uu].x, acc.x);
+            acc.y = fmaf(w, v[uu].y, acc.y);
+            acc.z = fmaf(w, v[uu].z, acc.z);
+            acc.w = fmaf(w, v[uu].w, acc.w);
         }
     }
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, sh);
     red[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {
         float4 tt = red[0][lane];
 #pragma unroll
-        for (int ww = 1; ww < 4; ++ww) {
+        for (int ww = 1; ww < kMergeWarps; ++ww) {
             tt.x += red[ww][lane].x;
             tt.y += red[ww][lane].y;
             tt.z += red[ww][lane].z;
@@ -1416,15 +1446,24 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
     const int C = StreamLaunch<T, HPC, STAGES>::grid();
     if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
     const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
-    cudaError_t e = cudaMemsetAsync(a.chunk_ctr, 0, sizeof(uint32_t), a.stream);  // dynamic-tail tickets
-    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode: counter reset: %s", cudaGetErrorString(e));
-    e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
+    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
                                a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
                                a.chunk_ctr, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G), dim3(128), 0, a.stream,
+    // weights smem: 2 floats per piece of one unit (at most kMaxStreamCtas slices
+    // plus the chunks of one unit's tail)
+    const int64_t unit_chunks = (static_cast<int64_t>(a.max_ctx) + kStageTokens - 1) / kStageTokens /
+                                kTailDenominator / kChunkStages + 1;
+    const size_t merge_smem = 2 * sizeof(float) * static_cast<size_t>(kMaxStreamCtas + unit_chunks);
+    if (merge_smem > 48 * 1024) {
+        static std::atomic<uint64_t> merge_cfg{0};
+        e = ensure_smem(stream_combine_kernel<T>, static_cast<int>(merge_smem), merge_cfg);
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine: smem attribute: %s", cudaGetErrorString(e));
+    }
+    e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G),
+                   dim3(kMergeThreads), merge_smem, a.stream,
                    static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
                    static_cast<const float2 *>(a.ml_part), static_cast<const int4 *>(a.unit_info), a.context_lens,
                    a.Hq, HG, HPC * G, a.bs, a.max_blocks, a.max_ctx, C,
