@@ -14,7 +14,9 @@ workload, through the C ABI (libpkv.so):
 the step (GB/s, inputs resident in HBM).  `e2e` is the same metric when
 every step also copies its per-step inputs from pinned host memory and reads
 the attention output back.  `roofline` is the decode-attention call
-(the dominant kernel) against the measured HBM copy bandwidth.
+(the dominant kernel), timed back to back as a decode loop issues it, against
+the measured HBM copy bandwidth; its per-call latency figure (one call between
+two events after an L2 eviction) is reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 For N > 1 launch under torch.distributed.run: every rank runs its own
@@ -269,11 +271,7 @@ class DecodeStep:
                                   c.num_kv_heads, c.head_dim, self.nb * c.block_size, self.dt, p(self.err),
                                   stream_ptr)
         rec(2)
-        ok |= L.pkv_paged_attention_decode(p(self.out), p(b.q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
-                                           b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads,
-                                           c.num_kv_heads, c.head_dim, c.block_size, self.nb, b.max_context_len,
-                                           b.scale, self.dt, p(self.workspace), self.workspace.numel(),
-                                           p(self.err), stream_ptr)
+        ok |= self.attention(stream_ptr)
         rec(3)
         s = self.snap
         for pool, dst in ((b.k_cache, self.unpacked_k), (b.v_cache, self.unpacked_v)):
@@ -283,6 +281,15 @@ class DecodeStep:
             rec(4 if dst is self.unpacked_k else 5)
         if ok != 0:
             raise RuntimeError("pkv call failed: " + L.pkv_last_error_string().decode())
+
+    def attention(self, stream_ptr) -> int:
+        """Enqueue the decode-attention call alone; returns its status."""
+        L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        return L.pkv_paged_attention_decode(p(self.out), p(b.q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
+                                            b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads,
+                                            c.num_kv_heads, c.head_dim, c.block_size, self.nb, b.max_context_len,
+                                            b.scale, self.dt, p(self.workspace), self.workspace.numel(),
+                                            p(self.err), stream_ptr)
 
     # per-step host inputs for the end-to-end measurement
     def host_inputs(self):
@@ -368,6 +375,38 @@ def time_kernels(step: DecodeStep, steps: int, world: int, stream):
         barrier(world)
     names = ["slot_mapping", "store_kvcache", "paged_attention_decode", "unpack_k", "unpack_v"]
     return {n: statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, n in enumerate(names)}
+
+
+ATTN_PER_GRAPH = 10
+
+
+def time_attention_sustained(step: DecodeStep, calls: int, world: int):
+    """Third pass: decode-attention calls back to back, as a decode loop issues
+    them, in CUDA graphs of ATTN_PER_GRAPH calls (launches chained by
+    programmatic dependent launch); `calls` calls (rounded up to whole graphs)
+    between two CUDA events.  Every bench workload reads more K/V per call than
+    the 129 MB L2 holds, and the K/V loads carry an evict-first L2 policy, so no
+    flush is needed.  Returns (ms per call, calls timed)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for _ in range(ATTN_PER_GRAPH):
+            if step.attention(ptr) != 0:
+                raise RuntimeError("pkv call failed: " + step.pkv._lib.pkv_last_error_string().decode())
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(1, (calls + ATTN_PER_GRAPH - 1) // ATTN_PER_GRAPH)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / (n * ATTN_PER_GRAPH), n * ATTN_PER_GRAPH
 
 
 def e2e_io(step: DecodeStep):
@@ -495,6 +534,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device error bits {err:#x} during the benchmark")
 
     per = time_kernels(step, args.steps, world, stream)
+    sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
     io, h2d, d2h = e2e_io(step)
     e2e_ms, _ = time_graphs(step, args.steps, world, io)
 
@@ -507,7 +547,9 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = measured_hbm_peak()
     attn_ms = per["paged_attention_decode"]
-    attn_gbs = step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9
+    attn_percall_gbs = step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9
+    sus_ms = reduce_max(sus_ms, world, device)
+    attn_gbs = step.bytes["paged_attention_decode"] / (sus_ms * 1e-3) / 1e9
     units = int(step.batch.context_lens.to(torch.int64).sum())  # tokens of context per launch
     traffic = profiled_traffic("paged_attention_decode", units)
     decode_ms = per["slot_mapping"] + per["store_kvcache"] + attn_ms
@@ -548,7 +590,11 @@ def run_ours(args, world, rank, local):
                      "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
                      "frac_of_8000_nominal": round(attn_gbs / 8000.0, 4),
-                     "traffic": None if traffic is None else round(traffic)},
+                     "traffic": None if traffic is None else round(traffic),
+                     "us_per_call": round(sus_ms * 1e3, 2), "calls_timed": sus_calls,
+                     "per_call_latency": {"us": round(attn_ms * 1e3, 2), "achieved": round(attn_percall_gbs, 1),
+                                          "frac": round(attn_percall_gbs / peak, 4),
+                                          "frac_of_8000_nominal": round(attn_percall_gbs / 8000.0, 4)}},
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
@@ -557,6 +603,10 @@ def run_ours(args, world, rank, local):
                             "launch) replayed until `steps` steps ran between two CUDA events",
                    "kernel_us": "second pass of `steps` eager steps with CUDA events between the kernels on the "
                                 "launching stream; a 512 MB read before each step (outside the events) evicts L2",
+                   "roofline": "third pass: `steps` decode-attention calls back to back in CUDA graphs of "
+                               f"{ATTN_PER_GRAPH} calls between two CUDA events (K/V read per call > L2; no flush); "
+                               "per_call_latency is the attention figure of the second pass (one call between "
+                               "two events after an L2 eviction, launch latency included)",
                    "e2e": "the same graphs with every step's pinned host->device input copies and the "
                           "device->host read of its attention output and error flag"},
         "clocks": clocks,

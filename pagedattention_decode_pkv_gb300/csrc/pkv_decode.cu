@@ -61,6 +61,7 @@ constexpr int kMinStreamStages = 4;    // work-balanced schedule: fewest stages 
 constexpr int kChunkStages = 4;        // work-balanced schedule: dynamic-tail chunk (64 tokens)
 constexpr int kTailDenominator = 8;    // work-balanced schedule: the dynamic tail is 1/8 of the stages
 constexpr int kGrabAhead = 2;          // work-balanced schedule: claim the next chunk this many stages early
+constexpr bool kKvEvictFirst = true;   // K/V tiles are read once: mark them first in line for L2 eviction
 
 // ----------------------------------------------------------------------------- plan
 struct Plan {
@@ -197,6 +198,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// The same load with an L2 eviction-priority policy (createpolicy) attached.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once: its lines are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -956,6 +974,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
             meta = min(kStageTokens, ctx - pos0) | flags | (pos0 % bs) << 16;
         };
+        const uint64_t kv_policy = l2_evict_first_policy();
         // batch bookkeeping (warp-uniform)
         int64_t c_sb = 0, c_se = 0, c_lo = 0, c_hi = 0;
         int c_seg = -1;
@@ -1034,8 +1053,13 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         const int slot_row = id * bs + (meta >> 16);
                         const uint32_t dst = tiles + slot * L::kStageBytes;
                         mbar_arrive_expect_tx(full, L::kStageBytes);
-                        tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
-                        tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full);
+                        if (kKvEvictFirst) {
+                            tma_load_3d_hint(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full, kv_policy);
+                            tma_load_3d_hint(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full, kv_policy);
+                        } else {
+                            tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
+                            tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full);
+                        }
                     } else {
                         mbar_arrive(full);  // nothing to load: the consumers mask the whole stage
                     }
@@ -1248,11 +1272,13 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 // Merges the pieces of every split unit.  One CTA of 8 warps per (unit, query
 // head of the unit).  unit_info[u] = (first static slice, last static slice,
 // first chunk, chunk count) gives the unit's pieces: slot (c + u) for its
-// static slices and (dyn_base + k + u) for its chunks.  The (max, sum) pairs of
-// all pieces are read in one round (threads over pieces) and turned into
-// weights in shared memory; then warp w loads pieces w, w + 8, ... (lanes over
-// the 128 dims as float4), all of them in flight at once, and the eight partial
-// sums meet in shared memory.
+// static slices and (dyn_base + k + u) for its chunks.  The kernel makes two
+// dependent rounds of loads: the unit's context length and unit_info, then
+// every piece's (max, sum) pair and output row at once.  Warp w folds pieces
+// w, w + 8, ... into a running (max, sum, row) of its own as they arrive (lanes
+// over the 128 dims as float4); the eight warps meet in shared memory.  The CTA
+// is small (4 KB of shared memory, 74 registers) so that it fits beside two
+// main-pass CTAs on an SM and is already resident when the main pass ends.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeInFlight = 8;  // pieces per warp per round
@@ -1263,16 +1289,15 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
                       const int4 *__restrict__ unit_info, const int32_t *__restrict__ context_lens, int32_t Hq,
                       int32_t HG, int32_t HU, int32_t bs, int32_t max_blocks, int32_t max_ctx, int32_t num_ctas,
                       int64_t dyn_base, int64_t max_slots) {
-    extern __shared__ float wsm[];                 // weight of every piece
     __shared__ float4 red[kMergeWarps][32];
-    __shared__ float scratch[32];
+    __shared__ float2 wml[kMergeWarps];
     pdl_wait();
     pdl_trigger();
     const int u = blockIdx.x, j = blockIdx.y;
     const int b = u / HG, hg = u - b * HG;
     const int ctx = context_lens[b];
-    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) return;
     const int4 ui = unit_info[u];
+    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) return;
     const int f = ui.x, l = ui.y, k0 = ui.z, nk = ui.w;
     if (f == l && nk == 0) return;  // one piece: the main kernel wrote the output
     // only after an aborted main pass (PKV_ERRBIT_TIMEOUT is set) can these fail
@@ -1284,52 +1309,65 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
         return slot * HU + j;
     };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float M = -INFINITY;
-    for (int k = threadIdx.x; k < np; k += kMergeThreads) {
-        const float2 v = ml_piece[row_of(k)];
-        wsm[2 * k] = v.x;
-        wsm[2 * k + 1] = v.y;
-        M = fmaxf(M, v.x);
-    }
-    M = block_reduce_n<kMergeWarps>(M, scratch, true);
-    float Lsum = 0.f;
-    for (int k = threadIdx.x; k < np; k += kMergeThreads) {
-        const float w = M == -INFINITY ? 0.f : exp2f(wsm[2 * k] - M);
-        Lsum += w * wsm[2 * k + 1];
-        wsm[2 * k] = w;
-    }
-    Lsum = block_reduce_n<kMergeWarps>(Lsum, scratch, false);  // its barriers also publish the weights
+    float m_w = -INFINITY, l_w = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0w = warp; k0w < np; k0w += kMergeWarps * kMergeInFlight) {
+    for (int kb = warp; kb < np; kb += kMergeWarps * kMergeInFlight) {
         float4 v[kMergeInFlight];
+        float2 ml[kMergeInFlight];
 #pragma unroll
         for (int uu = 0; uu < kMergeInFlight; ++uu) {
-            const int k = k0w + kMergeWarps * uu;
-            v[uu] = k < np ? __ldg(reinterpret_cast<const float4 *>(o_piece + row_of(k) * kFastHeadDim) + lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int k = kb + kMergeWarps * uu;
+            if (k < np) {
+                const int64_t row = row_of(k);
+                v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + row * kFastHeadDim) + lane);
+                ml[uu] = __ldg(ml_piece + row);
+            } else {
+                v[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+                ml[uu] = make_float2(-INFINITY, 0.f);
+            }
         }
+        float mn = m_w;
+#pragma unroll
+        for (int uu = 0; uu < kMergeInFlight; ++uu) mn = fmaxf(mn, ml[uu].x);
+        if (mn == -INFINITY) continue;  // nothing but empty pieces so far
+        const float sc = exp2f(m_w - mn);  // 0 while m_w is still -inf
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
+        l_w *= sc;
 #pragma unroll
         for (int uu = 0; uu < kMergeInFlight; ++uu) {
-            const int k = k0w + kMergeWarps * uu;
-            const float w = k < np ? wsm[2 * k] : 0.f;
+            const float w = exp2f(ml[uu].x - mn);  // 0 for an empty piece (max -inf)
             acc.x = fmaf(w, v[uu].x, acc.x);
             acc.y = fmaf(w, v[uu].y, acc.y);
             acc.z = fmaf(w, v[uu].z, acc.z);
             acc.w = fmaf(w, v[uu].w, acc.w);
+            l_w = fmaf(w, ml[uu].y, l_w);
         }
+        m_w = mn;
     }
     red[warp][lane] = acc;
+    if (lane == 0) wml[warp] = make_float2(m_w, l_w);
     __syncthreads();
     if (warp == 0) {
-        float4 tt = red[0][lane];
+        float M = -INFINITY;
 #pragma unroll
-        for (int ww = 1; ww < kMergeWarps; ++ww) {
-            tt.x += red[ww][lane].x;
-            tt.y += red[ww][lane].y;
-            tt.z += red[ww][lane].z;
-            tt.w += red[ww][lane].w;
+        for (int ww = 0; ww < kMergeWarps; ++ww) M = fmaxf(M, wml[ww].x);
+        float4 tt = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int ww = 0; ww < kMergeWarps; ++ww) {
+                const float w = exp2f(wml[ww].x - M);
+                tt.x = fmaf(w, red[ww][lane].x, tt.x);
+                tt.y = fmaf(w, red[ww][lane].y, tt.y);
+                tt.z = fmaf(w, red[ww][lane].z, tt.z);
+                tt.w = fmaf(w, red[ww][lane].w, tt.w);
+                L = fmaf(w, wml[ww].y, L);
+            }
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
         T *dst = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * HU + j) * kFastHeadDim + 4 * lane;
         dst[0] = from_f32<T>(tt.x * inv);
         dst[1] = from_f32<T>(tt.y * inv);
@@ -1452,18 +1490,8 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
                                a.chunk_ctr, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    // weights smem: 2 floats per piece of one unit (at most kMaxStreamCtas slices
-    // plus the chunks of one unit's tail)
-    const int64_t unit_chunks = (static_cast<int64_t>(a.max_ctx) + kStageTokens - 1) / kStageTokens /
-                                kTailDenominator / kChunkStages + 1;
-    const size_t merge_smem = 2 * sizeof(float) * static_cast<size_t>(kMaxStreamCtas + unit_chunks);
-    if (merge_smem > 48 * 1024) {
-        static std::atomic<uint64_t> merge_cfg{0};
-        e = ensure_smem(stream_combine_kernel<T>, static_cast<int>(merge_smem), merge_cfg);
-        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine: smem attribute: %s", cudaGetErrorString(e));
-    }
     e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G),
-                   dim3(kMergeThreads), merge_smem, a.stream,
+                   dim3(kMergeThreads), 0, a.stream,
                    static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
                    static_cast<const float2 *>(a.ml_part), static_cast<const int4 *>(a.unit_info), a.context_lens,
                    a.Hq, HG, HPC * G, a.bs, a.max_blocks, a.max_ctx, C,
