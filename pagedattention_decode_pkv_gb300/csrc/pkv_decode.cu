@@ -59,8 +59,8 @@ constexpr int kMaxStreamSeqs = 512;    // work-balanced schedule: sequences per 
 constexpr int kMaxStreamCtas = 512;    // work-balanced schedule: CTAs per launch (sizes the workspace)
 constexpr int kMinStreamStages = 4;    // work-balanced schedule: fewest stages a working CTA streams
 constexpr int kChunkStages = 4;        // work-balanced schedule: dynamic-tail chunk (64 tokens)
-constexpr int kTailDenominator = 8;    // work-balanced schedule: the dynamic tail is 1/8 of the stages
-constexpr int kGrabAhead = 2;          // work-balanced schedule: claim the next chunk this many stages early
+constexpr int kTailDenominator = 6;    // work-balanced schedule: the dynamic tail is 1/6 of the stages
+constexpr int kGrabAhead = 1;          // work-balanced schedule: claim the next chunk this many stages early
 constexpr bool kKvEvictFirst = true;   // K/V tiles are read once: mark them first in line for L2 eviction
 
 // ----------------------------------------------------------------------------- plan
@@ -773,20 +773,22 @@ cudaError_t launch_combine(T *out, const float *o_part, const float2 *ml, const 
 // One wave of CTAs (every SM holds two).  The work of the launch is the
 // flattened list of 16-token stages over (sequence b, head group hg, stage st):
 // sequences in order, head groups in order, stages in order; W stages in all.
-//  * Static part: the first 7/8 of the list is cut into equal contiguous
-//    slices, one per working CTA ("segment" c), so every CTA moves the same
-//    number of K/V bytes whatever the mix of context lengths.
-//  * Dynamic tail: the last 1/8 is cut into chunks of kChunkStages stages
-//    ("segment" C + k) that CTAs take from an atomic counter as they finish
-//    their slice.  SMs do not all get the same share of HBM bandwidth (the
-//    slow ones are the same from launch to launch), and the tail absorbs that.
-// A (b, hg) unit that lies wholly inside one segment is written straight to
-// `out`; a unit split over several segments leaves one unnormalised piece per
-// segment at slot (segment + unit), merged by stream_combine_kernel.  The
-// producer warp describes up to 32 stages at a time, one batch ahead of the
-// TMA issue (block-id loads and chunk grabs in flight meanwhile), and hands
-// each stage's (b, hg, valid rows, flags, segment) to the consumers through
-// shared memory.
+//  * Static part: every (b, hg) unit keeps about its last 1/kTailDenominator
+//    (whole chunks of kChunkStages stages) as a tail; the units' other stages,
+//    in order, are cut into equal contiguous slices, one per working CTA
+//    ("segment" c), so every CTA moves the same number of K/V bytes whatever
+//    the mix of context lengths.
+//  * Dynamic tail: the units' tails, in order, form a list of chunks
+//    ("segment" C + k) that CTAs claim from an atomic counter shortly before
+//    they run out of work.  SMs do not all get the same share of HBM bandwidth,
+//    and the chunks absorb that.
+// A unit that lies wholly inside one slice and has no tail is written straight
+// to `out`; otherwise every slice or chunk it touches leaves one unnormalised
+// piece, at slot (c + unit) for slice c and (kMaxStreamCtas + units + k + unit)
+// for chunk k, merged by stream_combine_kernel.  The producer warp describes up
+// to 32 stages at a time, one batch ahead of the TMA issue (block-id loads in
+// flight meanwhile), and hands each stage's (b, hg, valid rows, flags, piece
+// slot) to the consumers through shared memory.
 constexpr int kFlagFirst = 1 << 8;   // first stage of a piece: reset the running softmax
 constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
 constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
@@ -806,7 +808,7 @@ struct StreamSmem {
     static constexpr int kAlloc = kBytes + 1024;
 };
 
-// Tail stages of a sequence with n stages: whole chunks, about 1/8 of n.
+// Tail stages of a unit with n stages: whole chunks, about n / kTailDenominator.
 __device__ __forceinline__ int64_t tail_stages(int64_t n) {
     return n / kTailDenominator / kChunkStages * kChunkStages;
 }
@@ -868,6 +870,35 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // its reset until every chunk has been handed out again.
     if (c == 0 && threadIdx.x == 0) atomicExch(chunk_ctr, 0u);
     const uint64_t deadline = global_ns() + kCtaDeadlineNs;
+    // While the context lengths load, the producer guesses where its static
+    // slice starts if every sequence held max_ctx tokens and loads the block ids
+    // of that guess; describe() takes such an id when the real stage agrees
+    // (always, for equal-length batches), which saves one dependent global
+    // load before the first bulk copy.  The id is read from the same table
+    // entry either way.
+    int g_b = -1, g_hg = 0, g_st = 0, g_id = -1;
+    if (warp == HPC && max_ctx > 0) {
+        const int64_t n = (static_cast<int64_t>(max_ctx) + kStageTokens - 1) / kStageTokens;
+        const int64_t ns = n - tail_stages(n);
+        const int64_t wst = static_cast<int64_t>(HG) * B * ns;
+        int64_t cw = wst / kMinStreamStages;
+        if (cw > C) cw = C;
+        if (cw < 1) cw = 1;
+        if (c < cw) {
+            const int64_t sf = wst * c / cw + lane, se = wst * (c + 1) / cw;
+            if (sf < se) {
+                const int64_t unit = sf / ns;
+                const int st = static_cast<int>(sf - unit * ns);
+                const int blk = st * kStageTokens / bs;
+                if (blk < max_blocks) {
+                    g_b = static_cast<int>(unit / HG);
+                    g_hg = static_cast<int>(unit - static_cast<int64_t>(g_b) * HG);
+                    g_st = st;
+                    g_id = block_tables[static_cast<int64_t>(g_b) * max_blocks + blk];
+                }
+            }
+        }
+    }
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int ctx = context_lens[b];
         cx[b] = context_ok(ctx, max_ctx, bs, max_blocks) ? ctx : 0;
@@ -953,7 +984,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int64_t ns = spref[b + 1] - spref[b], nt = n - ns;
             const int st = dyn ? static_cast<int>(ns) + sp : sp;  // stage inside the unit
             const int pos0 = st * kStageTokens;
-            id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];  // checked when issued
+            if (b == g_b && hg == g_hg && st == g_st) id = g_id;  // the guess was right: same table entry
+            else id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];  // checked when issued
             const int64_t u = static_cast<int64_t>(b) * HG + hg;
             int flags = 0;
             if (sf == lo || (!dyn && sp == 0)) flags |= kFlagFirst;
@@ -1007,6 +1039,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         int n_seg = 0;
         bool have = next_batch(c_sb, c_se, c_lo, c_hi, c_seg);
         if (have) describe(c_sb, c_se, c_lo, c_hi, c_seg, cb, chg, cmeta, cid, cslot);
+        g_b = -1;  // the guess covers the first batch only
         bool aborted = false;
         int64_t issued = 0;
         while (have && !aborted) {
