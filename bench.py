@@ -291,6 +291,27 @@ class DecodeStep:
                                             b.scale, self.dt, p(self.workspace), self.workspace.numel(),
                                             p(self.err), stream_ptr)
 
+    def fused_step(self, stream_ptr) -> int:
+        """Enqueue the fused decode step (append the new K/V rows, then attend)."""
+        L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        return L.pkv_paged_attention_decode_append(p(self.out), p(b.q), p(b.new_key), p(b.new_value), p(b.k_cache),
+                                                   p(b.v_cache), p(b.block_tables), b.block_tables.shape[1],
+                                                   p(b.context_lens), self.B, c.num_q_heads, c.num_kv_heads,
+                                                   c.head_dim, c.block_size, self.nb, b.max_context_len, b.scale,
+                                                   self.dt, p(self.workspace), self.workspace.numel(), p(self.err),
+                                                   stream_ptr)
+
+    def separate_step(self, stream_ptr) -> int:
+        """Enqueue the same step as three calls: slot mapping, store, attention."""
+        L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        st = L.pkv_compute_slot_mapping(p(b.block_tables), b.block_tables.shape[1], p(b.starts), p(b.ends),
+                                        p(b.cu_new), self.B, c.block_size, self.nb, p(self.slots), self.B,
+                                        p(self.err), stream_ptr)
+        st |= L.pkv_store_kvcache(p(b.new_key), p(b.new_value), p(b.k_cache), p(b.v_cache), p(self.slots), self.B,
+                                  c.num_kv_heads, c.head_dim, self.nb * c.block_size, self.dt, p(self.err),
+                                  stream_ptr)
+        return st | self.attention(stream_ptr)
+
     # per-step host inputs for the end-to-end measurement
     def host_inputs(self):
         b, s = self.batch, self.snap
@@ -380,18 +401,20 @@ def time_kernels(step: DecodeStep, steps: int, world: int, stream):
 ATTN_PER_GRAPH = 10
 
 
-def time_attention_sustained(step: DecodeStep, calls: int, world: int):
+def time_attention_sustained(step: DecodeStep, calls: int, world: int, what=None):
     """Third pass: decode-attention calls back to back, as a decode loop issues
     them, in CUDA graphs of ATTN_PER_GRAPH calls (launches chained by
     programmatic dependent launch); `calls` calls (rounded up to whole graphs)
     between two CUDA events.  Every bench workload reads more K/V per call than
     the 129 MB L2 holds, and the K/V loads carry an evict-first L2 policy, so no
-    flush is needed.  Returns (ms per call, calls timed)."""
+    flush is needed.  `what` (default step.attention) enqueues one call.
+    Returns (ms per call, calls timed)."""
+    what = what or step.attention
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         for _ in range(ATTN_PER_GRAPH):
-            if step.attention(ptr) != 0:
+            if what(ptr) != 0:
                 raise RuntimeError("pkv call failed: " + step.pkv._lib.pkv_last_error_string().decode())
     for _ in range(2):
         g.replay()
@@ -535,6 +558,11 @@ def run_ours(args, world, rank, local):
 
     per = time_kernels(step, args.steps, world, stream)
     sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
+    fused_ms, _ = time_attention_sustained(step, args.steps, world, step.fused_step)
+    sep_ms, _ = time_attention_sustained(step, args.steps, world, step.separate_step)
+    fused_tok_s = reduce_sum(cfg.batch / (fused_ms * 1e-3), world, device)
+    fused_ms = reduce_max(fused_ms, world, device)
+    sep_ms = reduce_max(sep_ms, world, device)
     io, h2d, d2h = e2e_io(step)
     e2e_ms, _ = time_graphs(step, args.steps, world, io)
 
@@ -595,6 +623,14 @@ def run_ours(args, world, rank, local):
                      "per_call_latency": {"us": round(attn_ms * 1e3, 2), "achieved": round(attn_percall_gbs, 1),
                                           "frac": round(attn_percall_gbs / peak, 4),
                                           "frac_of_8000_nominal": round(attn_percall_gbs / 8000.0, 4)}},
+        "decode_step_fused": {
+            "what": "one decode step (append every sequence's new K/V row at position ctx-1, then attention over "
+                    "the whole context) back to back in CUDA graphs, as pkv_paged_attention_decode_append vs "
+                    "pkv_compute_slot_mapping + pkv_store_kvcache + pkv_paged_attention_decode",
+            "fused_us": round(fused_ms * 1e3, 2),
+            "separate_us": round(sep_ms * 1e3, 2),
+            "fused_tokens_per_s": round(fused_tok_s, 1),
+            "fused_kv_gbs": round(step.bytes["paged_attention_decode"] / (fused_ms * 1e-3) / 1e9, 1)},
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},

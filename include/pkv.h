@@ -155,6 +155,42 @@ PKV_API pkv_status pkv_paged_attention_decode(void *out, const void *q, const vo
                                       void *workspace, size_t workspace_bytes,
                                       int32_t *err_flag, void *stream);
 
+/*
+ * pkv_paged_attention_decode_append -- one decode step of the pages'
+ * "Walk the Shapes First" trace in one call: every sequence's new token sits
+ * at position context_lens[b] - 1 (context_lens counts it), its K/V rows are
+ * written to the paged caches at that position's slot
+ * (block_tables[b][p / block_size] * block_size + p % block_size, as in
+ * "Step 1: slot_mapping and store_kvcache"), and then the attention of
+ * pkv_paged_attention_decode runs over the whole context, the new token
+ * included ("Step 2: paged_attention_decode").  The result equals
+ * pkv_compute_slot_mapping over [ctx - 1, ctx) + pkv_store_kvcache +
+ * pkv_paged_attention_decode with the same arguments.
+ *
+ *   key, value       device [num_seqs, num_kv_heads, head_dim]: the new token's
+ *                    K/V rows (dtype), read only
+ *   k_cache, v_cache modified in place (one row per sequence)
+ *   all other arguments, the workspace and the output as in
+ *                    pkv_paged_attention_decode.
+ * On the tensor-core path with the work-balanced schedule (at most 512
+ * sequences) and 8-byte aligned key/value, the rows are written by the
+ * attention kernel itself right before it reads that block; otherwise a
+ * separate append kernel runs first on the same stream.
+ * Device errors: a sequence whose context length is invalid (see
+ * pkv_paged_attention_decode) is neither appended nor attended
+ * (PKV_ERRBIT_CONTEXT, zero row); a block id outside [0, num_blocks) at
+ * position ctx - 1 skips the append and sets PKV_ERRBIT_BLOCK_RANGE.
+ */
+PKV_API pkv_status pkv_paged_attention_decode_append(void *out, const void *q, const void *key,
+                                             const void *value, void *k_cache, void *v_cache,
+                                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t *context_lens, int32_t num_seqs,
+                                             int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                             int32_t max_context_len, float scale, pkv_dtype dtype,
+                                             void *workspace, size_t workspace_bytes,
+                                             int32_t *err_flag, void *stream);
+
 /* Workspace bytes pkv_paged_attention_decode needs for these sizes (0 is a
  * valid answer).  Pure host arithmetic; never fails (returns 0 on bad sizes,
  * which the decode call then rejects). */

@@ -139,6 +139,24 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     return out, err
 
 
+def decode_step(q, key, value, k_cache, v_cache, block_tables, context_lens, scale: float):
+    """One decode step as the walk in "Walk the Shapes First" runs it: the new
+    token of sequence b sits at position context_lens[b] - 1, its slot comes
+    from compute_slot_mapping over [ctx - 1, ctx), store_kvcache writes key[b]
+    and value[b] there, and paged_attention_decode attends over the whole
+    context.  Sequences with an empty context append nothing.  Returns
+    (binary64 output, k_cache, v_cache, error count) with CPU copies of the
+    caches."""
+    cl = _cpu(context_lens, torch.int32)
+    keep = (cl > 0).nonzero().reshape(-1)
+    bt = _cpu(block_tables, torch.int32)
+    nb = _cpu(k_cache).shape[0]
+    slots, e1 = compute_slot_mapping(bt[keep], cl[keep] - 1, cl[keep], _cpu(k_cache).shape[1], nb)
+    kc, vc, e2 = store_kvcache(_cpu(key)[keep], _cpu(value)[keep], k_cache, v_cache, slots)
+    out, e3 = paged_attention_decode(q, kc, vc, bt, cl, scale)
+    return out, kc, vc, e1 + e2 + e3
+
+
 def validate_index_buffers(seq_ptr, block_table, num_pages: int, index_dtype=torch.int64) -> int:
     """0 when p1's four storage invariants hold, else the first broken one (1..4)."""
     is_u64 = index_dtype in (torch.int64, torch.uint64)

@@ -44,6 +44,8 @@ _SIGS = {
     "pkv_store_kvcache": ([_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_paged_attention_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
+    "pkv_paged_attention_decode_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
     "pkv_paged_attention_decode_static_ws": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                               _i32, _i32, _f32, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_paged_attention_decode_workspace_size": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int], _sz),
@@ -164,7 +166,30 @@ def pkv_paged_attention_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_di
 def pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                max_context_len: int, *, out=None, workspace=None, err_flag=None, stream=None):
     """out[b, h] = softmax(scale * q[b, h] . K^T) V over the sequence's paged context."""
-    dev = _dev(q, k_cache, v_cache, block_tables, context_lens, out, workspace, err_flag)
+    return _decode(q, None, None, k_cache, v_cache, block_tables, context_lens, scale, max_context_len, out,
+                   workspace, err_flag, stream)
+
+
+def pkv_paged_attention_decode_append(q, key, value, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                      max_context_len: int, *, out=None, workspace=None, err_flag=None,
+                                      stream=None):
+    """One decode step: key[b] / value[b] go to the cache row of position
+    context_lens[b] - 1, then the attention of pkv_paged_attention_decode runs
+    over the whole context (new token included)."""
+    return _decode(q, key, value, k_cache, v_cache, block_tables, context_lens, scale, max_context_len, out,
+                   workspace, err_flag, stream)
+
+
+def _decode(q, key, value, k_cache, v_cache, block_tables, context_lens, scale, max_context_len, out, workspace,
+            err_flag, stream):
+    dev = _dev(q, key, value, k_cache, v_cache, block_tables, context_lens, out, workspace, err_flag)
+    if (key is None) != (value is None):
+        raise ValueError("key and value go together")
+    if key is not None:
+        if key.dtype != q.dtype or value.dtype != q.dtype or key.shape != value.shape or \
+                key.shape != (q.shape[0], k_cache.shape[2], q.shape[2]) or not key.is_contiguous() or \
+                not value.is_contiguous():
+            raise ValueError("key, value: contiguous [num_seqs, num_kv_heads, head_dim] of the cache dtype")
     _want(block_tables, torch.int32, "block_tables")
     _want(context_lens, torch.int32, "context_lens")
     if q.dtype not in _DTYPE or not (q.dtype == k_cache.dtype == v_cache.dtype):
@@ -180,12 +205,19 @@ def pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, 
     ws = pkv_paged_attention_decode_workspace_size(B, Hq, Hkv, d, bs, max_context_len, q.dtype) if B else 0
     if ws and workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    wsp = _ptr(workspace) if ws else None
+    wsn = workspace.numel() * workspace.element_size() if ws else 0
     with torch.cuda.device(dev):
-        _check(_lib.pkv_paged_attention_decode(
-            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
-            _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale), _DTYPE[q.dtype],
-            _ptr(workspace) if ws else None, workspace.numel() * workspace.element_size() if ws else 0,
-            _ptr(err_flag), _stream(dev, stream)))
+        if key is None:
+            _check(_lib.pkv_paged_attention_decode(
+                _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale), _DTYPE[q.dtype],
+                wsp, wsn, _ptr(err_flag), _stream(dev, stream)))
+        else:
+            _check(_lib.pkv_paged_attention_decode_append(
+                _ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale),
+                _DTYPE[q.dtype], wsp, wsn, _ptr(err_flag), _stream(dev, stream)))
     return out
 
 

@@ -792,6 +792,7 @@ cudaError_t launch_combine(T *out, const float *o_part, const float2 *ml, const 
 constexpr int kFlagFirst = 1 << 8;   // first stage of a piece: reset the running softmax
 constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
 constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
+constexpr int kFlagAppend = 1 << 11; // the stage holds the step's new token: append its K/V first
 
 template <int HPC, int STAGES>
 struct StreamSmem {
@@ -837,6 +838,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      int32_t G, int32_t HG, int32_t bs, int32_t num_blocks, int32_t max_ctx, float scale_log2,
                      float *__restrict__ o_piece, float2 *__restrict__ ml_piece, int4 *__restrict__ unit_info,
                      int32_t *__restrict__ ws_meta, uint32_t *__restrict__ chunk_ctr,
+                     const T *__restrict__ new_k, const T *__restrict__ new_v, T *k_cache_w, T *v_cache_w,
                      int32_t *__restrict__ err_flag) {
     using L = StreamSmem<HPC, STAGES>;
     using H = Half16<T>;
@@ -1004,6 +1006,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             } else {
                 slot_of_piece = static_cast<int>(dyn_base + (seg - C) + u);
             }
+            if (new_k && st == n - 1) flags |= kFlagAppend;  // position ctx - 1 is in this stage
             meta = min(kStageTokens, ctx - pos0) | flags | (pos0 % bs) << 16;
         };
         const uint64_t kv_policy = l2_evict_first_policy();
@@ -1064,6 +1067,36 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const int64_t i = issued;
                 const int slot = static_cast<int>(i % STAGES);
                 const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
+                const int b = __shfl_sync(0xffffffffu, cb, j), hg = __shfl_sync(0xffffffffu, chg, j);
+                int meta = __shfl_sync(0xffffffffu, cmeta, j);
+                int id = __shfl_sync(0xffffffffu, cid, j);
+                const int pslot = __shfl_sync(0xffffffffu, cslot, j);
+                if ((meta & kFlagAppend) && id >= 0 && id < num_blocks) {
+                    // Append: the step's new K/V rows of these HPC heads go to the
+                    // cache row of position ctx - 1 before the bulk copy reads it
+                    // back (the generic-proxy stores are ordered before the
+                    // async-proxy load by fence.proxy.async).
+                    const int64_t row = static_cast<int64_t>(id) * bs + (meta >> 16) + ((meta & 0xff) - 1);
+                    const int64_t src = (static_cast<int64_t>(b) * HG + hg) * HPC * kFastHeadDim;
+                    const int64_t dst = (row * HG + hg) * HPC * kFastHeadDim;
+                    const int2 *sk = reinterpret_cast<const int2 *>(new_k + src);
+                    const int2 *sv = reinterpret_cast<const int2 *>(new_v + src);
+                    int2 *dk = reinterpret_cast<int2 *>(k_cache_w + dst);
+                    int2 *dv = reinterpret_cast<int2 *>(v_cache_w + dst);
+                    int2 tk[HPC], tv[HPC];  // HPC heads x 256 bytes = HPC x 32 lanes x 8 bytes
+#pragma unroll
+                    for (int e = 0; e < HPC; ++e) {
+                        tk[e] = __ldg(sk + e * 32 + lane);
+                        tv[e] = __ldg(sv + e * 32 + lane);
+                    }
+#pragma unroll
+                    for (int e = 0; e < HPC; ++e) {
+                        dk[e * 32 + lane] = tk[e];
+                        dv[e * 32 + lane] = tv[e];
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __syncwarp();
+                }
                 int ok = 1;
                 if (lane == 0 && i >= STAGES) ok = mbar_wait(empty, ((i / STAGES) - 1) & 1, deadline) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1071,10 +1104,6 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     aborted = true;
                     break;
                 }
-                const int b = __shfl_sync(0xffffffffu, cb, j), hg = __shfl_sync(0xffffffffu, chg, j);
-                int meta = __shfl_sync(0xffffffffu, cmeta, j);
-                int id = __shfl_sync(0xffffffffu, cid, j);
-                const int pslot = __shfl_sync(0xffffffffu, cslot, j);
                 if (lane == 0) {
                     if (id < 0 || id >= num_blocks) {  // skip the block: its rows count as masked
                         id = -1;
@@ -1409,6 +1438,60 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
     }
 }
 
+// ----------------------------------------------------------------------------- append (other paths)
+// The step's new K/V rows for the paths that do not append inside the
+// attention kernel: row ctx - 1 of every sequence with a valid, non-empty
+// context receives key[b] / value[b] (the slot rule of "Step 1: slot_mapping
+// and store_kvcache").  One warp per (sequence, segment of 32 x 4 vectors).
+constexpr int kAppendThreads = 256;
+
+template <typename V>
+__global__ void __launch_bounds__(kAppendThreads)
+append_kv_kernel(const char *__restrict__ key, const char *__restrict__ value, char *__restrict__ k_cache,
+                 char *__restrict__ v_cache, const int32_t *__restrict__ block_tables, int32_t max_blocks,
+                 const int32_t *__restrict__ context_lens, int32_t B, int32_t bs, int32_t num_blocks,
+                 int32_t max_ctx, int64_t row_bytes, int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int64_t kSeg = 32 * 4 * static_cast<int64_t>(sizeof(V));
+    const int lane = threadIdx.x & 31;
+    const int64_t nseg = (row_bytes + kSeg - 1) / kSeg;
+    const int64_t items = static_cast<int64_t>(B) * nseg;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kAppendThreads / 32);
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * (kAppendThreads / 32) + (threadIdx.x >> 5); it < items;
+         it += warps) {
+        const int b = static_cast<int>(it / nseg);
+        const int64_t seg = it - static_cast<int64_t>(b) * nseg;
+        const int ctx = context_lens[b];
+        if (ctx <= 0 || !context_ok(ctx, max_ctx, bs, max_blocks)) continue;  // the attention flags it
+        const int p = ctx - 1;
+        const int32_t blk = block_tables[static_cast<int64_t>(b) * max_blocks + p / bs];
+        if (blk < 0 || blk >= num_blocks) {
+            if (lane == 0 && seg == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
+            continue;
+        }
+        const int64_t src = static_cast<int64_t>(b) * row_bytes + seg * kSeg;
+        const int64_t dst = (static_cast<int64_t>(blk) * bs + p % bs) * row_bytes + seg * kSeg;
+        V kv[4], vv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t off = (static_cast<int64_t>(u) * 32 + lane) * static_cast<int64_t>(sizeof(V));
+            if (seg * kSeg + off < row_bytes) {
+                kv[u] = *reinterpret_cast<const V *>(key + src + off);
+                vv[u] = *reinterpret_cast<const V *>(value + src + off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t off = (static_cast<int64_t>(u) * 32 + lane) * static_cast<int64_t>(sizeof(V));
+            if (seg * kSeg + off < row_bytes) {
+                *reinterpret_cast<V *>(k_cache + dst + off) = kv[u];
+                *reinterpret_cast<V *>(v_cache + dst + off) = vv[u];
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1471,9 +1554,38 @@ struct DecodeArgs {
     int4 *unit_info;  // work-balanced schedule only
     int32_t *ws_meta;
     uint32_t *chunk_ctr;
+    const void *new_k, *new_v;  // the step's new K/V rows [B, Hkv, d] to append first, or null
     int32_t *err;
     cudaStream_t stream;
 };
+
+pkv_status launch_append(const DecodeArgs &a, int64_t es) {
+    const int64_t row_bytes = static_cast<int64_t>(a.Hkv) * a.d * es;
+    auto kc = static_cast<char *>(const_cast<void *>(a.k_cache));
+    auto vc = static_cast<char *>(const_cast<void *>(a.v_cache));
+    auto kk = static_cast<const char *>(a.new_k);
+    auto vv = static_cast<const char *>(a.new_v);
+    const bool v16 = row_bytes % 16 == 0 && aligned(kc, 16) && aligned(vc, 16) && aligned(kk, 16) && aligned(vv, 16);
+    const bool v8 = row_bytes % 8 == 0 && aligned(kc, 8) && aligned(vc, 8) && aligned(kk, 8) && aligned(vv, 8);
+    const int64_t vec = v16 ? 16 : v8 ? 8 : es;
+    const int64_t items = static_cast<int64_t>(a.B) * ((row_bytes + 128 * vec - 1) / (128 * vec));
+    int64_t grid = (items + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
+    if (grid > 1024) grid = 1024;
+    if (grid < 1) grid = 1;
+    cudaError_t e;
+#define PKV_APPEND(V) \
+    launch_pdl(kPdlStore, append_kv_kernel<V>, dim3(static_cast<unsigned>(grid)), dim3(kAppendThreads), 0, a.stream, kk, \
+               vv, kc, vc, a.block_tables, a.max_blocks, a.context_lens, a.B, a.bs, a.num_blocks, a.max_ctx, row_bytes, a.err)
+    switch (vec) {
+    case 16: e = PKV_APPEND(int4); break;
+    case 8: e = PKV_APPEND(int2); break;
+    case 4: e = PKV_APPEND(int); break;
+    default: e = PKV_APPEND(short); break;
+    }
+#undef PKV_APPEND
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
 
 // CTAs of the one-wave work-balanced grid on the current device:
 // (resident CTAs per SM) x (SMs), capped by the workspace bound.
@@ -1521,7 +1633,9 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
                                a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
-                               a.chunk_ctr, a.err);
+                               a.chunk_ctr, static_cast<const T *>(a.new_k), static_cast<const T *>(a.new_v),
+                               static_cast<T *>(const_cast<void *>(a.k_cache)),
+                               static_cast<T *>(const_cast<void *>(a.v_cache)), a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G),
                    dim3(kMergeThreads), 0, a.stream,
@@ -1642,15 +1756,17 @@ extern "C" pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t 
     return ok();
 }
 
-extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
-                                                 const void *v_cache, const int32_t *block_tables,
-                                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                                 int32_t num_seqs, int32_t num_q_heads,
-                                                 int32_t num_kv_heads, int32_t head_dim,
-                                                 int32_t block_size, int32_t num_blocks,
-                                                 int32_t max_context_len, float scale, pkv_dtype dtype,
-                                                 void *workspace, size_t workspace_bytes,
-                                                 int32_t *err_flag, void *stream) {
+namespace pkv {
+namespace {
+
+// Decode attention, with the step's new K/V rows appended first when new_k is
+// not null (the fused decode step).
+pkv_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                        pkv_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
+                        const void *new_k, const void *new_v) {
     const int64_t es = dtype_bytes(dtype);
     if (es == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
@@ -1667,6 +1783,9 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
     if (!out || !q || !context_lens || (max_blocks_per_seq > 0 && !block_tables) ||
         (num_blocks > 0 && (!k_cache || !v_cache)))
         return set_error(PKV_ERR_INVALID_ARG, "decode: NULL pointer");
+    const bool append = new_k != nullptr || new_v != nullptr;
+    if (append && (!new_k || !new_v || !aligned(new_k, es) || !aligned(new_v, es)))
+        return set_error(PKV_ERR_INVALID_ARG, "decode append: key/value NULL or not aligned to the element size");
     Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
     if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
         return set_error(PKV_ERR_WORKSPACE, "decode: workspace needs %zu bytes (256-byte aligned), got %zu",
@@ -1694,8 +1813,21 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
                  p.stream ? reinterpret_cast<int4 *>(ws + p.o_bytes + p.ml_bytes) : nullptr,
                  p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes) : nullptr,
                  p.stream ? reinterpret_cast<uint32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes + 8) : nullptr,
-                 err_flag, static_cast<cudaStream_t>(stream)};
+                 nullptr, nullptr, err_flag, static_cast<cudaStream_t>(stream)};
     pkv_status st;
+    // The work-balanced kernel appends in its producer warp (8-byte copies);
+    // every other path runs the append kernel first, in stream order.
+    const bool fused = append && fast && p.stream && aligned(new_k, 8) && aligned(new_v, 8);
+    if (fused) {
+        a.new_k = new_k;
+        a.new_v = new_v;
+    } else if (append && num_blocks > 0 && max_blocks_per_seq > 0) {
+        a.new_k = new_k;
+        a.new_v = new_v;
+        st = launch_append(a, es);
+        if (st != PKV_OK) return st;
+        a.new_k = a.new_v = nullptr;
+    }
     if (fast && p.stream) {
         st = dtype == PKV_BF16 ? launch_stream_any<__nv_bfloat16>(a, p) : launch_stream_any<__half>(a, p);
     } else if (fast) {
@@ -1712,6 +1844,39 @@ extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const
     }
     if (st != PKV_OK) return st;
     return ok();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *block_tables,
+                                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                                 int32_t num_seqs, int32_t num_q_heads,
+                                                 int32_t num_kv_heads, int32_t head_dim,
+                                                 int32_t block_size, int32_t num_blocks,
+                                                 int32_t max_context_len, float scale, pkv_dtype dtype,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int32_t *err_flag, void *stream) {
+    return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
+                        workspace, workspace_bytes, err_flag, stream, nullptr, nullptr);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_append(void *out, const void *q, const void *key,
+                                                        const void *value, void *k_cache, void *v_cache,
+                                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                        const int32_t *context_lens, int32_t num_seqs,
+                                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                                        int32_t max_context_len, float scale, pkv_dtype dtype,
+                                                        void *workspace, size_t workspace_bytes,
+                                                        int32_t *err_flag, void *stream) {
+    if (num_seqs > 0 && (!key || !value))
+        return set_error(PKV_ERR_INVALID_ARG, "decode append: NULL key or value");
+    return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
+                        workspace, workspace_bytes, err_flag, stream, key, value);
 }
 
 // ----------------------------------------------------------------------------- no-allocation variant

@@ -120,6 +120,15 @@ def test_decode_argument_errors_are_synchronous(pkv):
         pkv.PKV_ERR_INVALID_ARG
     assert lib.pkv_unpack_block_paged(None, None, None, None, 2, None, 1, 1, 4, 5, 2, 8, 9, pkv.PKV_BF16, None,
                                       None) == pkv.PKV_ERR_INVALID_ARG
+    # the fused decode step: missing key/value, then the decode checks
+    st = lib.pkv_paged_attention_decode_append(None, None, None, None, None, None, None, 1, None, 2, 8, 4, 128, 16,
+                                               10, 64, 1.0, pkv.PKV_BF16, None, 0, None, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG and b"key or value" in lib.pkv_last_error_string()
+    st = lib.pkv_paged_attention_decode_append(None, None, 8, 8, None, None, None, 1, None, 2, 6, 4, 128, 16,
+                                               10, 64, 1.0, pkv.PKV_BF16, None, 0, None, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG and b"multiple" in lib.pkv_last_error_string()
+    assert lib.pkv_paged_attention_decode_append(None, None, None, None, None, None, None, 0, None, 0, 8, 4, 128,
+                                                 16, 10, 64, 1.0, pkv.PKV_BF16, None, 0, None, None) == pkv.PKV_OK
 
 
 def test_workspace_size_and_plan(pkv):

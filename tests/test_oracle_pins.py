@@ -282,6 +282,33 @@ def test_attention_empty_context_and_bad_block(orc):
 
 
 # --------------------------------------------------------------------------- CSR snapshot
+def test_decode_step_walk_appends_at_ctx_minus_one_and_attends(orc):
+    """The walk of "Walk the Shapes First": after the prefill (A: 6 tokens in
+    blocks [7, 2], B: 3 tokens in block [5]), decode step 1 appends A's token at
+    slot 10 and B's at slot 23 (the golden trace), then attends over 7 and 4
+    tokens; the output equals SDPA over the same rows stored contiguously."""
+    g = torch.Generator().manual_seed(5)
+    bs, Hkv, Hq, d = 4, 2, 4, 4
+    kc, vc = torch.randn(8, bs, Hkv, d, generator=g), torch.randn(8, bs, Hkv, d, generator=g)
+    tables = torch.tensor([[7, 2], [5, -1]], dtype=torch.int32)
+    key, value = torch.randn(2, Hkv, d, generator=g), torch.randn(2, Hkv, d, generator=g)
+    q = torch.randn(2, Hq, d, generator=g)
+    cl = torch.tensor([7, 4], dtype=torch.int32)
+    out, kc2, vc2, err = orc.decode_step(q, key, value, kc, vc, tables, cl, 0.5)
+    assert err == 0
+    want = load_golden("walk_trace.json")["derived_by_the_page_rules"]["steps"][1]["slots"]
+    flat_k, flat_v = kc2.reshape(-1, Hkv, d), vc2.reshape(-1, Hkv, d)
+    for b, slot in enumerate(want):
+        assert torch.equal(flat_k[slot], key[b]) and torch.equal(flat_v[slot], value[b])
+    changed = (kc2 != kc).reshape(-1, Hkv * d).any(1).nonzero().reshape(-1).tolist()
+    assert changed == sorted(want)
+    # contiguous K/V by hand: A = block 7 rows 0-3, block 2 rows 0-1, then its new row;
+    # B = block 5 rows 0-2, then its new row
+    Ks = [torch.cat([kc[7], kc[2, :2], key[0:1]]), torch.cat([kc[5, :3], key[1:2]])]
+    Vs = [torch.cat([vc[7], vc[2, :2], value[0:1]]), torch.cat([vc[5, :3], value[1:2]])]
+    torch.testing.assert_close(out, _sdpa_reference(q, Ks, Vs, Hq, Hkv, 0.5), atol=1e-12, rtol=1e-12)
+
+
 def test_element_offset_printed_example_and_alias(orc):
     g = load_golden("element_offset_example.json")
     args = (g["page_size"], g["num_pages"], g["num_heads"], g["head_dim"], g["block_table"],
