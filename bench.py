@@ -432,6 +432,27 @@ def time_attention_sustained(step: DecodeStep, calls: int, world: int, what=None
     return e0.elapsed_time(e1) / (n * ATTN_PER_GRAPH), n * ATTN_PER_GRAPH
 
 
+def time_host_allocator(pkv, step: DecodeStep, steps: int = 200):
+    """Host block allocator on the workload's pool: the batch's sequences are
+    admitted with their context lengths, then every step appends one token to
+    each (a new block whenever a length becomes 1 mod block_size).  Returns
+    microseconds per decode step of bookkeeping, or None if the pool is too
+    small for the extra tokens."""
+    cfg = step.cfg
+    a = pkv.pkv_allocator_create(step.nb, cfg.block_size)
+    for i, n in enumerate(step.batch.context_lens.cpu().tolist()):
+        pkv.pkv_allocator_add_sequence(a, i, n)
+    if pkv.pkv_allocator_stats(a)["free"] < step.B * (steps // cfg.block_size + 1):
+        return None
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for i in range(step.B):
+            pkv.pkv_allocator_append(a, i)
+    dt = time.perf_counter() - t0
+    assert pkv.pkv_allocator_check(a) == 0
+    return dt / steps * 1e6
+
+
 def e2e_io(step: DecodeStep):
     pairs = step.host_inputs()
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
@@ -560,6 +581,7 @@ def run_ours(args, world, rank, local):
     sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
     fused_ms, _ = time_attention_sustained(step, args.steps, world, step.fused_step)
     sep_ms, _ = time_attention_sustained(step, args.steps, world, step.separate_step)
+    alloc_us = time_host_allocator(pkv, step)
     fused_tok_s = reduce_sum(cfg.batch / (fused_ms * 1e-3), world, device)
     fused_ms = reduce_max(fused_ms, world, device)
     sep_ms = reduce_max(sep_ms, world, device)
@@ -631,6 +653,7 @@ def run_ours(args, world, rank, local):
             "separate_us": round(sep_ms * 1e3, 2),
             "fused_tokens_per_s": round(fused_tok_s, 1),
             "fused_kv_gbs": round(step.bytes["paged_attention_decode"] / (fused_ms * 1e-3) / 1e9, 1)},
+        "host_allocator_us_per_step": None if alloc_us is None else round(alloc_us, 1),
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},

@@ -321,6 +321,62 @@ PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, in
                                           pkv_index_type index_type, int64_t num_seqs,
                                           int64_t *flat_out);
 
+/*
+ * Host block allocator -- which physical block of the pool each sequence
+ * owns ("Paged KV Cache - AI infra interview lesson": Walk the Shapes First;
+ * Append slots during decode; Separate allocation, sharing and release).
+ * Host memory only, no CUDA call; thread-safe per handle.  It hands out the
+ * lowest-numbered free block first, so traces are deterministic, and keeps a
+ * reference count per block: the number of block-table entries that point at
+ * it.  A block returns to the free pool when its count reaches zero.
+ *
+ *   pkv_allocator_create       pool of num_blocks blocks of block_size tokens
+ *                              (num_blocks * block_size < 2^31)
+ *   pkv_allocator_add_sequence new sequence `seq` holding num_tokens tokens:
+ *                              ceil(num_tokens / block_size) blocks, taken from
+ *                              the pool, or the caller's `blocks` (host int32
+ *                              list; each must be free) when not NULL
+ *   pkv_allocator_fork         new sequence `child` sharing the first
+ *                              num_tokens tokens (whole blocks) of `parent`;
+ *                              the shared blocks' counts go up
+ *   pkv_allocator_append       grows `seq` by num_tokens tokens, taking a new
+ *                              block whenever a position p has p % block_size
+ *                              == 0; writes their slots
+ *                              (block_table[p / bs] * bs + p % bs) to the host
+ *                              int32 `slots` [num_tokens] if not NULL
+ *   pkv_allocator_release      drops `seq`; its blocks' counts go down
+ *   pkv_allocator_block_table  host int32 row [max_blocks] of `seq` (padded
+ *                              with -1), its length and block count
+ *   pkv_allocator_stats        free, allocated (count > 0) and referenced
+ *                              blocks, live sequences; any output may be NULL
+ *   pkv_allocator_check        0 when every accounting invariant holds, else
+ *                              the first broken one: 1 free + allocated !=
+ *                              pool, 2 a count differs from the table entries
+ *                              that point at the block, 3 a block is both free
+ *                              and referenced (or neither), 4 a sequence's
+ *                              partly filled last block is shared, 5 a table
+ *                              does not cover its sequence's length
+ *                              ("Chapter 2 -- KV cache, memory hierarchy,
+ *                              continuous batching, and PagedAttention",
+ *                              Deterministic evals for this layer)
+ * Errors: PKV_ERR_INVALID_ARG (unknown or duplicate sequence id, a prefix that
+ * is not whole blocks, a block that is not free); PKV_ERR_OUT_OF_RANGE (not
+ * enough free blocks, or a row too short).  A failed call changes nothing.
+ */
+typedef struct pkv_block_allocator pkv_block_allocator;
+PKV_API pkv_status pkv_allocator_create(int32_t num_blocks, int32_t block_size, pkv_block_allocator **out);
+PKV_API void pkv_allocator_destroy(pkv_block_allocator *a);
+PKV_API pkv_status pkv_allocator_add_sequence(pkv_block_allocator *a, int64_t seq, int64_t num_tokens,
+                                              const int32_t *blocks);
+PKV_API pkv_status pkv_allocator_fork(pkv_block_allocator *a, int64_t parent, int64_t child, int64_t num_tokens);
+PKV_API pkv_status pkv_allocator_append(pkv_block_allocator *a, int64_t seq, int64_t num_tokens, int32_t *slots);
+PKV_API pkv_status pkv_allocator_release(pkv_block_allocator *a, int64_t seq);
+PKV_API pkv_status pkv_allocator_block_table(pkv_block_allocator *a, int64_t seq, int32_t *row,
+                                             int32_t max_blocks, int64_t *num_tokens, int32_t *num_used);
+PKV_API pkv_status pkv_allocator_stats(pkv_block_allocator *a, int64_t *free_blocks, int64_t *allocated_blocks,
+                                       int64_t *referenced_blocks, int64_t *num_seqs);
+PKV_API int32_t pkv_allocator_check(pkv_block_allocator *a);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,15 @@ _SIGS = {
     "pkv_validate_block_paged_shape": ([_vp, _i32, _i32, _i32], ctypes.c_int),
     "pkv_block_paged_element_offset": ([_i64, _i64, _i64, _i64, _i32, _i64, _i32, _i32, _vp, _vp, ctypes.c_int,
                                         _i64, _vp], ctypes.c_int),
+    "pkv_allocator_create": ([_i32, _i32, _vp], ctypes.c_int),
+    "pkv_allocator_destroy": ([_vp], None),
+    "pkv_allocator_add_sequence": ([_vp, _i64, _i64, _vp], ctypes.c_int),
+    "pkv_allocator_fork": ([_vp, _i64, _i64, _i64], ctypes.c_int),
+    "pkv_allocator_append": ([_vp, _i64, _i64, _vp], ctypes.c_int),
+    "pkv_allocator_release": ([_vp, _i64], ctypes.c_int),
+    "pkv_allocator_block_table": ([_vp, _i64, _vp, _i32, _vp, _vp], ctypes.c_int),
+    "pkv_allocator_stats": ([_vp, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "pkv_allocator_check": ([_vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -289,3 +298,66 @@ def pkv_block_paged_element_offset(seq, token, head, dim, page_size, num_pages, 
                                                _ptr(bt), _ptr(sp), _INDEX[sp.dtype], sp.numel() - 1,
                                                ctypes.byref(flat)))
     return flat.value
+
+
+# ----------------------------------------------------------------------------- host block allocator
+class BlockAllocator:
+    """Handle of a host block allocator (see pkv_allocator_* in pkv.h); the
+    pool is freed with the object."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        h = ctypes.c_void_p()
+        _check(_lib.pkv_allocator_create(num_blocks, block_size, ctypes.byref(h)))
+        self._h, self.num_blocks, self.block_size = h, num_blocks, block_size
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            _lib.pkv_allocator_destroy(h)
+
+
+def pkv_allocator_create(num_blocks: int, block_size: int) -> BlockAllocator:
+    return BlockAllocator(num_blocks, block_size)
+
+
+def pkv_allocator_add_sequence(a: BlockAllocator, seq: int, num_tokens: int, blocks=None):
+    arr = None
+    if blocks is not None:
+        blocks = list(blocks)
+        arr = (ctypes.c_int32 * max(1, len(blocks)))(*blocks)
+        if len(blocks) < -(-num_tokens // a.block_size):
+            raise ValueError("blocks must cover num_tokens")
+    _check(_lib.pkv_allocator_add_sequence(a._h, seq, num_tokens, arr))
+
+
+def pkv_allocator_fork(a: BlockAllocator, parent: int, child: int, num_tokens: int):
+    _check(_lib.pkv_allocator_fork(a._h, parent, child, num_tokens))
+
+
+def pkv_allocator_append(a: BlockAllocator, seq: int, num_tokens: int = 1) -> list:
+    """Grows the sequence; returns the slots of its new positions."""
+    arr = (ctypes.c_int32 * max(1, num_tokens))()
+    _check(_lib.pkv_allocator_append(a._h, seq, num_tokens, arr))
+    return list(arr[:num_tokens])
+
+
+def pkv_allocator_release(a: BlockAllocator, seq: int):
+    _check(_lib.pkv_allocator_release(a._h, seq))
+
+
+def pkv_allocator_block_table(a: BlockAllocator, seq: int, max_blocks: int):
+    """(row of max_blocks block ids padded with -1, length in tokens, blocks used)."""
+    row = (ctypes.c_int32 * max(1, max_blocks))()
+    n, used = ctypes.c_int64(), ctypes.c_int32()
+    _check(_lib.pkv_allocator_block_table(a._h, seq, row, max_blocks, ctypes.byref(n), ctypes.byref(used)))
+    return list(row[:max_blocks]), n.value, used.value
+
+
+def pkv_allocator_stats(a: BlockAllocator) -> dict:
+    v = [ctypes.c_int64() for _ in range(4)]
+    _check(_lib.pkv_allocator_stats(a._h, *[ctypes.byref(x) for x in v]))
+    return dict(zip(("free", "allocated", "referenced", "sequences"), (x.value for x in v)))
+
+
+def pkv_allocator_check(a: BlockAllocator) -> int:
+    return int(_lib.pkv_allocator_check(a._h))

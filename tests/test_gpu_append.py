@@ -164,3 +164,49 @@ def test_full_size_append_step(pkv, orc, cuda_dev, name):
     ref, _ = orc.paged_attention_decode(batch.q.cpu()[idx], kr, vr, batch.block_tables.cpu()[idx],
                                         batch.context_lens.cpu()[idx], batch.scale)
     assert _max_err(out[idx.to(cuda_dev)], ref) <= ATOL_16
+
+
+def test_allocator_driven_decode_steps(pkv, orc, cuda_dev):
+    """Several decode steps of a changing batch: the host allocator hands out
+    the blocks (a new one exactly when a length becomes 1 mod 16), sequences
+    finish and new ones are admitted into freed blocks, and every step runs the
+    fused append + attention.  Each step's caches match the oracle's decode
+    step bit for bit, the new rows sit at the allocator's slots, and the
+    attention is within the bar."""
+    g = torch.Generator().manual_seed(40)
+    nb, bs, Hq, Hkv, d, dtype = 160, 16, 32, 8, 128, torch.bfloat16
+    a = pkv.pkv_allocator_create(nb, bs)
+    kc = torch.randn(nb, bs, Hkv, d, generator=g).to(dtype).to(cuda_dev)
+    vc = torch.randn(nb, bs, Hkv, d, generator=g).to(dtype).to(cuda_dev)
+    live, next_id = [], 0
+    for n in (300, 17, 16, 1, 900, 64):
+        pkv.pkv_allocator_add_sequence(a, next_id, n)
+        live.append(next_id)
+        next_id += 1
+    for step in range(6):
+        if step in (2, 4):  # one sequence finishes, a new one is admitted
+            pkv.pkv_allocator_release(a, live.pop(1))
+            pkv.pkv_allocator_add_sequence(a, next_id, 40 + 100 * step)
+            live.append(next_id)
+            next_id += 1
+        slots = [pkv.pkv_allocator_append(a, s)[0] for s in live]
+        assert pkv.pkv_allocator_check(a) == 0
+        rows = [pkv.pkv_allocator_block_table(a, s, 64) for s in live]
+        tables = torch.tensor([r[0] for r in rows], dtype=torch.int32)
+        lens = torch.tensor([r[1] for r in rows], dtype=torch.int32)
+        B = len(live)
+        q = torch.randn(B, Hq, d, generator=g).to(dtype)
+        key = torch.randn(B, Hkv, d, generator=g).to(dtype)
+        value = torch.randn(B, Hkv, d, generator=g).to(dtype)
+        kc0, vc0 = kc.cpu(), vc.cpu()
+        err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+        out = pkv.pkv_paged_attention_decode_append(q.to(cuda_dev), key.to(cuda_dev), value.to(cuda_dev), kc, vc,
+                                                    tables.to(cuda_dev), lens.to(cuda_dev), d ** -0.5,
+                                                    int(lens.max()), err_flag=err)
+        ref, kr, vr, nerr = orc.decode_step(q, key, value, kc0, vc0, tables, lens, d ** -0.5)
+        assert nerr == 0 and int(err.item()) == 0
+        assert torch.equal(_bits(kc), _bits(kr)) and torch.equal(_bits(vc), _bits(vr))
+        flat = kc.cpu().reshape(-1, Hkv, d)
+        for b, slot in enumerate(slots):
+            assert torch.equal(_bits(flat[slot]), _bits(key[b]))
+        assert _max_err(out, ref) <= ATOL_16
