@@ -68,6 +68,18 @@ def _load():
             lib.orc_unpack_block_paged.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, i64, i64,
                                                    u64, i64, i64, i64]
             lib.orc_unpack_block_paged.restype = i64
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_decode.restype = dbl
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_quantize_kvcache_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int]
+            lib.orc_quantize_kvcache_fp8.restype = None
+            lib.orc_store_kvcache_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                  ctypes.c_int]
+            lib.orc_store_kvcache_fp8.restype = i64
+            lib.orc_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                           i32, i32, i32, i32, dbl, ctypes.c_int]
+            lib.orc_paged_attention_decode_fp8.restype = i64
             _lib = lib
     return _lib
 
@@ -155,6 +167,57 @@ def decode_step(q, key, value, k_cache, v_cache, block_tables, context_lens, sca
     kc, vc, e2 = store_kvcache(_cpu(key)[keep], _cpu(value)[keep], k_cache, v_cache, slots)
     out, e3 = paged_attention_decode(q, kc, vc, bt, cl, scale)
     return out, kc, vc, e1 + e2 + e3
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of an 8-bit E4M3 code (OCP FP8)."""
+    return _load().orc_e4m3_decode(code)
+
+
+def e4m3_encode(x: float) -> int:
+    """binary32 -> E4M3 code: round to nearest even, saturating at +-448."""
+    return int(_load().orc_e4m3_encode(x))
+
+
+def quantize_kvcache_fp8(cache):
+    """[num_blocks, bs, H, d] cache -> (uint8 codes of the same shape, float32
+    scales [num_blocks, H]); per (block, head) s = max|x| / 448."""
+    src = _cpu(cache)
+    nb, bs, H, d = src.shape
+    codes = torch.empty(nb, bs, H, d, dtype=torch.uint8)
+    scales = torch.empty(nb, H, dtype=torch.float32)
+    _load().orc_quantize_kvcache_fp8(_ptr(src), _ptr(codes), _ptr(scales), nb, bs, H, d, _DTYPE_CODE[src.dtype])
+    return codes, scales
+
+
+def store_kvcache_fp8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping):
+    """fp8 "Step 1" on CPU copies of the code caches; returns (k_codes,
+    v_codes, error count)."""
+    key, value = _cpu(key), _cpu(value)
+    kc, vc = _cpu(k_codes).clone(), _cpu(v_codes).clone()
+    ks, vs = _cpu(k_scale, torch.float32), _cpu(v_scale, torch.float32)
+    sm = _cpu(slot_mapping, torch.int32)
+    nb, bs, H, d = kc.shape
+    err = _load().orc_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(sm),
+                                        sm.numel(), H, d, bs, nb * bs, _DTYPE_CODE[key.dtype])
+    return kc, vc, err
+
+
+def paged_attention_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float):
+    """Binary64 output [B, Hq, d] and error count over an fp8 cache."""
+    q = _cpu(q)
+    kc, vc = _cpu(k_codes), _cpu(v_codes)
+    ks, vs = _cpu(k_scale, torch.float32), _cpu(v_scale, torch.float32)
+    bt = _cpu(block_tables, torch.int32)
+    cl = _cpu(context_lens, torch.int32)
+    B, Hq, d = q.shape
+    nb, bs, Hkv, d2 = kc.shape
+    assert d2 == d and Hq % Hkv == 0 and kc.dtype == torch.uint8
+    out = torch.empty(B, Hq, d, dtype=torch.float64)
+    err = _load().orc_paged_attention_decode_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                                 _ptr(bt), bt.shape[1] if bt.dim() == 2 else 0, _ptr(cl), B, Hq,
+                                                 Hkv, d, bs, nb, float(scale), _DTYPE_CODE[q.dtype])
+    return out, err
 
 
 def validate_index_buffers(seq_ptr, block_table, num_pages: int, index_dtype=torch.int64) -> int:

@@ -315,3 +315,186 @@ int64_t orc_unpack_block_paged(void *out, const void *page_pool, const void *blo
     }
     return errors;
 }
+
+/* ---------------------------------------------------------------------------
+ * [P1] "Quantization compatibility": an fp8 cache keeps its scales per page
+ * slot (per-block-affine with block_size == page_size), so a shared page
+ * carries its own scales.  The pages give that placement rule only.  Readings:
+ * the codes are OCP 8-bit E4M3 (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, no infinities, S.1111.111 = NaN, largest finite 448); each
+ * (physical block, KV head) has one binary32 scale for K and one for V, laid
+ * out [num_blocks, H_kv]; a stored value is scale * decode(code).
+ * ------------------------------------------------------------------------- */
+
+/* E4M3 code -> value, from the format's definition. */
+double orc_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* subnormal: (m / 8) * 2^-6 */
+    else
+        v = ldexp((double)(8 + m), e - 10); /* normal: (1 + m / 8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+/* binary32 -> E4M3, round to nearest with ties to even, saturating: magnitudes
+ * above 448 (infinities included) give +-448; NaN gives the NaN code with the
+ * input's sign.  The magnitude is rounded on the quantum of its binade (2^-9
+ * below the smallest normal 2^-6) with rint in the default rounding mode. */
+uint8_t orc_e4m3_encode(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    int E, e;
+    double v, n;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    if (a > 448.0) return (uint8_t)(sign | 0x7E);
+    if (a == 0.0) return sign;
+    frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) */
+    E = e - 1;             /* a = 1.xxx * 2^E */
+    if (E < -6) E = -6;
+    n = rint(a / ldexp(1.0, E - 3));   /* exact scaling by a power of two, then RN-even */
+    v = n * ldexp(1.0, E - 3);
+    if (v == 0.0) return sign;
+    if (v < ldexp(1.0, -6))            /* subnormal */
+        return (uint8_t)(sign | (int)(v / ldexp(1.0, -9)));
+    frexp(v, &e);
+    E = e - 1;
+    return (uint8_t)(sign | ((E + 7) << 3) | ((int)(v / ldexp(1.0, E - 3)) - 8));
+}
+
+/* The code of x stored with scale s: encode(x / s), the division in binary32
+ * (the precision the kernels use); a zero scale stores +0. */
+static uint8_t encode_scaled(double x, float s)
+{
+    if (s == 0.0f) return 0;
+    return orc_e4m3_encode((float)x / s);
+}
+
+/* Quantizes a [num_blocks, bs, H_kv, d] cache of `dtype`: per (block, head),
+ * s = max |x| / 448 in binary32 (NaN entries ignored), then every element
+ * becomes encode(x / s).  Writes codes [num_blocks, bs, H_kv, d] and scales
+ * [num_blocks, H_kv]. */
+void orc_quantize_kvcache_fp8(const void *src, uint8_t *codes, float *scales, int64_t num_blocks,
+                              int64_t bs, int64_t num_kv_heads, int64_t head_dim, int dtype)
+{
+    build_f16_table();
+    for (int64_t blk = 0; blk < num_blocks; ++blk) {
+        for (int64_t h = 0; h < num_kv_heads; ++h) {
+            float amax = 0.0f;
+            for (int64_t t = 0; t < bs; ++t)
+                for (int64_t i = 0; i < head_dim; ++i) {
+                    float a = (float)fabs(load_elem(src, ((blk * bs + t) * num_kv_heads + h) * head_dim + i, dtype));
+                    if (a > amax) amax = a;
+                }
+            float s = amax / 448.0f;
+            scales[blk * num_kv_heads + h] = s;
+            for (int64_t t = 0; t < bs; ++t)
+                for (int64_t i = 0; i < head_dim; ++i) {
+                    int64_t idx = ((blk * bs + t) * num_kv_heads + h) * head_dim + i;
+                    codes[idx] = encode_scaled(load_elem(src, idx, dtype), s);
+                }
+        }
+    }
+}
+
+/* [P3] "Step 1" for an fp8 cache: row slot_mapping[i] of the code caches
+ * receives encode(key[i] / s) per element, s the scale of the row's block and
+ * head (slot / bs); -1 is skipped, other slots outside [0, num_slots) are
+ * counted and skipped.  key/value are [num_tokens, H_kv, d] of `dtype`. */
+int64_t orc_store_kvcache_fp8(const void *key, const void *value, uint8_t *k_codes, uint8_t *v_codes,
+                              const float *k_scale, const float *v_scale, const int32_t *slot_mapping,
+                              int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim, int64_t bs,
+                              int64_t num_slots, int dtype)
+{
+    int64_t errors = 0;
+    build_f16_table();
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= num_slots) { ++errors; continue; }
+        for (int64_t h = 0; h < num_kv_heads; ++h) {
+            float sk = k_scale[(slot / bs) * num_kv_heads + h], sv = v_scale[(slot / bs) * num_kv_heads + h];
+            for (int64_t d = 0; d < head_dim; ++d) {
+                int64_t src = (i * num_kv_heads + h) * head_dim + d;
+                int64_t dst = (slot * num_kv_heads + h) * head_dim + d;
+                k_codes[dst] = encode_scaled(load_elem(key, src, dtype), sk);
+                v_codes[dst] = encode_scaled(load_elem(value, src, dtype), sv);
+            }
+        }
+    }
+    return errors;
+}
+
+/* [P3] "Step 2" over an fp8 cache: as orc_paged_attention_decode, with every
+ * K/V element read as scale[block][kv head] * decode(code) in binary64. */
+int64_t orc_paged_attention_decode_fp8(double *out, const void *q, const uint8_t *k_codes,
+                                       const uint8_t *v_codes, const float *k_scale, const float *v_scale,
+                                       const int32_t *block_tables, int32_t max_blocks,
+                                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t bs, int32_t num_blocks,
+                                       double scale, int q_dtype)
+{
+    int64_t errors = 0;
+    int32_t group = num_q_heads / num_kv_heads;
+    build_f16_table();
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int64_t n = context_lens[b];
+        const int32_t *row = block_tables + (int64_t)b * max_blocks;
+        if (n < 0 || (n + bs - 1) / bs > max_blocks) {
+            ++errors;
+            n = -1;
+        }
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        char *usable = (char *)malloc((size_t)(n > 0 ? n : 1));
+        if (n > 0) {
+            for (int64_t j = 0; j < (n + bs - 1) / bs; ++j)
+                if (row[j] < 0 || row[j] >= num_blocks) ++errors;
+        }
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            int32_t g = h / group;
+            double *o = out + ((int64_t)b * num_q_heads + h) * head_dim;
+            for (int32_t i = 0; i < head_dim; ++i) o[i] = 0.0;
+            if (n <= 0) continue;
+            int64_t q_base = ((int64_t)b * num_q_heads + h) * head_dim;
+            double m = -INFINITY;
+            for (int64_t t = 0; t < n; ++t) {
+                int32_t phys = row[t / bs];
+                usable[t] = (phys >= 0 && phys < num_blocks);
+                if (!usable[t]) continue;
+                int64_t cache_row = (int64_t)phys * bs + t % bs;
+                int64_t k_base = (cache_row * num_kv_heads + g) * head_dim;
+                double sk = k_scale[(int64_t)phys * num_kv_heads + g];
+                double s = 0.0;
+                for (int32_t i = 0; i < head_dim; ++i)
+                    s += load_elem(q, q_base + i, q_dtype) * (sk * orc_e4m3_decode(k_codes[k_base + i]));
+                scores[t] = scale * s;
+                if (scores[t] > m) m = scores[t];
+            }
+            if (m == -INFINITY) continue;
+            double l = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                if (!usable[t]) continue;
+                scores[t] = exp(scores[t] - m);
+                l += scores[t];
+            }
+            for (int64_t t = 0; t < n; ++t) {
+                if (!usable[t]) continue;
+                int32_t phys = row[t / bs];
+                int64_t cache_row = (int64_t)phys * bs + t % bs;
+                int64_t v_base = (cache_row * num_kv_heads + g) * head_dim;
+                double sv = v_scale[(int64_t)phys * num_kv_heads + g];
+                double p = scores[t] / l;
+                for (int32_t i = 0; i < head_dim; ++i)
+                    o[i] += p * (sv * orc_e4m3_decode(v_codes[v_base + i]));
+            }
+        }
+        free(scores);
+        free(usable);
+    }
+    return errors;
+}

@@ -387,3 +387,90 @@ def test_unpack_missing_page_is_zero_and_counted(orc):
     out, err = orc.unpack_block_paged(pool, [1], [0, 1], [0, 3])   # token 2 needs a 2nd page
     assert torch.equal(out[:2], pool[1])
     assert torch.equal(out[2], torch.zeros(1, 4)) and err == 4
+
+
+# --------------------------------------------------------------------------- fp8 (E4M3) cache
+def test_e4m3_decode_exhaustive_matches_torch(orc):
+    """Every one of the 256 codes against torch's float8_e4m3fn."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).double()
+    got = torch.tensor([orc.e4m3_decode(c) for c in range(256)], dtype=torch.float64)
+    nan = torch.isnan(want)
+    assert torch.equal(nan, torch.isnan(got)) and nan.sum() == 2  # S.1111.111
+    assert torch.equal(got[~nan], want[~nan])
+    assert orc.e4m3_decode(0x7E) == 448.0 and orc.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encode_rounds_to_nearest_even(orc):
+    """Against torch's cast (round to nearest even) on every representable
+    value, every midpoint and its float32 neighbours, and random magnitudes
+    from the subnormal range to 448."""
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).float()
+    fin = vals[~torch.isnan(vals)].unique()
+    pos = fin[fin >= 0]
+    mids = (pos[1:] + pos[:-1]) / 2
+    g = torch.Generator().manual_seed(8)
+    rnd = torch.exp(torch.empty(20000).uniform_(-10 * 0.6931, 8.8 * 0.6931, generator=g))
+    xs = torch.cat([fin, mids, torch.nextafter(mids, torch.full_like(mids, 1e9)),
+                    torch.nextafter(mids, torch.zeros_like(mids)), rnd, -rnd]).float()
+    xs = xs[xs.abs() <= 448]
+    want = xs.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([orc.e4m3_encode(float(x)) for x in xs], dtype=torch.uint8)
+    assert torch.equal(got, want)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan(orc):
+    for x, code in [(448.0, 0x7E), (463.9, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (float("inf"), 0x7E),
+                    (-1e30, 0xFE), (float("-inf"), 0xFE), (float("nan"), 0x7F), (-0.0, 0x80),
+                    (2.0 ** -10, 0x00), (1.5 * 2.0 ** -9, 0x02)]:
+        assert orc.e4m3_encode(x) == code, x
+
+
+def test_quantize_and_store_fp8_match_a_torch_restatement(orc):
+    """Per (block, head) s = max|x| / 448, codes = x / s cast to E4M3 (binary32
+    division), against torch; the store writes the same codes at the slots."""
+    g = torch.Generator().manual_seed(9)
+    nb, bs, H, d = 5, 4, 2, 8
+    cache = (torch.randn(nb, bs, H, d, generator=g) * 3).to(torch.bfloat16)
+    cache[2, :, 1] = 0  # an all-zero (block, head): scale 0, codes +0
+    codes, scales = orc.quantize_kvcache_fp8(cache)
+    amax = cache.float().abs().amax(dim=(1, 3))
+    assert torch.equal(scales, amax / 448.0)
+    safe = torch.where(scales == 0, torch.ones_like(scales), scales)
+    want = (cache.float() / safe[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    want[2, :, 1] = 0
+    assert torch.equal(codes, want)
+    # the store: tokens 0..2 at slots 9, -1, 17 with the blocks' scales
+    key = (torch.randn(3, H, d, generator=g) * 2).to(torch.bfloat16)
+    value = (torch.randn(3, H, d, generator=g) * 2).to(torch.bfloat16)
+    slots = torch.tensor([9, -1, 17], dtype=torch.int32)
+    kc, vc, err = orc.store_kvcache_fp8(key, value, codes, codes, scales, scales, slots)
+    assert err == 0
+    for i, slot in ((0, 9), (2, 17)):  # slot 9 is block 2, whose head 1 has scale 0
+        blk = slot // bs
+        x = (key[i].float() / safe[blk][:, None]).clamp(-448, 448)  # saturation, then RN-even
+        want_k = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        want_k[scales[blk] == 0] = 0
+        assert torch.equal(kc.reshape(-1, H, d)[slot], want_k)
+    assert torch.equal(kc.reshape(-1, H, d)[[s for s in range(nb * bs) if s not in (9, 17)]],
+                       codes.reshape(-1, H, d)[[s for s in range(nb * bs) if s not in (9, 17)]])
+
+
+def test_attention_fp8_matches_sdpa_on_dequantized_kv(orc):
+    """The fp8 attention equals SDPA (binary64) over K/V dequantized as
+    scale * decode(code) and stored contiguously."""
+    bs, Hq, Hkv, d, nb = 4, 4, 2, 8, 12
+    q, kc, vc, bt, cl, _, _ = _paged_case(bs, Hq, Hkv, d, [1, bs, 2 * bs + 3], nb, seed=10)
+    kq, ks = orc.quantize_kvcache_fp8(kc)
+    vq, vs = orc.quantize_kvcache_fp8(vc)
+    out, err = orc.paged_attention_decode_fp8(q, kq, vq, ks, vs, bt, cl, d ** -0.5)
+    assert err == 0
+    dk = kq.view(torch.float8_e4m3fn).double() * ks.double()[:, None, :, None]
+    dv = vq.view(torch.float8_e4m3fn).double() * vs.double()[:, None, :, None]
+    Ks, Vs = [], []
+    for b in range(3):
+        n = int(cl[b])
+        rows = [(int(bt[b, t // bs]), t % bs) for t in range(n)]
+        Ks.append(torch.stack([dk[p, o] for p, o in rows]))
+        Vs.append(torch.stack([dv[p, o] for p, o in rows]))
+    torch.testing.assert_close(out, _sdpa_reference(q, Ks, Vs, Hq, Hkv, d ** -0.5), atol=1e-12, rtol=1e-12)
