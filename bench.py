@@ -127,6 +127,15 @@ def step_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> dict:
     }
 
 
+def fp8_attention_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> int:
+    """Algorithmic bytes of decode attention over E4M3 caches: one byte per K/V
+    element, a K and a V scale per (block, head), q, out and the tables."""
+    es = torch.tensor([], dtype=cfg.dtype).element_size()
+    B, T = int(ctx.numel()), int(ctx.to(torch.int64).sum())
+    return (T * 2 * cfg.num_kv_heads * cfg.head_dim + 2 * B * cfg.num_q_heads * cfg.head_dim * es + nnz * 4 + B * 4
+            + nnz * cfg.num_kv_heads * 8)
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -290,6 +299,20 @@ class DecodeStep:
                                             c.num_kv_heads, c.head_dim, c.block_size, self.nb, b.max_context_len,
                                             b.scale, self.dt, p(self.workspace), self.workspace.numel(),
                                             p(self.err), stream_ptr)
+
+    def make_fp8(self):
+        """E4M3 copies of the caches (per-(block, head) scales) for the fp8 pass."""
+        self.kq, self.ks = self.pkv.pkv_quantize_kvcache_fp8(self.batch.k_cache)
+        self.vq, self.vs = self.pkv.pkv_quantize_kvcache_fp8(self.batch.v_cache)
+
+    def fp8_attention(self, stream_ptr) -> int:
+        """Enqueue the decode-attention call over the E4M3 caches."""
+        L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        return L.pkv_paged_attention_decode_fp8(p(self.out), p(b.q), p(self.kq), p(self.vq), p(self.ks), p(self.vs),
+                                                p(b.block_tables), b.block_tables.shape[1], p(b.context_lens),
+                                                self.B, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                                                self.nb, b.max_context_len, b.scale, self.dt, p(self.workspace),
+                                                self.workspace.numel(), p(self.err), stream_ptr)
 
     def fused_step(self, stream_ptr) -> int:
         """Enqueue the fused decode step (append the new K/V rows, then attend)."""
@@ -581,6 +604,11 @@ def run_ours(args, world, rank, local):
     sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
     fused_ms, _ = time_attention_sustained(step, args.steps, world, step.fused_step)
     sep_ms, _ = time_attention_sustained(step, args.steps, world, step.separate_step)
+    step.make_fp8()
+    fp8_bytes = fp8_attention_bytes(cfg, step.batch.context_lens.cpu(), step.snap.nnz)
+    fp8_ms, _ = time_attention_sustained(step, args.steps, world, step.fp8_attention)
+    fp8_tok_s = reduce_sum(cfg.batch / (fp8_ms * 1e-3), world, device)
+    fp8_ms = reduce_max(fp8_ms, world, device)
     alloc_us = time_host_allocator(pkv, step)
     fused_tok_s = reduce_sum(cfg.batch / (fused_ms * 1e-3), world, device)
     fused_ms = reduce_max(fused_ms, world, device)
@@ -653,6 +681,14 @@ def run_ours(args, world, rank, local):
             "separate_us": round(sep_ms * 1e3, 2),
             "fused_tokens_per_s": round(fused_tok_s, 1),
             "fused_kv_gbs": round(step.bytes["paged_attention_decode"] / (fused_ms * 1e-3) / 1e9, 1)},
+        "decode_fp8": {
+            "what": "pkv_paged_attention_decode_fp8 over E4M3 copies of the caches (one fp32 scale per block and "
+                    "KV head), back to back in CUDA graphs like the roofline pass",
+            "us_per_call": round(fp8_ms * 1e3, 2),
+            "gbs": round(fp8_bytes / (fp8_ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(fp8_bytes / (fp8_ms * 1e-3) / 1e9 / peak, 4),
+            "tokens_per_s": round(fp8_tok_s, 1),
+            "speedup_vs_16bit": round(sus_ms / fp8_ms, 3)},
         "host_allocator_us_per_step": None if alloc_us is None else round(alloc_us, 1),
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

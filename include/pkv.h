@@ -322,6 +322,53 @@ PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, in
                                           int64_t *flat_out);
 
 /*
+ * fp8 (E4M3) paged caches -- "Block-Paged KV Cache", Quantization
+ * compatibility: per-block-affine scales with block_size == page_size stay per
+ * page slot, so a shared page carries its own scales.  The pages give that
+ * placement rule only.  This library's reading: the caches hold OCP E4M3
+ * codes (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite 448), [num_blocks, block_size, num_kv_heads,
+ * head_dim] bytes, and every (physical block, KV head) has one float32 scale
+ * for K and one for V, k_scale / v_scale [num_blocks, num_kv_heads].  A
+ * stored value is scale * decode(code).  Encoding divides by the scale in
+ * binary32 and rounds to the nearest even code, saturating at +-448; a zero
+ * scale stores +0.
+ *
+ * pkv_quantize_kvcache_fp8: a 16-bit or fp32 cache `src` of `dtype` -> codes
+ *   and scales, per (block, head) s = max|x| / 448 (NaN ignored).  Used to
+ *   fill a cache (e.g. after a prefill); head_dim must be even.
+ * pkv_store_kvcache_fp8: "Step 1" into an fp8 cache: row slot_mapping[i]
+ *   receives encode(key[i] / s) with the scale of the row's block and head
+ *   (a value beyond 448 * s saturates).  Slot -1 is skipped; other slots
+ *   outside [0, num_slots) set PKV_ERRBIT_SLOT_RANGE and are skipped.
+ * pkv_paged_attention_decode_fp8: "Step 2" over fp8 caches, q and out in
+ *   fp16 or bf16, with the arguments, workspace
+ *   (pkv_paged_attention_decode_workspace_size with the q dtype) and device
+ *   errors of pkv_paged_attention_decode.  Codes are widened exactly to f16
+ *   and the products run on f16 tensor cores (q is rounded to f16 once;
+ *   values beyond 65504 overflow).  Only the tensor-core, work-balanced
+ *   shapes run: head_dim 128, num_q_heads / num_kv_heads <= 8, block_size a
+ *   multiple of 16, at most 512 sequences, 16-byte aligned code pools;
+ *   others return PKV_ERR_UNSUPPORTED.
+ */
+PKV_API pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
+                                            int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                            pkv_dtype dtype, void *stream);
+PKV_API pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                         const float *k_scale, const float *v_scale, const int32_t *slot_mapping,
+                                         int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                         int64_t num_slots, int32_t block_size, pkv_dtype dtype,
+                                         int32_t *err_flag, void *stream);
+PKV_API pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                                  const void *v_cache, const float *k_scale, const float *v_scale,
+                                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                  const int32_t *context_lens, int32_t num_seqs,
+                                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                                  float scale, pkv_dtype dtype, void *workspace,
+                                                  size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
  * Host block allocator -- which physical block of the pool each sequence
  * owns ("Paged KV Cache - AI infra interview lesson": Walk the Shapes First;
  * Append slots during decode; Separate allocation, sharing and release).

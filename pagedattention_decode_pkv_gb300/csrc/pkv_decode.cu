@@ -41,6 +41,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "pkv_internal.h"
 #include "pkv_pdl.cuh"
@@ -239,6 +240,52 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Two bf16 -> two f16 (round to nearest even; the fp8 path runs its MMAs in f16).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two E4M3 codes -> two f16, exactly (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+    uint32_t d;
+    const uint16_t h = static_cast<uint16_t>(v16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
+    return d;
+}
+
+// Widens one head's E4M3 tile [16 tokens][128 B] (the TMA 128-byte swizzle puts
+// the 16-byte chunk c of row t at chunk c ^ (t & 7)) into the f16 tile
+// [2 halves][16 tokens][128 B] with the same swizzle, which the ldmatrix
+// offsets of the 16-bit path read.  Lane l widens half l & 1 of row l >> 1;
+// rows >= nrows become zeros.
+__device__ __forceinline__ void widen_e4m3_rows(uint32_t src, uint32_t dst, int lane, int nrows) {
+    const int t = lane >> 1, half = lane & 1;
+    const bool live = t < nrows;
+    const uint32_t row = dst + static_cast<uint32_t>(half * kStageTokens + t) * 128;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+        const int c = 4 * half + c4;  // 16 codes: dims 16c .. 16c + 15
+        uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+        if (live)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(src + static_cast<uint32_t>(t) * 128 + ((c ^ (t & 7)) << 4)));
+        const uint32_t a0 = e4m3x2_to_f16x2(w0 & 0xffffu), a1 = e4m3x2_to_f16x2(w0 >> 16);
+        const uint32_t a2 = e4m3x2_to_f16x2(w1 & 0xffffu), a3 = e4m3x2_to_f16x2(w1 >> 16);
+        const uint32_t b0 = e4m3x2_to_f16x2(w2 & 0xffffu), b1 = e4m3x2_to_f16x2(w2 >> 16);
+        const uint32_t b2 = e4m3x2_to_f16x2(w3 & 0xffffu), b3 = e4m3x2_to_f16x2(w3 >> 16);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2 * c4) ^ (t & 7)) << 4)),
+                     "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2 * c4 + 1) ^ (t & 7)) << 4)),
+                     "r"(b0), "r"(b1), "r"(b2), "r"(b3)
+                     : "memory");
+    }
 }
 
 template <typename T> struct Half16;
@@ -794,12 +841,18 @@ constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
 constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
 constexpr int kFlagAppend = 1 << 11; // the stage holds the step's new token: append its K/V first
 
-template <int HPC, int STAGES>
+// FP8: the cache holds E4M3 codes, one 128-byte row per (token, head); each
+// consumer warp widens its head's rows into an f16 scratch tile laid out like
+// the 16-bit tiles, and a per-stage ring holds the (block, head) scales.
+template <int HPC, int STAGES, bool FP8 = false>
 struct StreamSmem {
-    static constexpr int kTileBytes = HPC * 2 * kStageTokens * 128;
+    static constexpr int kTileBytes = FP8 ? HPC * kStageTokens * 128 : HPC * 2 * kStageTokens * 128;
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kTilesBytes = STAGES * kStageBytes;
-    static constexpr int kCtxOffset = kTilesBytes;                        // int32 effective ctx per sequence
+    static constexpr int kScratchOffset = kTilesBytes;                    // FP8: [HPC][2][16][128 B] f16
+    static constexpr int kScaleOffset = kScratchOffset + (FP8 ? HPC * 2 * kStageTokens * 128 : 0);
+    static constexpr int kBatchScaleOffset = kScaleOffset + (FP8 ? STAGES * 2 * HPC * 4 : 0);  // [2][32][2][HPC]
+    static constexpr int kCtxOffset = kBatchScaleOffset + (FP8 ? 2 * 32 * 2 * HPC * 4 : 0);  // int32 ctx per sequence
     static constexpr int kPrefOffset = kCtxOffset + 4 * kMaxStreamSeqs;   // int64 stage prefix per sequence
     static constexpr int kSPrefOffset = kPrefOffset + 8 * (kMaxStreamSeqs + 16);  // int64 static-part prefix
     static constexpr int kInfoOffset = kSPrefOffset + 8 * (kMaxStreamSeqs + 16);
@@ -830,7 +883,7 @@ __device__ __forceinline__ void locate_stage(Pre pre, int B, int HG, int64_t s, 
     st = static_cast<int>(off - hg * n);
 }
 
-template <typename T, int HPC, int STAGES>
+template <typename T, int HPC, int STAGES, bool FP8>
 __global__ void __launch_bounds__((HPC + 1) * 32, 2)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
@@ -839,9 +892,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      float *__restrict__ o_piece, float2 *__restrict__ ml_piece, int4 *__restrict__ unit_info,
                      int32_t *__restrict__ ws_meta, uint32_t *__restrict__ chunk_ctr,
                      const T *__restrict__ new_k, const T *__restrict__ new_v, T *k_cache_w, T *v_cache_w,
+                     const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                      int32_t *__restrict__ err_flag) {
-    using L = StreamSmem<HPC, STAGES>;
-    using H = Half16<T>;
+    using L = StreamSmem<HPC, STAGES, FP8>;
+    using H = Half16<typename std::conditional<FP8, __half, T>::type>;  // FP8 tiles are widened to f16
     const int c = blockIdx.x, C = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ uint8_t smem_raw[];
@@ -853,6 +907,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlagOffset);
     const uint32_t tiles = smem_u32(smem);
+    float *scl = reinterpret_cast<float *>(smem + L::kScaleOffset);  // FP8: [STAGES][2][HPC] K / V scales
+    float *bscl = reinterpret_cast<float *>(smem + L::kBatchScaleOffset);  // FP8: [2 batches][32][2][HPC]
     auto pre_all = [&](int b) { return pref[b]; };
     auto pre_static = [&](int b) { return spref[b]; };
     auto pre_tail = [&](int b) { return pref[b] - spref[b]; };
@@ -971,8 +1027,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         bool bad = false;
         // Stage sb + lane of a batch [sb, se) that lies in segment [lo, hi) of
         // the static region (seg = c) or of the dynamic region (seg = C + k).
+        int cbuf = 0;  // FP8: the batch-scale buffer of the current batch (the next one uses cbuf ^ 1)
         auto describe = [&](int64_t sb, int64_t se, int64_t lo, int64_t hi, int seg, int &b, int &hg,
-                            int &meta, int &id, int &slot_of_piece) {
+                            int &meta, int &id, int &slot_of_piece, int buf) {
             b = hg = meta = slot_of_piece = 0;
             id = -1;
             const int64_t sf = sb + lane;
@@ -1008,6 +1065,16 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
             if (new_k && st == n - 1) flags |= kFlagAppend;  // position ctx - 1 is in this stage
             meta = min(kStageTokens, ctx - pos0) | flags | (pos0 % bs) << 16;
+            if constexpr (FP8) {  // this stage's (block, head) scales, 0 for a block that will be skipped
+                float *dst = bscl + (buf * 32 + lane) * 2 * HPC;
+                const bool ok_id = id >= 0 && id < num_blocks;
+                const int64_t base = (static_cast<int64_t>(id) * HG + hg) * HPC;
+#pragma unroll
+                for (int e = 0; e < HPC; ++e) {
+                    dst[e] = ok_id ? __ldg(k_scale + base + e) : 0.f;
+                    dst[HPC + e] = ok_id ? __ldg(v_scale + base + e) : 0.f;
+                }
+            }
         };
         const uint64_t kv_policy = l2_evict_first_policy();
         // batch bookkeeping (warp-uniform)
@@ -1041,7 +1108,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         int64_t n_sb = 0, n_se = 0, n_lo = 0, n_hi = 0;
         int n_seg = 0;
         bool have = next_batch(c_sb, c_se, c_lo, c_hi, c_seg);
-        if (have) describe(c_sb, c_se, c_lo, c_hi, c_seg, cb, chg, cmeta, cid, cslot);
+        if (have) describe(c_sb, c_se, c_lo, c_hi, c_seg, cb, chg, cmeta, cid, cslot, cbuf);
         g_b = -1;  // the guess covers the first batch only
         bool aborted = false;
         int64_t issued = 0;
@@ -1054,14 +1121,14 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             bool have_next = false, decided = false;
             if (static_next < s1) {
                 have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
-                describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
+                describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot, cbuf ^ 1);
                 decided = true;
             }
             const int cnt = static_cast<int>(c_se - c_sb);
             for (int j = 0; j < cnt; ++j) {
                 if (!decided && cnt - j <= kGrabAhead) {
                     have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
-                    if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot);
+                    if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot, cbuf ^ 1);
                     decided = true;
                 }
                 const int64_t i = issued;
@@ -1111,16 +1178,22 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         meta &= ~0xff;
                     }
                     info[slot] = make_int4(b, hg, meta & 0xffff, pslot);
+                    if constexpr (FP8) {
+                        const float *srcs = bscl + (cbuf * 32 + j) * 2 * HPC;
+#pragma unroll
+                        for (int e = 0; e < 2 * HPC; ++e) scl[slot * 2 * HPC + e] = srcs[e];
+                    }
                     if (id >= 0) {
                         const int slot_row = id * bs + (meta >> 16);
                         const uint32_t dst = tiles + slot * L::kStageBytes;
+                        const int z = FP8 ? hg * HPC : 2 * hg * HPC;  // first head (FP8) or half-row of the box
                         mbar_arrive_expect_tx(full, L::kStageBytes);
                         if (kKvEvictFirst) {
-                            tma_load_3d_hint(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full, kv_policy);
-                            tma_load_3d_hint(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full, kv_policy);
+                            tma_load_3d_hint(dst, &tm_k, 0, slot_row, z, full, kv_policy);
+                            tma_load_3d_hint(dst + L::kTileBytes, &tm_v, 0, slot_row, z, full, kv_policy);
                         } else {
-                            tma_load_3d(dst, &tm_k, 0, slot_row, 2 * hg * HPC, full);
-                            tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, 2 * hg * HPC, full);
+                            tma_load_3d(dst, &tm_k, 0, slot_row, z, full);
+                            tma_load_3d(dst + L::kTileBytes, &tm_v, 0, slot_row, z, full);
                         }
                     } else {
                         mbar_arrive(full);  // nothing to load: the consumers mask the whole stage
@@ -1132,6 +1205,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             have = have_next;
             c_sb = n_sb; c_se = n_se; c_lo = n_lo; c_hi = n_hi; c_seg = n_seg;
             cb = nb; chg = nhg; cmeta = nmeta; cid = nid; cslot = nslot;
+            cbuf ^= 1;
         }
         if (lane == 0) {
             if (!aborted) {
@@ -1163,7 +1237,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // ---------------------------------------------------------------- consumer warp
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, r = lane & 7;
-    const uint32_t head_off = static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
+    // 16-bit caches: this head's rows of the stage tile; FP8: the warp's own
+    // widened tile (the same [2 halves][16 tokens][128 B] swizzled layout)
+    const uint32_t head_off = FP8 ? 0u : static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
+    const uint32_t scratch = smem_u32(smem + L::kScratchOffset) + static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
     uint32_t k_off[8], v_off[8];
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc) {
@@ -1189,6 +1266,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         for (int kc = 0; kc < 8; ++kc) {
             qf[kc][0] = live ? __ldg(q32 + kc * 8 + t) : 0u;
             qf[kc][1] = live ? __ldg(q32 + kc * 8 + 4 + t) : 0u;
+            if constexpr (FP8 && std::is_same<T, __nv_bfloat16>::value) {  // the MMAs run in f16
+                qf[kc][0] = bf16x2_to_f16x2(qf[kc][0]);
+                qf[kc][1] = bf16x2_to_f16x2(qf[kc][1]);
+            }
         }
         q_b = b;
         q_hg = hg;
@@ -1220,20 +1301,34 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
         }
-        const uint32_t kt = tiles + slot * L::kStageBytes;
-        const uint32_t vt = kt + L::kTileBytes;
-        if (nvalid < kStageTokens) {
-            // Rows past the context (or of a skipped block) may hold anything,
-            // NaN included: zero this head's V rows so that 0 * row stays 0.
-            const int nbad = kStageTokens - nvalid;
-            for (int idx = lane; idx < nbad * 16; idx += 32) {
-                const int tok = nvalid + (idx >> 4);
-                const int half = (idx >> 3) & 1;
-                const int chunk = idx & 7;
-                const uint32_t addr = vt + head_off + (half * kStageTokens + tok) * 128 + chunk * 16;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
-            }
+        uint32_t kt, vt;  // K / V tiles the ldmatrix offsets apply to
+        float sl = scale_log2, sv = 1.f;
+        if constexpr (FP8) {
+            // Widen this head's E4M3 rows to f16 in the warp's scratch tile, K
+            // first; V replaces it once the score MMAs have read K.  V rows past
+            // the valid ones become zeros (codes there may be NaN).
+            const uint32_t k8 = tiles + slot * L::kStageBytes + static_cast<uint32_t>(warp) * kStageTokens * 128;
+            sl = scale_log2 * scl[slot * 2 * HPC + warp];
+            sv = scl[slot * 2 * HPC + HPC + warp];
+            widen_e4m3_rows(k8, scratch, lane, kStageTokens);
             __syncwarp();
+            kt = vt = scratch;
+        } else {
+            kt = tiles + slot * L::kStageBytes;
+            vt = kt + L::kTileBytes;
+            if (nvalid < kStageTokens) {
+                // Rows past the context (or of a skipped block) may hold anything,
+                // NaN included: zero this head's V rows so that 0 * row stays 0.
+                const int nbad = kStageTokens - nvalid;
+                for (int idx = lane; idx < nbad * 16; idx += 32) {
+                    const int tok = nvalid + (idx >> 4);
+                    const int half = (idx >> 3) & 1;
+                    const int chunk = idx & 7;
+                    const uint32_t addr = vt + head_off + (half * kStageTokens + tok) * 128 + chunk * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
+                }
+                __syncwarp();
+            }
         }
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1242,11 +1337,19 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             ldsm_x4(kt + k_off[kc], a);
             H::mma(sc, a, qf[kc][0], qf[kc][1]);
         }
+        if constexpr (FP8) {
+            __syncwarp();  // every lane's K reads are done: the scratch takes V
+            widen_e4m3_rows(tiles + slot * L::kStageBytes + L::kTileBytes +
+                                static_cast<uint32_t>(warp) * kStageTokens * 128,
+                            scratch, lane, nvalid);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));  // the stage's bytes are no longer read
+        }
         const bool vg = g < nvalid, vg8 = g + 8 < nvalid;
-        const float x0 = vg ? sc[0] * scale_log2 : -INFINITY;
-        const float x1 = vg ? sc[1] * scale_log2 : -INFINITY;
-        const float x2 = vg8 ? sc[2] * scale_log2 : -INFINITY;
-        const float x3 = vg8 ? sc[3] * scale_log2 : -INFINITY;
+        const float x0 = vg ? sc[0] * sl : -INFINITY;
+        const float x1 = vg ? sc[1] * sl : -INFINITY;
+        const float x2 = vg8 ? sc[2] * sl : -INFINITY;
+        const float x3 = vg8 ? sc[3] * sl : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
@@ -1270,17 +1373,22 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             o[dc][2] *= a0;
             o[dc][3] *= a1;
         }
-        const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+        // FP8: the V scale rides on P (sv = 1 for 16-bit caches); the sums l use P itself
+        const uint32_t pb0 = movmatrix_trans(H::pack(p0 * sv, p1 * sv));
+        const uint32_t pb1 = movmatrix_trans(H::pack(p2 * sv, p3 * sv));
 #pragma unroll
         for (int dc = 0; dc < 8; ++dc) {
             uint32_t a[4];
             ldsm_x4_trans(vt + v_off[dc], a);
             H::mma(o[dc], a, pb0, pb1);
         }
-        if (nvalid < kStageTokens) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));
+        if constexpr (!FP8) {
+            if (nvalid < kStageTokens) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));
+        } else {
+            __syncwarp();  // the next stage's K widening overwrites the scratch
+        }
 
         if (meta & kFlagLast) {
 #pragma unroll
@@ -1527,6 +1635,23 @@ pkv_status make_kv_map(CUtensorMap *map, const void *pool, CUtensorMapDataType t
     return PKV_OK;
 }
 
+// E4M3 pool [num_slots, Hkv, 128] of bytes viewed as (128 codes, num_slots,
+// Hkv heads): one 128-byte row per (token, head), HPC heads per box.
+pkv_status make_kv_map_fp8(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int hpc) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled entry point unavailable");
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kFastHeadDim), static_cast<cuuint64_t>(num_slots),
+                                static_cast<cuuint64_t>(Hkv)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hkv) * kFastHeadDim, kFastHeadDim};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kFastHeadDim), kStageTokens, static_cast<cuuint32_t>(hpc)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PKV_OK;
+}
+
 // cudaFuncSetAttribute once per (kernel, device); `done` is the caller's
 // per-kernel bitmask of devices already configured.
 template <typename K>
@@ -1555,6 +1680,7 @@ struct DecodeArgs {
     int32_t *ws_meta;
     uint32_t *chunk_ctr;
     const void *new_k, *new_v;  // the step's new K/V rows [B, Hkv, d] to append first, or null
+    const float *k_scale, *v_scale;  // E4M3 caches: scales [num_blocks, Hkv]; null for 16-bit caches
     int32_t *err;
     cudaStream_t stream;
 };
@@ -1605,37 +1731,41 @@ int stream_ctas(K kernel, int threads, int smem, std::atomic<int> *per_device) {
     return c;
 }
 
-template <typename T, int HPC, int STAGES>
+template <typename T, int HPC, int STAGES, bool FP8>
 struct StreamLaunch {
     static std::atomic<int> ctas[64];
     static std::atomic<uint64_t> configured;
     static int grid() {
-        using L = StreamSmem<HPC, STAGES>;
-        if (ensure_smem(decode_stream_kernel<T, HPC, STAGES>, L::kAlloc, configured) != cudaSuccess) return 0;
-        return stream_ctas(decode_stream_kernel<T, HPC, STAGES>, (HPC + 1) * 32, L::kAlloc, ctas);
+        using L = StreamSmem<HPC, STAGES, FP8>;
+        if (ensure_smem(decode_stream_kernel<T, HPC, STAGES, FP8>, L::kAlloc, configured) != cudaSuccess) return 0;
+        return stream_ctas(decode_stream_kernel<T, HPC, STAGES, FP8>, (HPC + 1) * 32, L::kAlloc, ctas);
     }
 };
-template <typename T, int HPC, int STAGES> std::atomic<int> StreamLaunch<T, HPC, STAGES>::ctas[64];
-template <typename T, int HPC, int STAGES> std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES>::configured{0};
+template <typename T, int HPC, int STAGES, bool FP8> std::atomic<int> StreamLaunch<T, HPC, STAGES, FP8>::ctas[64];
+template <typename T, int HPC, int STAGES, bool FP8>
+std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES, FP8>::configured{0};
 
-template <typename T, int HPC, int STAGES>
+template <typename T, int HPC, int STAGES, bool FP8>
 pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
-    using L = StreamSmem<HPC, STAGES>;
+    using L = StreamSmem<HPC, STAGES, FP8>;
     CUtensorMap mk, mv;
-    pkv_status st = make_kv_map(&mk, a.k_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    const int64_t slots = static_cast<int64_t>(a.num_blocks) * a.bs;
+    pkv_status st = FP8 ? make_kv_map_fp8(&mk, a.k_cache, slots, a.Hkv, HPC)
+                        : make_kv_map(&mk, a.k_cache, Half16<T>::kTmaType, slots, a.Hkv, HPC);
     if (st != PKV_OK) return st;
-    st = make_kv_map(&mv, a.v_cache, Half16<T>::kTmaType, static_cast<int64_t>(a.num_blocks) * a.bs, a.Hkv, HPC);
+    st = FP8 ? make_kv_map_fp8(&mv, a.v_cache, slots, a.Hkv, HPC)
+             : make_kv_map(&mv, a.v_cache, Half16<T>::kTmaType, slots, a.Hkv, HPC);
     if (st != PKV_OK) return st;
-    const int C = StreamLaunch<T, HPC, STAGES>::grid();
+    const int C = StreamLaunch<T, HPC, STAGES, FP8>::grid();
     if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
     const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
-    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES>, dim3(C), dim3((HPC + 1) * 32), L::kAlloc,
-                               a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
+    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES, FP8>, dim3(C), dim3((HPC + 1) * 32),
+                               L::kAlloc, a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
                                a.chunk_ctr, static_cast<const T *>(a.new_k), static_cast<const T *>(a.new_v),
                                static_cast<T *>(const_cast<void *>(a.k_cache)),
-                               static_cast<T *>(const_cast<void *>(a.v_cache)), a.err);
+                               static_cast<T *>(const_cast<void *>(a.v_cache)), a.k_scale, a.v_scale, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G),
                    dim3(kMergeThreads), 0, a.stream,
@@ -1647,27 +1777,36 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
     return PKV_OK;
 }
 
+// Pipeline depth per (heads per CTA, cache format): about 96 KB of stages
+// (16-bit) or 80 KB plus the f16 scratch (FP8), two CTAs per SM.
 template <typename T>
 pkv_status launch_stream_any(const DecodeArgs &a, const Plan &p) {
+    if (a.k_scale) {
+        switch (p.hpc) {
+        case 4: return launch_stream<T, 4, 5, true>(a, p);
+        case 2: return launch_stream<T, 2, 8, true>(a, p);
+        default: return launch_stream<T, 1, 8, true>(a, p);
+        }
+    }
     switch (p.hpc) {
-    case 4: return launch_stream<T, 4, 3>(a, p);
-    case 2: return launch_stream<T, 2, 6>(a, p);
-    default: return launch_stream<T, 1, 8>(a, p);
+    case 4: return launch_stream<T, 4, 3, false>(a, p);
+    case 2: return launch_stream<T, 2, 6, false>(a, p);
+    default: return launch_stream<T, 1, 8, false>(a, p);
     }
 }
 
 int stream_grid_for(pkv_dtype dt, int hpc) {
     if (dt == PKV_BF16) {
         switch (hpc) {
-        case 4: return StreamLaunch<__nv_bfloat16, 4, 3>::grid();
-        case 2: return StreamLaunch<__nv_bfloat16, 2, 6>::grid();
-        default: return StreamLaunch<__nv_bfloat16, 1, 8>::grid();
+        case 4: return StreamLaunch<__nv_bfloat16, 4, 3, false>::grid();
+        case 2: return StreamLaunch<__nv_bfloat16, 2, 6, false>::grid();
+        default: return StreamLaunch<__nv_bfloat16, 1, 8, false>::grid();
         }
     }
     switch (hpc) {
-    case 4: return StreamLaunch<__half, 4, 3>::grid();
-    case 2: return StreamLaunch<__half, 2, 6>::grid();
-    default: return StreamLaunch<__half, 1, 8>::grid();
+    case 4: return StreamLaunch<__half, 4, 3, false>::grid();
+    case 2: return StreamLaunch<__half, 2, 6, false>::grid();
+    default: return StreamLaunch<__half, 1, 8, false>::grid();
     }
 }
 
@@ -1766,8 +1905,10 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                         int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
                         pkv_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
-                        const void *new_k, const void *new_v) {
+                        const void *new_k, const void *new_v, const float *k_scale = nullptr,
+                        const float *v_scale = nullptr) {
     const int64_t es = dtype_bytes(dtype);
+    const bool fp8 = k_scale != nullptr;  // E4M3 caches with per-(block, head) scales
     if (es == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks < 0 || max_context_len < 0 || max_blocks_per_seq < 0)
@@ -1794,6 +1935,15 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
         return set_error(PKV_ERR_INVALID_ARG, "decode: buffers not aligned to the element size");
     // The fast path additionally wants 16-byte aligned pools (TMA) and 4-byte aligned q.
     const bool fast = p.fast && num_blocks > 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4);
+    if (fp8) {
+        if (!fast || !p.stream || append)
+            return set_error(PKV_ERR_UNSUPPORTED,
+                             "decode fp8: needs fp16/bf16 q, head_dim 128, Hq/Hkv <= 8, block_size a multiple of "
+                             "16, at most %d sequences and 16-byte aligned code pools",
+                             kMaxStreamSeqs);
+        if (!v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+            return set_error(PKV_ERR_INVALID_ARG, "decode fp8: scales NULL or not 4-byte aligned");
+    }
     if (p.fast && !fast) {
         // CUDA-core fallback with partitions that fit the workspace sized for the fast plan.
         const int64_t per_part = static_cast<int64_t>(num_seqs) * num_q_heads * (head_dim * 4 + 8);
@@ -1813,10 +1963,12 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
                  p.stream ? reinterpret_cast<int4 *>(ws + p.o_bytes + p.ml_bytes) : nullptr,
                  p.stream ? reinterpret_cast<int32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes) : nullptr,
                  p.stream ? reinterpret_cast<uint32_t *>(ws + p.o_bytes + p.ml_bytes + p.unit_bytes + 8) : nullptr,
-                 nullptr, nullptr, err_flag, static_cast<cudaStream_t>(stream)};
+                 nullptr, nullptr, nullptr, nullptr, err_flag, static_cast<cudaStream_t>(stream)};
     pkv_status st;
     // The work-balanced kernel appends in its producer warp (8-byte copies);
     // every other path runs the append kernel first, in stream order.
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     const bool fused = append && fast && p.stream && aligned(new_k, 8) && aligned(new_v, 8);
     if (fused) {
         a.new_k = new_k;
@@ -1877,6 +2029,22 @@ extern "C" pkv_status pkv_paged_attention_decode_append(void *out, const void *q
     return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                         num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
                         workspace, workspace_bytes, err_flag, stream, key, value);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                                     const void *v_cache, const float *k_scale, const float *v_scale,
+                                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                     const int32_t *context_lens, int32_t num_seqs,
+                                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                     int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                                     float scale, pkv_dtype dtype, void *workspace,
+                                                     size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    if (num_seqs > 0 && (!k_scale || !v_scale))
+        return set_error(PKV_ERR_INVALID_ARG, "decode fp8: NULL scales");
+    if (dtype == PKV_F32) return set_error(PKV_ERR_UNSUPPORTED, "decode fp8: q/out must be fp16 or bf16");
+    return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
+                        workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, k_scale, v_scale);
 }
 
 // ----------------------------------------------------------------------------- no-allocation variant

@@ -1,0 +1,195 @@
+// E4M3 (fp8) paged caches: quantizing a 16-bit cache and the slot-mapping
+// scatter into an fp8 cache.
+//
+// "Block-Paged KV Cache" (Hurray format documentation), Quantization
+// compatibility: per-block-affine scales with block_size == page_size stay per
+// page slot, so a shared page carries its own scales.  The pages fix only that
+// placement; this library keeps one binary32 scale per (physical block, KV
+// head) for K and one for V ([num_blocks, Hkv]), a stored value being
+// scale * decode(code) with OCP E4M3 codes.  Encoding divides by the scale in
+// binary32 and rounds to the nearest even code, saturating at +-448
+// (cvt.rn.satfinite); a zero scale stores +0.
+//
+// "Paged KV Cache - AI infra interview lesson", Step 1: slot_mapping and
+// store_kvcache -- row slot of the [num_slots, Hkv * d] cache view receives the
+// token's K/V; slot -1 is skipped.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "pkv_internal.h"
+#include "pkv_pdl.cuh"
+
+namespace pkv {
+namespace {
+
+template <typename T> __device__ __forceinline__ float widen(T x);
+template <> __device__ __forceinline__ float widen<float>(float x) { return x; }
+template <> __device__ __forceinline__ float widen<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float widen<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Two binary32 -> two E4M3 codes (lo in the low byte), round to nearest even,
+// saturating; x / s with a zero scale gives +0.
+__device__ __forceinline__ uint32_t encode2(float lo, float hi, float s) {
+    if (s == 0.f) return 0u;
+    const float a = __fdiv_rn(lo, s), b = __fdiv_rn(hi, s);
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
+    return d;
+}
+
+constexpr int kQuantThreads = 128;
+
+// One CTA per (block, head): the block's bs x d values of this head, max |x|
+// (NaN ignored) -> s = max / 448, then every value -> its code.
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales, int32_t bs,
+                    int32_t Hkv, int32_t d) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t blk = blockIdx.x / Hkv;
+    const int h = blockIdx.x - static_cast<int>(blk * Hkv);
+    const int n = bs * d;
+    auto at = [&](int i) -> int64_t {  // element i of (block, head): token i / d, dim i % d
+        return ((blk * bs + i / d) * Hkv + h) * static_cast<int64_t>(d) + i % d;
+    };
+    float m = 0.f;
+    for (int i = threadIdx.x; i < n; i += kQuantThreads) m = fmaxf(m, fabsf(widen(src[at(i)])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
+    const float s = __fdiv_rn(m, 448.f);
+    if (threadIdx.x == 0) scales[blk * Hkv + h] = s;
+    for (int i = 2 * threadIdx.x; i < n; i += 2 * kQuantThreads) {  // d is even: pairs share a token
+        const int64_t e = at(i);
+        const uint32_t c = encode2(widen(src[e]), widen(src[e + 1]), s);
+        codes[e] = static_cast<uint8_t>(c & 0xff);
+        codes[e + 1] = static_cast<uint8_t>(c >> 8);
+    }
+}
+
+constexpr int kStoreThreads = 256;
+
+// One thread per (token, head, pair of dims).
+template <typename T>
+__global__ void __launch_bounds__(kStoreThreads)
+store_fp8_kernel(const T *__restrict__ key, const T *__restrict__ value, uint8_t *__restrict__ k_codes,
+                 uint8_t *__restrict__ v_codes, const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                 const int32_t *__restrict__ slot_mapping, int64_t num_tokens, int32_t Hkv, int32_t d, int32_t bs,
+                 int64_t num_slots, int32_t *__restrict__ err_flag) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t pairs_per_token = static_cast<int64_t>(Hkv) * d / 2;
+    const int64_t total = num_tokens * pairs_per_token;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kStoreThreads + threadIdx.x; w < total;
+         w += static_cast<int64_t>(gridDim.x) * kStoreThreads) {
+        const int64_t i = w / pairs_per_token;
+        const int64_t e = 2 * (w - i * pairs_per_token);  // element within the token's [Hkv, d] row
+        const int32_t slot = __ldg(slot_mapping + i);
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= num_slots) {
+            if (e == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_SLOT_RANGE);
+            continue;
+        }
+        const int h = static_cast<int>(e / d);
+        const int64_t sidx = static_cast<int64_t>(slot / bs) * Hkv + h;
+        const int64_t src = i * Hkv * static_cast<int64_t>(d) + e;
+        const int64_t dst = static_cast<int64_t>(slot) * Hkv * d + e;
+        const uint32_t ck = encode2(widen(key[src]), widen(key[src + 1]), __ldg(k_scale + sidx));
+        const uint32_t cv = encode2(widen(value[src]), widen(value[src + 1]), __ldg(v_scale + sidx));
+        *reinterpret_cast<uint16_t *>(k_codes + dst) = static_cast<uint16_t>(ck);
+        *reinterpret_cast<uint16_t *>(v_codes + dst) = static_cast<uint16_t>(cv);
+    }
+}
+
+int sm_count() {
+    static int count = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        return n;
+    }();
+    return count;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
+                                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                               pkv_dtype dtype, void *stream) {
+    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: unknown dtype %d", (int)dtype);
+    if (num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2)
+        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: bad sizes (head_dim must be even)");
+    if (static_cast<int64_t>(num_blocks) * num_kv_heads > INT32_MAX)
+        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: too many (block, head) pairs");
+    if (num_blocks == 0) return ok();
+    if (!src || !codes || !scales) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: NULL pointer");
+    if (!aligned(src, dtype_bytes(dtype)) || !aligned(codes, 2) || !aligned(scales, 4))
+        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: misaligned buffers");
+    const dim3 grid(static_cast<unsigned>(num_blocks * num_kv_heads));
+    auto s = static_cast<cudaStream_t>(stream);
+    auto c = static_cast<uint8_t *>(codes);
+    cudaError_t e;
+    switch (dtype) {
+    case PKV_BF16:
+        e = launch_pdl(kPdlStore, quantize_fp8_kernel<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, s,
+                       static_cast<const __nv_bfloat16 *>(src), c, scales, block_size, num_kv_heads, head_dim);
+        break;
+    case PKV_F16:
+        e = launch_pdl(kPdlStore, quantize_fp8_kernel<__half>, grid, dim3(kQuantThreads), 0, s,
+                       static_cast<const __half *>(src), c, scales, block_size, num_kv_heads, head_dim);
+        break;
+    default:
+        e = launch_pdl(kPdlStore, quantize_fp8_kernel<float>, grid, dim3(kQuantThreads), 0, s,
+                       static_cast<const float *>(src), c, scales, block_size, num_kv_heads, head_dim);
+        break;
+    }
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize fp8 launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+extern "C" pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                            const float *k_scale, const float *v_scale,
+                                            const int32_t *slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                                            int32_t head_dim, int64_t num_slots, int32_t block_size,
+                                            pkv_dtype dtype, int32_t *err_flag, void *stream) {
+    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "store fp8: unknown dtype %d", (int)dtype);
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2 || num_slots < 0 || block_size <= 0)
+        return set_error(PKV_ERR_INVALID_ARG, "store fp8: bad sizes (head_dim must be even)");
+    if (num_tokens == 0) return ok();
+    if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+        return set_error(PKV_ERR_INVALID_ARG, "store fp8: NULL pointer");
+    if (!aligned(key, dtype_bytes(dtype)) || !aligned(value, dtype_bytes(dtype)) || !aligned(k_cache, 2) ||
+        !aligned(v_cache, 2) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return set_error(PKV_ERR_INVALID_ARG, "store fp8: misaligned buffers");
+    const int64_t total = num_tokens * num_kv_heads * head_dim / 2;
+    int64_t grid = (total + kStoreThreads - 1) / kStoreThreads;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    if (grid > cap) grid = cap;
+    auto s = static_cast<cudaStream_t>(stream);
+    auto kc = static_cast<uint8_t *>(k_cache);
+    auto vc = static_cast<uint8_t *>(v_cache);
+    cudaError_t e;
+#define PKV_STORE_FP8(T)                                                                                             \
+    launch_pdl(kPdlStore, store_fp8_kernel<T>, dim3(static_cast<unsigned>(grid)), dim3(kStoreThreads), 0, s,        \
+               static_cast<const T *>(key), static_cast<const T *>(value), kc, vc, k_scale, v_scale, slot_mapping, \
+               num_tokens, num_kv_heads, head_dim, block_size, num_slots, err_flag)
+    switch (dtype) {
+    case PKV_BF16: e = PKV_STORE_FP8(__nv_bfloat16); break;
+    case PKV_F16: e = PKV_STORE_FP8(__half); break;
+    default: e = PKV_STORE_FP8(float); break;
+    }
+#undef PKV_STORE_FP8
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "store fp8 launch: %s", cudaGetErrorString(e));
+    return ok();
+}
