@@ -348,7 +348,7 @@ PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, in
  *   and the products run on f16 tensor cores (q is rounded to f16 once;
  *   values beyond 65504 overflow).  Only the tensor-core, work-balanced
  *   shapes run: head_dim 128, num_q_heads / num_kv_heads <= 8, block_size a
- *   multiple of 16, at most 512 sequences, 16-byte aligned code pools;
+ *   multiple of 16, at most 512 sequences, 16-byte aligned q and code pools;
  *   others return PKV_ERR_UNSUPPORTED.
  */
 PKV_API pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
