@@ -63,6 +63,9 @@ def parse_args(argv=None):
                     help="wall-clock budget of the oracle CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true",
                     help="omit the oracle timing (for profiler runs)")
+    ap.add_argument("--profile-calls", choices=["decode", "fp8"], default=None,
+                    help="profiler driver: run --steps decode-attention calls (16-bit or E4M3 caches) of the "
+                         "workload back to back, eagerly, and exit without timing")
     return ap.parse_args(argv)
 
 
@@ -710,12 +713,36 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_profile_calls(args, local):
+    """The workload's attention calls only, for an ncu capture of one launch."""
+    import pagedattention_decode_pkv_gb300 as pkv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    step = DecodeStep(pkv, wl.CONFIGS[args.config], seed=args.seed, device=device)
+    call = step.attention
+    if args.profile_calls == "fp8":
+        step.make_fp8()
+        call = step.fp8_attention
+    ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(args.steps):
+        if call(ptr) != 0:
+            raise RuntimeError("pkv call failed: " + pkv._lib.pkv_last_error_string().decode())
+    torch.cuda.synchronize()
+    if int(step.err.item()):
+        raise RuntimeError(f"device error bits {int(step.err.item()):#x}")
+    print(f"{args.steps} {args.profile_calls} calls on {args.config}", flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_init(args)
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.profile_calls:
+            return run_profile_calls(args, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:
