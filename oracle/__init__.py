@@ -80,6 +80,9 @@ def _load():
             lib.orc_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
                                                            i32, i32, i32, i32, dbl, ctypes.c_int]
             lib.orc_paged_attention_decode_fp8.restype = i64
+            lib.orc_paged_attention_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                                        i32, i32, dbl, ctypes.c_int]
+            lib.orc_paged_attention_prefill.restype = i64
             _lib = lib
     return _lib
 
@@ -217,6 +220,25 @@ def paged_attention_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tabl
     err = _load().orc_paged_attention_decode_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
                                                  _ptr(bt), bt.shape[1] if bt.dim() == 2 else 0, _ptr(cl), B, Hq,
                                                  Hkv, d, bs, nb, float(scale), _DTYPE_CODE[q.dtype])
+    return out, err
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, starts, cu_q, scale: float):
+    """Causal prefill attention over the paged cache: q [cu_q[-1], Hq, d], the
+    queries of sequence b at positions starts[b] + i.  Binary64 output of q's
+    shape and the error count."""
+    q, kc, vc = _cpu(q), _cpu(k_cache), _cpu(v_cache)
+    assert q.dtype == kc.dtype == vc.dtype
+    bt = _cpu(block_tables, torch.int32)
+    st = _cpu(starts, torch.int32).reshape(-1)
+    cu = _cpu(cu_q, torch.int32).reshape(-1)
+    Tq, Hq, d = q.shape
+    nb, bs, Hkv, d2 = kc.shape
+    assert d2 == d and Hq % Hkv == 0 and cu.numel() == st.numel() + 1
+    out = torch.empty(Tq, Hq, d, dtype=torch.float64)
+    err = _load().orc_paged_attention_prefill(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt),
+                                              bt.shape[1] if bt.dim() == 2 else 0, _ptr(st), _ptr(cu), st.numel(),
+                                              Hq, Hkv, d, bs, nb, float(scale), _DTYPE_CODE[q.dtype])
     return out, err
 
 

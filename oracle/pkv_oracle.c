@@ -498,3 +498,79 @@ int64_t orc_paged_attention_decode_fp8(double *out, const void *q, const uint8_t
     }
     return errors;
 }
+
+/* ---------------------------------------------------------------------------
+ * [P3] "Step 3: varlen attention and cu_seqlens" names prefill attention over
+ * sequences of different lengths and gives no further content.  Reading (the
+ * plain one the rest of the page supports): sequence b's new tokens occupy
+ * positions [start_b, start_b + n_b), n_b = cu_q[b+1] - cu_q[b]; their K/V are
+ * already in the paged cache (stored by "Step 1"), as are the K/V of positions
+ * [0, start_b) (a cached prefix or earlier chunks).  Query i of sequence b sits
+ * at position p = start_b + i and attends causally over positions 0 .. p
+ * through the block table:
+ *     out[cu_q[b] + i, h] = softmax_{t <= p}(scale * q . K[t]) . V[t],
+ * query head h reading KV head h / (Hq / H_kv).  Binary64 throughout.
+ * Readings for bad input: a sequence whose last position needs a table entry
+ * past max_blocks, or with start_b < 0, gives zero rows and is counted; a used
+ * block id outside [0, num_blocks) drops that block's tokens and is counted
+ * once per (sequence, block). */
+int64_t orc_paged_attention_prefill(double *out, const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
+                                    const int32_t *cu_q, int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t bs, int32_t num_blocks,
+                                    double scale, int dtype)
+{
+    int64_t errors = 0;
+    int32_t group = num_q_heads / num_kv_heads;
+    build_f16_table();
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int64_t n = (int64_t)cu_q[b + 1] - cu_q[b];
+        int64_t start = starts[b];
+        int64_t total = start + n;
+        const int32_t *row = block_tables + (int64_t)b * max_blocks;
+        int bad = n < 0 || start < 0 || (total + bs - 1) / bs > max_blocks;
+        if (bad) ++errors;
+        if (!bad) {
+            for (int64_t j = 0; j < (total + bs - 1) / bs; ++j)
+                if (row[j] < 0 || row[j] >= num_blocks) ++errors;
+        }
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(total > 0 ? total : 1));
+        for (int64_t i = 0; i < (n > 0 ? n : 0); ++i) {
+            int64_t p = start + i;
+            for (int32_t h = 0; h < num_q_heads; ++h) {
+                int32_t g = h / group;
+                double *o = out + (((int64_t)cu_q[b] + i) * num_q_heads + h) * head_dim;
+                int64_t q_base = (((int64_t)cu_q[b] + i) * num_q_heads + h) * head_dim;
+                double m = -INFINITY, l = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+                if (bad) continue;
+                for (int64_t t = 0; t <= p; ++t) {
+                    int32_t phys = row[t / bs];
+                    scores[t] = -INFINITY;
+                    if (phys < 0 || phys >= num_blocks) continue;
+                    int64_t k_base = (((int64_t)phys * bs + t % bs) * num_kv_heads + g) * head_dim;
+                    double s = 0.0;
+                    for (int32_t d = 0; d < head_dim; ++d)
+                        s += load_elem(q, q_base + d, dtype) * load_elem(k_cache, k_base + d, dtype);
+                    scores[t] = scale * s;
+                    if (scores[t] > m) m = scores[t];
+                }
+                if (m == -INFINITY) continue;
+                for (int64_t t = 0; t <= p; ++t) {
+                    if (scores[t] == -INFINITY) continue;
+                    scores[t] = exp(scores[t] - m);
+                    l += scores[t];
+                }
+                for (int64_t t = 0; t <= p; ++t) {
+                    if (scores[t] == -INFINITY) continue;
+                    int32_t phys = row[t / bs];
+                    int64_t v_base = (((int64_t)phys * bs + t % bs) * num_kv_heads + g) * head_dim;
+                    double w = scores[t] / l;
+                    for (int32_t d = 0; d < head_dim; ++d) o[d] += w * load_elem(v_cache, v_base + d, dtype);
+                }
+            }
+        }
+        free(scores);
+    }
+    return errors;
+}

@@ -474,3 +474,75 @@ def test_attention_fp8_matches_sdpa_on_dequantized_kv(orc):
         Ks.append(torch.stack([dk[p, o] for p, o in rows]))
         Vs.append(torch.stack([dv[p, o] for p, o in rows]))
     torch.testing.assert_close(out, _sdpa_reference(q, Ks, Vs, Hq, Hkv, d ** -0.5), atol=1e-12, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------- varlen / chunked prefill
+def _prefill_case(bs, Hq, Hkv, d, spans, nb, seed, dtype=torch.float32):
+    """spans: (start, n) per sequence; contiguous K/V of length start + n are
+    scattered into random blocks; q holds the n queries of each sequence."""
+    g = torch.Generator().manual_seed(seed)
+    kc = torch.randn(nb, bs, Hkv, d, generator=g).to(dtype)
+    vc = torch.randn(nb, bs, Hkv, d, generator=g).to(dtype)
+    free = torch.randperm(nb, generator=g).tolist()
+    tables, Ks, Vs = [], [], []
+    for start, n in spans:
+        L = start + n
+        bt = [free.pop() for _ in range((L + bs - 1) // bs)]
+        K, V = torch.randn(L, Hkv, d, generator=g).to(dtype), torch.randn(L, Hkv, d, generator=g).to(dtype)
+        for p in range(L):
+            kc[bt[p // bs], p % bs], vc[bt[p // bs], p % bs] = K[p], V[p]
+        tables.append(bt)
+        Ks.append(K)
+        Vs.append(V)
+    M = max(1, max(len(t) for t in tables))
+    block_tables = torch.tensor([t + [-1] * (M - len(t)) for t in tables], dtype=torch.int32)
+    starts = torch.tensor([s for s, _ in spans], dtype=torch.int32)
+    cu = torch.zeros(len(spans) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor([n for _, n in spans]), 0)
+    q = torch.randn(int(cu[-1]), Hq, d, generator=g).to(dtype)
+    return q, kc, vc, block_tables, starts, cu, Ks, Vs
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+def test_prefill_matches_sdpa_with_causal_mask(orc, bs):
+    """Against SDPA (binary64) on the same K/V stored contiguously, with the
+    mask key <= query position, for a plain prefill, chunks after a cached
+    prefix, a single new token and block-straddling spans."""
+    Hq, Hkv, d = 4, 2, 8
+    spans = [(0, 2 * bs + 3), (bs + 1, 5), (3 * bs, bs), (7, 1), (0, 1)]
+    q, kc, vc, bt, st, cu, Ks, Vs = _prefill_case(bs, Hq, Hkv, d, spans, 40, seed=bs + 60)
+    out, err = orc.paged_attention_prefill(q, kc, vc, bt, st, cu, d ** -0.5)
+    assert err == 0
+    for b, (start, n) in enumerate(spans):
+        L = start + n
+        K = Ks[b].double().repeat_interleave(Hq // Hkv, 1).transpose(0, 1)  # [Hq, L, d]
+        V = Vs[b].double().repeat_interleave(Hq // Hkv, 1).transpose(0, 1)
+        Q = q[int(cu[b]):int(cu[b + 1])].double().transpose(0, 1)            # [Hq, n, d]
+        mask = torch.arange(L)[None, :] <= (start + torch.arange(n))[:, None]
+        ref = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=d ** -0.5).transpose(0, 1)
+        torch.testing.assert_close(out[int(cu[b]):int(cu[b + 1])], ref, atol=1e-12, rtol=1e-12)
+
+
+def test_prefill_last_query_equals_decode(orc):
+    """The last new token of a sequence sees its whole context: the prefill
+    row equals the (separately pinned) decode attention over start + n tokens."""
+    bs, Hq, Hkv, d = 16, 8, 2, 16
+    spans = [(40, 9), (0, 33), (16, 16)]
+    q, kc, vc, bt, st, cu, _, _ = _prefill_case(bs, Hq, Hkv, d, spans, 30, seed=61, dtype=torch.bfloat16)
+    out, err = orc.paged_attention_prefill(q, kc, vc, bt, st, cu, 0.3)
+    last = cu[1:] - 1
+    dec, derr = orc.paged_attention_decode(q[last], kc, vc, bt, st + (cu[1:] - cu[:-1]), 0.3)
+    assert err == 0 == derr
+    torch.testing.assert_close(out[last], dec, atol=1e-12, rtol=1e-12)
+
+
+def test_prefill_bad_inputs_zero_rows_and_count(orc):
+    bs, Hq, Hkv, d = 4, 2, 1, 4
+    q, kc, vc, bt, st, cu, _, _ = _prefill_case(bs, Hq, Hkv, d, [(2, 3), (0, 4)], 8, seed=62)
+    bt2 = bt.clone()
+    bt2[1, 0] = 99  # sequence 1's only block is outside the pool: all its keys dropped
+    out, err = orc.paged_attention_prefill(q, kc, vc, bt2, st, cu, 0.5)
+    assert err == 1 and torch.count_nonzero(out[3:]) == 0
+    st3 = torch.tensor([-1, 0], dtype=torch.int32)  # a negative start: zero rows, counted
+    out, err = orc.paged_attention_prefill(q, kc, vc, bt, st3, cu, 0.5)
+    assert err == 1 and torch.count_nonzero(out[:3]) == 0
