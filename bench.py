@@ -149,6 +149,14 @@ def measured_hbm_peak():
         return HBM_FALLBACK_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def profiled_traffic(kernel_key: str, units: float):
     """DRAM bytes per launch from a committed ncu summary, scaled to `units`,
     or None when the summary was taken on a different kernel source."""
@@ -479,6 +487,42 @@ def time_host_allocator(pkv, step: DecodeStep, steps: int = 200):
     return dt / steps * 1e6
 
 
+PREFILL_NEW_TOKENS = 512
+
+
+def time_prefill(step: DecodeStep, calls: int, world: int):
+    """Chunked prefill on the workload's own cache: every sequence's last
+    min(ctx, 512) positions are taken as the new tokens of a prefill chunk
+    (fresh random queries) and attend causally over their whole context.
+    Calls back to back in a CUDA graph.  Returns (ms per call, algorithmic
+    FLOPs per call, queries): 2 d flops for q.k and 2 d for p.v per (query,
+    key) pair and query head."""
+    pkv, b, c = step.pkv, step.batch, step.cfg
+    ctx = b.context_lens.cpu().to(torch.int64)
+    ns = ctx.clamp(max=PREFILL_NEW_TOKENS)
+    starts = (ctx - ns).to(torch.int32)
+    cu = torch.zeros(step.B + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(ns, 0).to(torch.int32)
+    nq = int(cu[-1])
+    pairs = int(sum(int(n) * int(s) + int(n) * (int(n) + 1) // 2 for s, n in zip(starts, ns)))
+    flops = pairs * 4 * c.head_dim * c.num_q_heads
+    g = torch.Generator(device=step.device).manual_seed(11)
+    q = torch.randn(nq, c.num_q_heads, c.head_dim, generator=g, device=step.device).to(c.dtype)
+    out = torch.empty_like(q)
+    st, cud = starts.to(step.device), cu.to(step.device)
+    L, p = pkv._lib, lambda t: t.data_ptr()
+    mq = int(ns.max())
+
+    def call(ptr):
+        return L.pkv_paged_attention_prefill(p(out), p(q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
+                                             b.block_tables.shape[1], p(st), p(cud), step.B, mq, c.num_q_heads,
+                                             c.num_kv_heads, c.head_dim, c.block_size, step.nb, b.scale, step.dt,
+                                             p(step.err), ptr)
+
+    ms, n = time_attention_sustained(step, calls, world, call)
+    return ms, flops, nq
+
+
 def e2e_io(step: DecodeStep):
     pairs = step.host_inputs()
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
@@ -612,6 +656,8 @@ def run_ours(args, world, rank, local):
     fp8_ms, _ = time_attention_sustained(step, args.steps, world, step.fp8_attention)
     fp8_tok_s = reduce_sum(cfg.batch / (fp8_ms * 1e-3), world, device)
     fp8_ms = reduce_max(fp8_ms, world, device)
+    pre_ms, pre_flops, pre_q = time_prefill(step, max(10, args.steps // 20), world)
+    pre_ms = reduce_max(pre_ms, world, device)
     alloc_us = time_host_allocator(pkv, step)
     fused_tok_s = reduce_sum(cfg.batch / (fused_ms * 1e-3), world, device)
     fused_ms = reduce_max(fused_ms, world, device)
@@ -627,6 +673,7 @@ def run_ours(args, world, rank, local):
     e2e_value = all_bytes / (e2e_ms_max * 1e-3) / 1e9
 
     peak, peak_kind = measured_hbm_peak()
+    bf16_peak, bf16_kind = measured_bf16_peak()
     attn_ms = per["paged_attention_decode"]
     attn_percall_gbs = step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9
     sus_ms = reduce_max(sus_ms, world, device)
@@ -692,6 +739,14 @@ def run_ours(args, world, rank, local):
             "frac_of_peak": round(fp8_bytes / (fp8_ms * 1e-3) / 1e9 / peak, 4),
             "tokens_per_s": round(fp8_tok_s, 1),
             "speedup_vs_16bit": round(sus_ms / fp8_ms, 3)},
+        "prefill": {
+            "what": f"pkv_paged_attention_prefill: each sequence's last min(ctx, {PREFILL_NEW_TOKENS}) positions as a "
+                    "prefill chunk over its own paged context (causal), back to back in CUDA graphs",
+            "queries": pre_q, "us_per_call": round(pre_ms * 1e3, 2),
+            "roofline": {"bound": "tensor", "achieved": round(pre_flops / (pre_ms * 1e-3) / 1e12, 2),
+                         "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(pre_flops / (pre_ms * 1e-3) / 1e12 / bf16_peak, 4),
+                         "peak_kind": bf16_kind, "flops_per_call": pre_flops}},
         "host_allocator_us_per_step": None if alloc_us is None else round(alloc_us, 1),
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

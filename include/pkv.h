@@ -322,6 +322,41 @@ PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, in
                                           int64_t *flat_out);
 
 /*
+ * pkv_paged_attention_prefill -- causal varlen / chunked prefill over the paged
+ * cache ("Paged KV Cache - AI infra interview lesson": Step 3, varlen
+ * attention and cu_seqlens, is named there without content; the reading here
+ * is the plain one its Steps 1 and 2 support).  Sequence b's new tokens sit
+ * at positions [starts[b], starts[b] + n_b), n_b = cu_q[b+1] - cu_q[b], and
+ * their K/V are already stored in the caches (pkv_compute_slot_mapping over
+ * that range + pkv_store_kvcache), as are those of positions [0, starts[b])
+ * (a cached prefix or earlier chunks).  For query i of sequence b, at position
+ * p = starts[b] + i, and query head h:
+ *   out[cu_q[b] + i, h] = softmax_{t <= p}(scale * q[cu_q[b] + i, h] . K_t) . V_t
+ * with K_t / V_t read through the block table and KV head h / (Hq / Hkv).
+ *
+ *   out, q         device [cu_q[num_seqs], num_q_heads, head_dim] (dtype)
+ *   starts         device int32 [num_seqs], first new position per sequence
+ *   cu_q           device int32 [num_seqs + 1], offsets of each sequence's queries
+ *   max_q_len      host bound on n_b (sizes the grid)
+ *   caches, block_tables, num_blocks as in pkv_paged_attention_decode.
+ * fp32 accumulation, one rounding to dtype.  Tensor cores (mma.sync): fp16 or
+ * bf16, head_dim 128, num_q_heads / num_kv_heads in {1, 2, 4, 8}, block_size a
+ * multiple of 16, 16-byte aligned pools; other shapes return
+ * PKV_ERR_UNSUPPORTED.  No workspace.
+ * Device errors: starts[b] < 0 or a span needing more than max_blocks_per_seq
+ * blocks gives zero rows and PKV_ERRBIT_CONTEXT; n_b < 0 or n_b > max_q_len
+ * sets PKV_ERRBIT_CONTEXT (rows past max_q_len are not written); a used block
+ * id outside [0, num_blocks) drops that block's tokens and sets
+ * PKV_ERRBIT_BLOCK_RANGE.
+ */
+PKV_API pkv_status pkv_paged_attention_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                               const int32_t *starts, const int32_t *cu_q, int32_t num_seqs,
+                                               int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                               float scale, pkv_dtype dtype, int32_t *err_flag, void *stream);
+
+/*
  * fp8 (E4M3) paged caches -- "Block-Paged KV Cache", Quantization
  * compatibility: per-block-affine scales with block_size == page_size stay per
  * page slot, so a shared page carries its own scales.  The pages give that

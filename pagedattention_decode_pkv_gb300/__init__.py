@@ -58,6 +58,8 @@ _SIGS = {
     "pkv_validate_block_paged_shape": ([_vp, _i32, _i32, _i32], ctypes.c_int),
     "pkv_block_paged_element_offset": ([_i64, _i64, _i64, _i64, _i32, _i64, _i32, _i32, _vp, _vp, ctypes.c_int,
                                         _i64, _vp], ctypes.c_int),
+    "pkv_paged_attention_prefill": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                     _i32, _f32, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_quantize_kvcache_fp8": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_int, _vp], ctypes.c_int),
     "pkv_store_kvcache_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i32, ctypes.c_int, _vp,
                                _vp], ctypes.c_int),
@@ -303,6 +305,31 @@ def pkv_block_paged_element_offset(seq, token, head, dim, page_size, num_pages, 
                                                _ptr(bt), _ptr(sp), _INDEX[sp.dtype], sp.numel() - 1,
                                                ctypes.byref(flat)))
     return flat.value
+
+
+def pkv_paged_attention_prefill(q, k_cache, v_cache, block_tables, starts, cu_q, scale: float, max_q_len: int, *,
+                                out=None, err_flag=None, stream=None):
+    """Causal prefill: query i of sequence b (row cu_q[b] + i of q, position
+    starts[b] + i) attends over positions 0 .. starts[b] + i of its paged context."""
+    dev = _dev(q, k_cache, v_cache, block_tables, starts, cu_q, out, err_flag)
+    _want(block_tables, torch.int32, "block_tables")
+    _want(starts, torch.int32, "starts")
+    _want(cu_q, torch.int32, "cu_q")
+    if q.dtype not in _DTYPE or not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and caches must share one of float32/float16/bfloat16")
+    Tq, Hq, d = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    B = starts.numel()
+    if cu_q.numel() != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    with torch.cuda.device(dev):
+        _check(_lib.pkv_paged_attention_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                                block_tables.shape[1], _ptr(starts), _ptr(cu_q), B, max_q_len, Hq,
+                                                Hkv, d, bs, nb, float(scale), _DTYPE[q.dtype], _ptr(err_flag),
+                                                _stream(dev, stream)))
+    return out
 
 
 # ----------------------------------------------------------------------------- fp8 (E4M3) caches
