@@ -63,7 +63,7 @@ def parse_args(argv=None):
                     help="wall-clock budget of the oracle CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true",
                     help="omit the oracle timing (for profiler runs)")
-    ap.add_argument("--profile-calls", choices=["decode", "fp8"], default=None,
+    ap.add_argument("--profile-calls", choices=["decode", "fp8", "prefill"], default=None,
                     help="profiler driver: run --steps decode-attention calls (16-bit or E4M3 caches) of the "
                          "workload back to back, eagerly, and exit without timing")
     return ap.parse_args(argv)
@@ -490,13 +490,12 @@ def time_host_allocator(pkv, step: DecodeStep, steps: int = 200):
 PREFILL_NEW_TOKENS = 512
 
 
-def time_prefill(step: DecodeStep, calls: int, world: int):
+def prefill_call(step: DecodeStep):
     """Chunked prefill on the workload's own cache: every sequence's last
     min(ctx, 512) positions are taken as the new tokens of a prefill chunk
     (fresh random queries) and attend causally over their whole context.
-    Calls back to back in a CUDA graph.  Returns (ms per call, algorithmic
-    FLOPs per call, queries): 2 d flops for q.k and 2 d for p.v per (query,
-    key) pair and query head."""
+    Returns (enqueue function, algorithmic FLOPs per call, queries): 2 d flops
+    for q.k and 2 d for p.v per (query, key) pair and query head."""
     pkv, b, c = step.pkv, step.batch, step.cfg
     ctx = b.context_lens.cpu().to(torch.int64)
     ns = ctx.clamp(max=PREFILL_NEW_TOKENS)
@@ -519,7 +518,14 @@ def time_prefill(step: DecodeStep, calls: int, world: int):
                                              c.num_kv_heads, c.head_dim, c.block_size, step.nb, b.scale, step.dt,
                                              p(step.err), ptr)
 
-    ms, n = time_attention_sustained(step, calls, world, call)
+    step.prefill_buffers = (q, out, st, cud)  # kept alive with the step
+    return call, flops, nq
+
+
+def time_prefill(step: DecodeStep, calls: int, world: int):
+    """prefill_call back to back in CUDA graphs: (ms per call, FLOPs per call, queries)."""
+    call, flops, nq = prefill_call(step)
+    ms, _ = time_attention_sustained(step, calls, world, call)
     return ms, flops, nq
 
 
@@ -779,6 +785,8 @@ def run_profile_calls(args, local):
     if args.profile_calls == "fp8":
         step.make_fp8()
         call = step.fp8_attention
+    elif args.profile_calls == "prefill":
+        call = prefill_call(step)[0]
     ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for _ in range(args.steps):
         if call(ptr) != 0:

@@ -14,14 +14,16 @@
 // KV head: 64 / G positions x the G query heads of the group, so every K/V
 // byte it stages serves all G heads.  A producer warp streams 16-token K and V
 // tiles of that head through a TMA -> shared-memory ring (the decode path's
-// 3-D tensor map with one head per box, 128-byte swizzle).  Four consumer
-// warps hold 16 query rows each as mma A fragments and, per stage, compute
-// S = Q K^T (16 MMAs: ldmatrix of K as the B operand), the online softmax
-// on the accumulators (row statistics over the quad of lanes sharing a row),
-// and O += P V (16 MMAs: P re-used from the accumulator layout as the A
-// operand, V through ldmatrix.trans).  Grid (B, H_kv, query tiles) with the
-// tile index counted from the end of each sequence, so the longest tiles
-// (most keys) launch first.
+// 3-D tensor map with one head per box, 128-byte swizzle).  The Q rows sit in
+// shared memory (swizzled 256-byte rows), which keeps the consumers at 128
+// registers and three CTAs per SM.  Four consumer warps take 16 rows each
+// and, per stage, compute S = Q K^T (16 MMAs in four independent chains:
+// ldmatrix of Q as A and of K as B), the online softmax on the accumulators
+// (row statistics over the quad of lanes sharing a row), and O += P V (16
+// MMAs: P re-used from the accumulator layout as the A operand, V through
+// ldmatrix.trans).  Grid (B, H_kv, query tiles) with the tile index counted
+// from the end of each sequence, so the longest tiles (most keys) launch
+// first.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -43,14 +45,15 @@ constexpr float kPreLog2e = 1.4426950408889634f;
 
 struct PreSmem {
     static constexpr int kStageBytes = 2 * kPreTile;           // K then V
-    static constexpr int kIdOffset = kPreStages * kStageBytes;  // int32 block id per ring slot (-1: skipped)
+    static constexpr int kQOffset = kPreStages * kStageBytes;   // Q rows [64][256 B], chunks swizzled by row
+    static constexpr int kIdOffset = kQOffset + kPreRows * 256;  // int32 block id per ring slot (-1: skipped)
     static constexpr int kBarOffset = kIdOffset + 16 * kPreStages;
     static constexpr int kBytes = kBarOffset + 16 * kPreStages;
     static constexpr int kAlloc = kBytes + 1024;
 };
 
 template <typename T>
-__global__ void __launch_bounds__((kPreWarps + 1) * 32)
+__global__ void __launch_bounds__((kPreWarps + 1) * 32, 3)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                int32_t max_blocks, const int32_t *__restrict__ starts, const int32_t *__restrict__ cu_q,
@@ -156,17 +159,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const bool live0 = q0 + r0 / G < n, live1 = q0 + r1 / G < n;
     const int64_t qrow0 = (static_cast<int64_t>(q_begin) + q0 + r0 / G) * Hq + kh * G + r0 % G;
     const int64_t qrow1 = (static_cast<int64_t>(q_begin) + q0 + r1 / G) * Hq + kh * G + r1 % G;
-    uint32_t qa[8][4];  // A fragments of Q: rows g / g+8, dims 16kc + 2t (+8)
+    // Q rows of this warp into shared memory (zeros past the sequence): lane l
+    // copies half l & 1 of row l >> 1; 16-byte chunk c of row r sits at c ^ (r & 7)
+    const uint32_t qs = smem_u32(smem + L::kQOffset);
     {
-        const uint32_t *q0p = reinterpret_cast<const uint32_t *>(q + qrow0 * kFastHeadDim);
-        const uint32_t *q1p = reinterpret_cast<const uint32_t *>(q + qrow1 * kFastHeadDim);
+        const int rw = lane >> 1, hf = lane & 1, r = 16 * warp + rw;
+        const bool live = q0 + r / G < n;
+        const int4 *src = reinterpret_cast<const int4 *>(
+            q + ((static_cast<int64_t>(q_begin) + q0 + r / G) * Hq + kh * G + r % G) * kFastHeadDim);
 #pragma unroll
-        for (int kc = 0; kc < 8; ++kc) {
-            qa[kc][0] = live0 ? __ldg(q0p + kc * 8 + t) : 0u;
-            qa[kc][1] = live1 ? __ldg(q1p + kc * 8 + t) : 0u;
-            qa[kc][2] = live0 ? __ldg(q0p + kc * 8 + 4 + t) : 0u;
-            qa[kc][3] = live1 ? __ldg(q1p + kc * 8 + 4 + t) : 0u;
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const int c = 8 * hf + c8;
+            const int4 v = live ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(qs + r * 256 + ((c ^ (r & 7)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
         }
+        __syncwarp();
+    }
+    uint32_t q_off[8];  // A fragments by ldmatrix: rows (lane & 7) + 8 ((lane >> 3) & 1), dims 16kc + 8 (lane >> 4)
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+        const int r = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1), c = 2 * kc + (lane >> 4);
+        q_off[kc] = qs + r * 256 + ((c ^ (r & 7)) << 4);
     }
     // ldmatrix lane addresses inside a stage: K (B operand, non-transposed): matrix
     // m = lane >> 3 covers keys 8 (m >> 1) .. +7 and dims 16kc + 8 (m & 1) .. +7;
@@ -214,14 +229,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 }
                 __syncwarp();
             }
+            // four independent accumulation chains (key halves x even / odd k-steps)
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-            for (int kc = 0; kc < 8; ++kc) {
-                uint32_t bk[4];
+            for (int kc = 0; kc < 8; kc += 2) {
+                uint32_t bk[4], bk2[4], qa[4], qb[4];
+                ldsm_x4(q_off[kc], qa);
+                ldsm_x4(q_off[kc + 1], qb);
                 ldsm_x4(kt + k_off[kc], bk);  // (keys 0-7: dims lo, hi), (keys 8-15: dims lo, hi)
-                H::mma(sc[0], qa[kc], bk[0], bk[1]);
-                H::mma(sc[1], qa[kc], bk[2], bk[3]);
+                ldsm_x4(kt + k_off[kc + 1], bk2);
+                H::mma(sc[0], qa, bk[0], bk[1]);
+                H::mma(sc[1], qa, bk[2], bk[3]);
+                H::mma(sd[0], qb, bk2[0], bk2[1]);
+                H::mma(sd[1], qb, bk2[2], bk2[3]);
             }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
             // scores of keys kbase + 8 nt + 2t + {0, 1}, rows pos0 / pos1; causal mask
             float x[2][4];
 #pragma unroll
