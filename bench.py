@@ -164,10 +164,11 @@ def profiled_traffic(kernel_key: str, units: float):
     try:
         with open(path) as f:
             rec = json.load(f)[kernel_key]
-        src = os.path.join(ROOT, rec["source"])
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if sha != rec["source_sha256"]:
+        h = hashlib.sha256()  # every source file of the kernel, in the listed order
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
             return None
         return rec["dram_bytes_per_unit"] * units
     except (OSError, KeyError, ValueError, TypeError):
