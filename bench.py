@@ -278,6 +278,31 @@ class DecodeStep:
         combine = self.plan[2] and self.plan[0] == 0 or self.plan[1] > 1
         self.launches_per_step = 1 + 1 + (2 if combine else 1) + 2
 
+    def input_sets(self):
+        """Two sets of the step's per-step device inputs (and outputs), so a
+        pipelined loop can copy step i+1's inputs while step i runs: set 0 is
+        the batch's own tensors, set 1 a copy; the caches are shared."""
+        if not hasattr(self, "_sets"):
+            from dataclasses import replace
+
+            b, s = self.batch, self.snap
+            b1 = replace(b, q=b.q.clone(), new_key=b.new_key.clone(), new_value=b.new_value.clone(),
+                         block_tables=b.block_tables.clone(), context_lens=b.context_lens.clone(),
+                         starts=b.starts.clone(), ends=b.ends.clone(), cu_new=b.cu_new.clone())
+            s1 = replace(s, block_table=s.block_table.clone(), seq_ptr=s.seq_ptr.clone(),
+                         token_ptr=s.token_ptr.clone())
+            self._sets = [(b, s, self.out), (b1, s1, torch.empty_like(self.out))]
+        return self._sets
+
+    def run_set(self, stream_ptr, k: int):
+        """Enqueue one step on input set k (see input_sets)."""
+        keep = (self.batch, self.snap, self.out)
+        self.batch, self.snap, self.out = self.input_sets()[k]
+        try:
+            self.run(stream_ptr)
+        finally:
+            self.batch, self.snap, self.out = keep
+
     def run(self, stream_ptr, events=None):
         """Enqueue one step; events (6 per step) bracket the kernels if given."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
@@ -348,8 +373,8 @@ class DecodeStep:
         return st | self.attention(stream_ptr)
 
     # per-step host inputs for the end-to-end measurement
-    def host_inputs(self):
-        b, s = self.batch, self.snap
+    def host_inputs(self, k: int = 0):
+        b, s, _ = self.input_sets()[k]
         dev_tensors = [b.q, b.new_key, b.new_value, b.block_tables, b.context_lens, b.starts, b.ends, b.cu_new,
                        s.block_table, s.seq_ptr, s.token_ptr]
         host = [t.cpu().pin_memory() for t in dev_tensors]
@@ -359,31 +384,65 @@ class DecodeStep:
 STEPS_PER_GRAPH = 10
 
 
-def capture_step_graph(step: DecodeStep, n_steps: int, with_io=None):
+def capture_step_graph(step: DecodeStep, n_steps: int):
     """CUDA graph of n_steps hot-path steps (kernels chained by programmatic
-    dependent launch).  with_io = (host/device input pairs, out_host, err_host)
-    adds every step's host->device input copies and the device->host read of
-    its result to the graph."""
+    dependent launch)."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         for _ in range(n_steps):
-            if with_io is not None:
-                pairs, out_host, err_host = with_io
-                for h, d in pairs:
-                    d.copy_(h, non_blocking=True)
             step.run(ptr)
-            if with_io is not None:
-                out_host.copy_(step.out, non_blocking=True)
-                err_host.copy_(step.err, non_blocking=True)
     return g
 
 
-def time_graphs(step: DecodeStep, steps: int, world: int, with_io=None):
+def capture_pipelined_io_graph(step: DecodeStep, n_steps: int, io):
+    """CUDA graph of n_steps steps as a decode loop with host inputs runs them:
+    step i reads input set i % 2, whose host->device copies run on a second
+    stream as soon as step i - 2 is done with that set (overlapping step
+    i - 1), and the device->host read of step i's output runs on that stream
+    after step i while step i + 1 computes.  io = (per-set host/device input
+    pairs, per-set pinned output, pinned error flag)."""
+    pairs, out_host, err_host = io
+    sets = step.input_sets()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device=step.device)
+    with torch.cuda.graph(g):
+        comp = torch.cuda.current_stream()
+        ptr = ctypes.c_void_p(comp.cuda_stream)
+        ready = [torch.cuda.Event() for _ in range(n_steps)]
+        done = [torch.cuda.Event() for _ in range(n_steps)]
+        drained = [torch.cuda.Event() for _ in range(n_steps)]
+        side.wait_stream(comp)
+        for i in range(n_steps):
+            k = i % 2
+            with torch.cuda.stream(side):
+                if i >= 2:
+                    side.wait_event(done[i - 2])  # set k's inputs are no longer read
+                for h, d in pairs[k]:
+                    d.copy_(h, non_blocking=True)
+                ready[i].record(side)
+            comp.wait_event(ready[i])
+            if i >= 2:
+                comp.wait_event(drained[i - 2])  # output k has been read back
+            step.run_set(ptr, k)
+            done[i].record(comp)
+            with torch.cuda.stream(side):
+                side.wait_event(done[i])
+                out_host[k].copy_(sets[k][2], non_blocking=True)
+                err_host.copy_(step.err, non_blocking=True)
+                drained[i].record(side)
+        comp.wait_stream(side)
+    return g
+
+
+def time_graphs(step: DecodeStep, steps: int, world: int, io=None):
     """Replays graphs of STEPS_PER_GRAPH steps (and single steps for the
-    remainder) so that exactly `steps` steps run between the two events."""
-    big = capture_step_graph(step, STEPS_PER_GRAPH, with_io) if steps >= STEPS_PER_GRAPH else None
-    one = capture_step_graph(step, 1, with_io)
+    remainder) so that exactly `steps` steps run between the two events; with
+    io, the graphs are the pipelined end-to-end loop."""
+    cap = (lambda n: capture_pipelined_io_graph(step, n, io)) if io is not None else \
+        (lambda n: capture_step_graph(step, n))
+    big = cap(STEPS_PER_GRAPH) if steps >= STEPS_PER_GRAPH else None
+    one = cap(1)
     for _ in range(3):
         one.replay()
     if big is not None:
@@ -531,11 +590,12 @@ def time_prefill(step: DecodeStep, calls: int, world: int):
 
 
 def e2e_io(step: DecodeStep):
-    pairs = step.host_inputs()
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    """Pinned host buffers of the end-to-end pass, per input set."""
+    pairs = [step.host_inputs(0), step.host_inputs(1)]
+    out_host = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
     err_host = torch.empty(1, dtype=torch.int32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
-    d2h = out_host.numel() * out_host.element_size() + 4
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs[0])
+    d2h = out_host[0].numel() * out_host[0].element_size() + 4
     return (pairs, out_host, err_host), h2d, d2h
 
 
@@ -767,8 +827,9 @@ def run_ours(args, world, rank, local):
                                f"{ATTN_PER_GRAPH} calls between two CUDA events (K/V read per call > L2; no flush); "
                                "per_call_latency is the attention figure of the second pass (one call between "
                                "two events after an L2 eviction, launch latency included)",
-                   "e2e": "the same graphs with every step's pinned host->device input copies and the "
-                          "device->host read of its attention output and error flag"},
+                   "e2e": "graphs of the same steps as a pipelined decode loop runs them: every step copies "
+                          "its inputs from pinned host memory (two device input sets; step i+1's copies on a "
+                          "second stream overlap step i) and reads its attention output and error flag back"},
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -38,39 +38,38 @@ __device__ __forceinline__ uint32_t encode2(float lo, float hi, float s) {
     return d;
 }
 
-constexpr int kQuantThreads = 128;
+constexpr int kQuantThreads = 256;
 
-// One CTA per (block, head): the block's bs x d values of this head, max |x|
-// (NaN ignored) -> s = max / 448, then every value -> its code.
+// One CTA per block, one warp per head at a time: the head's bs x d values
+// (bs rows of d at a stride of Hkv * d), max |x| (NaN ignored) -> s = max / 448,
+// then every value -> its code.  The second pass re-reads the same bytes
+// (L1/L2 resident).
 template <typename T>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales, int32_t bs,
                     int32_t Hkv, int32_t d) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float red[kQuantThreads / 32];
-    const int64_t blk = blockIdx.x / Hkv;
-    const int h = blockIdx.x - static_cast<int>(blk * Hkv);
-    const int n = bs * d;
-    auto at = [&](int i) -> int64_t {  // element i of (block, head): token i / d, dim i % d
-        return ((blk * bs + i / d) * Hkv + h) * static_cast<int64_t>(d) + i % d;
-    };
-    float m = 0.f;
-    for (int i = threadIdx.x; i < n; i += kQuantThreads) m = fmaxf(m, fabsf(widen(src[at(i)])));
+    const int64_t blk = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n2 = bs * d / 2;  // pairs of the (block, head) slice; d is even
+    for (int h = warp; h < Hkv; h += kQuantThreads / 32) {
+        auto at = [&](int i) -> int64_t {  // element i of (block, head): token i / d, dim i % d
+            return ((blk * bs + i / d) * Hkv + h) * static_cast<int64_t>(d) + i % d;
+        };
+        float m = 0.f;
+        for (int p = lane; p < n2; p += 32) {
+            const int64_t e = at(2 * p);
+            m = fmaxf(m, fmaxf(fabsf(widen(src[e])), fabsf(widen(src[e + 1]))));
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = red[0];
-#pragma unroll
-    for (int w = 1; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
-    const float s = __fdiv_rn(m, 448.f);
-    if (threadIdx.x == 0) scales[blk * Hkv + h] = s;
-    for (int i = 2 * threadIdx.x; i < n; i += 2 * kQuantThreads) {  // d is even: pairs share a token
-        const int64_t e = at(i);
-        const uint32_t c = encode2(widen(src[e]), widen(src[e + 1]), s);
-        codes[e] = static_cast<uint8_t>(c & 0xff);
-        codes[e + 1] = static_cast<uint8_t>(c >> 8);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float s = __fdiv_rn(m, 448.f);
+        if (lane == 0) scales[blk * Hkv + h] = s;
+        for (int p = lane; p < n2; p += 32) {
+            const int64_t e = at(2 * p);
+            *reinterpret_cast<uint16_t *>(codes + e) = static_cast<uint16_t>(encode2(widen(src[e]), widen(src[e + 1]), s));
+        }
     }
 }
 
@@ -130,13 +129,12 @@ extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, flo
     if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: unknown dtype %d", (int)dtype);
     if (num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2)
         return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: bad sizes (head_dim must be even)");
-    if (static_cast<int64_t>(num_blocks) * num_kv_heads > INT32_MAX)
-        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: too many (block, head) pairs");
+    if (num_blocks > INT32_MAX / 2) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: too many blocks");
     if (num_blocks == 0) return ok();
     if (!src || !codes || !scales) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: NULL pointer");
     if (!aligned(src, dtype_bytes(dtype)) || !aligned(codes, 2) || !aligned(scales, 4))
         return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: misaligned buffers");
-    const dim3 grid(static_cast<unsigned>(num_blocks * num_kv_heads));
+    const dim3 grid(static_cast<unsigned>(num_blocks));
     auto s = static_cast<cudaStream_t>(stream);
     auto c = static_cast<uint8_t *>(codes);
     cudaError_t e;
