@@ -653,6 +653,27 @@ def cpu_sample_run(batch, budget_s: float, start_seq: int = 0, max_seqs: int | N
     return nbytes / t_total / 1e9, t_total, done, nbytes
 
 
+def cpu_all_cores_run(batch, max_seqs: int):
+    """The same oracle step on the first max_seqs sequences, one sequence per
+    task on a pool of host threads (the C oracle runs outside the GIL); inputs
+    are prepared before the clock starts.  Returns (GB/s, seconds, sequences,
+    bytes, threads)."""
+    import oracle as orc
+    from concurrent.futures import ThreadPoolExecutor
+
+    orc.build()
+    cfg = batch.cfg
+    n = min(max_seqs, cfg.batch)
+    samples = [oracle_sample_inputs(batch, [i]) for i in range(n)]
+    threads = max(1, min(len(os.sched_getaffinity(0)), n))
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t0 = time.perf_counter()
+        list(pool.map(lambda smp: oracle_step(orc, smp, cfg, batch.scale), samples))
+        secs = time.perf_counter() - t0
+    nbytes = sum(sum(step_bytes(cfg, smp["ctx"], smp["nnz"]).values()) for smp in samples)
+    return nbytes / secs / 1e9, secs, n, nbytes, threads
+
+
 # ----------------------------------------------------------------------------- arms
 def run_reference(args, world, rank):
     """The oracle as it stands, on the host cores, one bounded sample per step."""
@@ -757,6 +778,11 @@ def run_ours(args, world, rank, local):
                         "sample": f"first {nseq} of {cfg.batch} sequences of the batch, whole step per sequence "
                                   f"({nbytes / 1e9:.3f} GB of step bytes in {secs:.1f} s), single-threaded C "
                                   f"oracle in binary64"}
+        mgbs, msecs, mseq, mbytes, threads = cpu_all_cores_run(step.batch, max(nseq, 1))
+        cpu_baseline["all_cores"] = {
+            "value": round(mgbs, 4), "unit": "GB/s", "cores": threads,
+            "sample": f"the same {mseq} sequences ({mbytes / 1e9:.3f} GB of step bytes in {msecs:.2f} s), one "
+                      f"sequence per task on {threads} host threads"}
 
     if rank != 0:
         return 0
