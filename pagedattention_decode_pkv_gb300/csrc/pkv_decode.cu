@@ -671,6 +671,15 @@ struct StreamSmem {
     static constexpr int kAlloc = kBytes + 1024;
 };
 
+// a / b for a >= 0, b > 0.  A 64-bit division by a runtime value is a long
+// dependent instruction sequence (~0.4 us for one warp on GB300), and the
+// schedule below sits on the path to the first bulk copy; operands that fit
+// 32 bits (always, short of ~2^31 stages) take the short unsigned form.
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+    if (((a | b) >> 32) == 0) return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+    return a / b;
+}
+
 // Tail stages of a unit with n stages: whole chunks, about n / kTailDenominator.
 __device__ __forceinline__ int64_t tail_stages(int64_t n) {
     return n / kTailDenominator / kChunkStages * kChunkStages;
@@ -688,7 +697,7 @@ __device__ __forceinline__ void locate_stage(Pre pre, int B, int HG, int64_t s, 
     b = lo;
     const int64_t n = pre(b + 1) - pre(b);
     const int64_t off = s - static_cast<int64_t>(HG) * pre(b);
-    hg = static_cast<int>(off / n);
+    hg = static_cast<int>(div_nonneg(off, n));
     st = static_cast<int>(off - hg * n);
 }
 
@@ -722,12 +731,14 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     auto pre_static = [&](int b) { return spref[b]; };
     auto pre_tail = [&](int b) { return pref[b] - spref[b]; };
 
-    if (threadIdx.x == 0) {
+    if (warp == HPC && lane == 0) {  // the producer's lane 0 initialises the barriers it issues on first
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(bar0 + 8 * i, 1);
             mbar_init(bar0 + 8 * (STAGES + i), HPC);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tm_k);  // the maps are parameters: nothing the previous grid writes
+        prefetch_tensormap(&tm_v);
     }
     pdl_wait();
     pdl_trigger();
@@ -744,24 +755,82 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // load before the first bulk copy.  The id is read from the same table
     // entry either way.
     int g_b = -1, g_hg = 0, g_st = 0, g_id = -1;
+    const int64_t g_n = (static_cast<int64_t>(max_ctx) + kStageTokens - 1) / kStageTokens;  // stages at max_ctx
     if (warp == HPC && max_ctx > 0) {
-        const int64_t n = (static_cast<int64_t>(max_ctx) + kStageTokens - 1) / kStageTokens;
+        const int64_t n = g_n;
         const int64_t ns = n - tail_stages(n);
         const int64_t wst = static_cast<int64_t>(HG) * B * ns;
         int64_t cw = wst / kMinStreamStages;
         if (cw > C) cw = C;
         if (cw < 1) cw = 1;
         if (c < cw) {
-            const int64_t sf = wst * c / cw + lane, se = wst * (c + 1) / cw;
+            const int64_t sf = div_nonneg(wst * c, cw) + lane, se = div_nonneg(wst * (c + 1), cw);
             if (sf < se) {
-                const int64_t unit = sf / ns;
+                const int64_t unit = div_nonneg(sf, ns);
                 const int st = static_cast<int>(sf - unit * ns);
                 const int blk = st * kStageTokens / bs;
                 if (blk < max_blocks) {
-                    g_b = static_cast<int>(unit / HG);
+                    g_b = static_cast<int>(div_nonneg(unit, HG));
                     g_hg = static_cast<int>(unit - static_cast<int64_t>(g_b) * HG);
                     g_st = st;
                     g_id = block_tables[static_cast<int64_t>(g_b) * max_blocks + blk];
+                }
+            }
+        }
+    }
+    // Early issue.  When every sequence holds max_ctx tokens the guess is the
+    // real schedule, so the producer starts the bulk copies of its first stages
+    // (at most STAGES, so no slot is reused) as soon as their block ids and the
+    // context lengths are in, instead of after the plan and describe() below.
+    // They go out under mbarrier.expect_tx alone: the stage's arrival, with its
+    // info, comes when the issue loop reaches the same stage, and a slot whose
+    // stage turns out different is handed to the consumers as one to skip.
+    // The producer also takes the abort decision, so that a CTA with copies in
+    // flight never leaves at the early return below.
+    int n_early = 0;
+    int e_id = -1, e_hg = 0, e_row = 0;  // lane e < n_early: stage e's block id, head group, row in block
+    const uint64_t kv_policy = l2_evict_first_policy();
+    if (warp == HPC) {
+        int abort_now = 0;
+        if (lane == 0 && err_flag)  // a broken pipeline elsewhere in the launch stops this CTA early
+            abort_now = (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT) ? 1 : 0;
+        abort_now = __shfl_sync(0xffffffffu, abort_now, 0);
+        if (lane == 0) *abort_flag = abort_now;
+        // (checked for up to 128 sequences: four independent loads per lane)
+        bool equal = !abort_now && max_ctx > 0 && B <= 128 &&
+                     g_n * kStageTokens <= static_cast<int64_t>(max_blocks) * bs;
+        if (equal) {
+            int lens[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) lens[k] = lane + 32 * k < B ? context_lens[lane + 32 * k] : max_ctx;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) equal = equal && lens[k] == max_ctx;
+        }
+        equal = __all_sync(0xffffffffu, equal);
+        if (equal) {
+            const bool ok = lane < STAGES && g_b >= 0 && g_id >= 0 && g_id < num_blocks &&
+                            !(new_k && g_st == g_n - 1);  // an append stage must write its row first
+            n_early = __ffs(~__ballot_sync(0xffffffffu, ok)) - 1;  // the leading run of ok lanes
+            if (lane < n_early) {
+                const int pos0 = g_st * kStageTokens;
+                e_id = g_id;
+                e_hg = g_hg;
+                e_row = pos0 - pos0 / bs * bs;
+            }
+            for (int e = 0; e < n_early; ++e) {
+                const int id = __shfl_sync(0xffffffffu, e_id, e), hg = __shfl_sync(0xffffffffu, e_hg, e);
+                const int row = __shfl_sync(0xffffffffu, e_row, e);
+                if (lane == 0) {
+                    const uint32_t full = bar0 + 8 * e, dst = tiles + e * L::kStageBytes;
+                    const int z = FP8 ? hg * HPC : 2 * hg * HPC;
+                    mbar_expect_tx(full, L::kStageBytes);
+                    if (kKvEvictFirst) {
+                        tma_load_3d_hint(dst, &tm_k, 0, id * bs + row, z, full, kv_policy);
+                        tma_load_3d_hint(dst + L::kTileBytes, &tm_v, 0, id * bs + row, z, full, kv_policy);
+                    } else {
+                        tma_load_3d(dst, &tm_k, 0, id * bs + row, z, full);
+                        tma_load_3d(dst + L::kTileBytes, &tm_v, 0, id * bs + row, z, full);
+                    }
                 }
             }
         }
@@ -770,8 +839,6 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int ctx = context_lens[b];
         cx[b] = context_ok(ctx, max_ctx, bs, max_blocks) ? ctx : 0;
     }
-    if (threadIdx.x == 0)  // a broken pipeline elsewhere in the launch stops this CTA early
-        *abort_flag = (err_flag && (*reinterpret_cast<volatile int32_t *>(err_flag) & PKV_ERRBIT_TIMEOUT)) ? 1 : 0;
     __syncthreads();
     if (warp == 0) {  // exclusive prefixes of stages and of static-part stages per sequence
         const int chunk = (B + 31) / 32;
@@ -817,7 +884,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     int64_t Cw = Wst / kMinStreamStages;
     if (Cw > C) Cw = C;
     if (Cw < 1) Cw = Wst > 0 ? 1 : 0;
-    const int64_t s0 = c < Cw ? Wst * c / Cw : 0, s1 = c < Cw ? Wst * (c + 1) / Cw : 0;
+    const int64_t s0 = c < Cw ? div_nonneg(Wst * c, Cw) : 0, s1 = c < Cw ? div_nonneg(Wst * (c + 1), Cw) : 0;
     if (c == 0 && threadIdx.x == 0) ws_meta[0] = static_cast<int32_t>(Cw);
 
     // Sequences with nothing to stream (empty or invalid context) get zero rows
@@ -852,8 +919,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const int64_t ns = spref[b + 1] - spref[b], nt = n - ns;
             const int st = dyn ? static_cast<int>(ns) + sp : sp;  // stage inside the unit
             const int pos0 = st * kStageTokens;
+            const int blk = pos0 / bs, in_blk = pos0 - blk * bs;
             if (b == g_b && hg == g_hg && st == g_st) id = g_id;  // the guess was right: same table entry
-            else id = block_tables[static_cast<int64_t>(b) * max_blocks + pos0 / bs];  // checked when issued
+            else id = block_tables[static_cast<int64_t>(b) * max_blocks + blk];  // checked when issued
             const int64_t u = static_cast<int64_t>(b) * HG + hg;
             int flags = 0;
             if (sf == lo || (!dyn && sp == 0)) flags |= kFlagFirst;
@@ -873,7 +941,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 slot_of_piece = static_cast<int>(dyn_base + (seg - C) + u);
             }
             if (new_k && st == n - 1) flags |= kFlagAppend;  // position ctx - 1 is in this stage
-            meta = min(kStageTokens, ctx - pos0) | flags | (pos0 % bs) << 16;
+            meta = min(kStageTokens, ctx - pos0) | flags | in_blk << 16;
             if constexpr (FP8) {  // this stage's (block, head) scales, 0 for a block that will be skipped
                 float *dst = bscl + (buf * 32 + lane) * 2 * HPC;
                 const bool ok_id = id >= 0 && id < num_blocks;
@@ -885,7 +953,6 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 }
             }
         };
-        const uint64_t kv_policy = l2_evict_first_policy();
         // batch bookkeeping (warp-uniform)
         int64_t c_sb = 0, c_se = 0, c_lo = 0, c_hi = 0;
         int c_seg = -1;
@@ -922,31 +989,44 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         bool aborted = false;
         int64_t issued = 0;
         while (have && !aborted) {
-            // Static batches are described one batch ahead (their block-id loads
-            // stay in flight meanwhile); a dynamic chunk is claimed only when
+            // A static batch is described while the one before it is issued, as
+            // soon as that one's first STAGES stages are out (the most that can be
+            // in flight before the producer waits for a free slot), so its
+            // block-id loads stay in flight meanwhile and the launch's first bulk
+            // copies do not wait for them.  A dynamic chunk is claimed only when
             // kGrabAhead stages of the current batch remain, so that chunks go to
             // the CTAs that actually run out of work.
             int nb = 0, nhg = 0, nmeta = 0, nid = -1, nslot = 0;
             bool have_next = false, decided = false;
-            if (static_next < s1) {
-                have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
-                describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot, cbuf ^ 1);
-                decided = true;
-            }
             const int cnt = static_cast<int>(c_se - c_sb);
+            const int ahead_at = static_next < s1 ? min(cnt - 1, STAGES) : cnt - kGrabAhead;
             for (int j = 0; j < cnt; ++j) {
-                if (!decided && cnt - j <= kGrabAhead) {
+                if (!decided && j >= ahead_at) {
                     have_next = next_batch(n_sb, n_se, n_lo, n_hi, n_seg);
                     if (have_next) describe(n_sb, n_se, n_lo, n_hi, n_seg, nb, nhg, nmeta, nid, nslot, cbuf ^ 1);
                     decided = true;
                 }
-                const int64_t i = issued;
-                const int slot = static_cast<int>(i % STAGES);
-                const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
                 const int b = __shfl_sync(0xffffffffu, cb, j), hg = __shfl_sync(0xffffffffu, chg, j);
                 int meta = __shfl_sync(0xffffffffu, cmeta, j);
                 int id = __shfl_sync(0xffffffffu, cid, j);
                 const int pslot = __shfl_sync(0xffffffffu, cslot, j);
+                // Early copies: the next one is this stage's (same block, row and
+                // head group, no append) or its slot is skipped.
+                while (issued < n_early) {
+                    const int e = static_cast<int>(issued);
+                    const int eid = __shfl_sync(0xffffffffu, e_id, e), ehg = __shfl_sync(0xffffffffu, e_hg, e);
+                    const int erow = __shfl_sync(0xffffffffu, e_row, e);
+                    if (eid == id && ehg == hg && erow == (meta >> 16) && !(meta & kFlagAppend)) break;
+                    if (lane == 0) {
+                        info[e] = make_int4(-2, 0, 0, 0);
+                        mbar_arrive(bar0 + 8 * e);
+                    }
+                    issued = e + 1;
+                }
+                const int64_t i = issued;
+                const bool early = i < n_early;  // this stage's bulk copy is in flight already
+                const int slot = static_cast<int>(i % STAGES);
+                const uint32_t full = bar0 + 8 * slot, empty = bar0 + 8 * (STAGES + slot);
                 if ((meta & kFlagAppend) && id >= 0 && id < num_blocks) {
                     // Append: the step's new K/V rows of these HPC heads go to the
                     // cache row of position ctx - 1 before the bulk copy reads it
@@ -992,7 +1072,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
                         for (int e = 0; e < 2 * HPC; ++e) scl[slot * 2 * HPC + e] = srcs[e];
                     }
-                    if (id >= 0) {
+                    if (early) {
+                        mbar_arrive(full);  // its bytes were expected when the copy left
+                    } else if (id >= 0) {
                         const int slot_row = id * bs + (meta >> 16);
                         const uint32_t dst = tiles + slot * L::kStageBytes;
                         const int z = FP8 ? hg * HPC : 2 * hg * HPC;  // first head (FP8) or half-row of the box
@@ -1015,6 +1097,13 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             c_sb = n_sb; c_se = n_se; c_lo = n_lo; c_hi = n_hi; c_seg = n_seg;
             cb = nb; chg = nhg; cmeta = nmeta; cid = nid; cslot = nslot;
             cbuf ^= 1;
+        }
+        while (!aborted && issued < n_early) {  // early copies no stage claimed (none, when the guess holds)
+            if (lane == 0) {
+                info[issued] = make_int4(-2, 0, 0, 0);
+                mbar_arrive(bar0 + 8 * static_cast<int>(issued));
+            }
+            ++issued;
         }
         if (lane == 0) {
             if (!aborted) {
@@ -1119,7 +1208,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
         const int4 inf = info[slot];
         const int b = inf.x, hg = inf.y, meta = inf.z, pslot = inf.w;
-        if (b < 0) break;  // no more work
+        if (b == -1) break;  // no more work
+        if (b < 0) {         // an early copy no stage claimed: release the slot
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (STAGES + slot));
+            continue;
+        }
         const int nvalid = meta & 0xff;
         const int hk = hg * HPC + warp;
         if (meta & kFlagFirst) {
@@ -1306,58 +1400,77 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
 }
 
-// Merges the pieces of every split unit.  One CTA of 8 warps per (unit, query
-// head of the unit).  unit_info[u] = (first static slice, last static slice,
-// first chunk, chunk count) gives the unit's pieces: slot (c + u) for its
-// static slices and (dyn_base + k + u) for its chunks.  The kernel makes two
-// dependent rounds of loads: the unit's context length and unit_info, then
-// every piece's (max, sum) pair and output row at once.  Warp w folds pieces
-// w, w + 8, ... into a running (max, sum, row) of its own as they arrive (lanes
-// over the 128 dims as float4); the eight warps meet in shared memory.  The CTA
-// is small (4 KB of shared memory, 74 registers) so that it fits beside two
-// main-pass CTAs on an SM and is already resident when the main pass ends.
+// Merges the pieces of every split unit.  A row is one (unit, query head of
+// the unit) pair; WPR warps of a CTA of 8 share a row, so a CTA covers 8 / WPR
+// rows (the host picks WPR so that the grid stays near one wave: 8 warps per
+// row for launches with few units and many pieces each, fewer when units are
+// many).  unit_info[u] = (first static slice, last static slice, first chunk,
+// chunk count) gives the unit's pieces: slot (c + u) for its static slices and
+// (dyn_base + k + u) for its chunks.  The kernel makes two dependent rounds of
+// loads: the unit's context length and unit_info, then every piece's (max,
+// sum) pair and output row, kMergeInFlight per warp at once.  Each warp folds
+// its pieces into a running (max, sum, row) (lanes over the 128 dims as
+// float4); the row's warps meet in shared memory.  The CTA is small (4 KB of
+// shared memory) so that it fits beside two main-pass CTAs on an SM and is
+// already resident when the main pass ends.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeInFlight = 8;  // pieces per warp per round
+constexpr int kMergeWaveCtas = 608;   // grid target: 4 merge CTAs per SM (beat 8 per SM on GB300)
 
-template <typename T>
+template <typename T, int WPR>
 __global__ void __launch_bounds__(kMergeThreads)
 stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, const float2 *__restrict__ ml_piece,
                       const int4 *__restrict__ unit_info, const int32_t *__restrict__ context_lens, int32_t Hq,
                       int32_t HG, int32_t HU, int32_t bs, int32_t max_blocks, int32_t max_ctx, int32_t num_ctas,
-                      int64_t dyn_base, int64_t max_slots) {
+                      int64_t dyn_base, int64_t max_slots, int64_t rows) {
+    constexpr int RPC = kMergeWarps / WPR;  // rows per CTA
     __shared__ float4 red[kMergeWarps][32];
     __shared__ float2 wml[kMergeWarps];
     pdl_wait();
     pdl_trigger();
-    const int u = blockIdx.x, j = blockIdx.y;
-    const int b = u / HG, hg = u - b * HG;
-    const int ctx = context_lens[b];
-    const int4 ui = unit_info[u];
-    if (!context_ok(ctx, max_ctx, bs, max_blocks) || ctx == 0) return;
-    const int f = ui.x, l = ui.y, k0 = ui.z, nk = ui.w;
-    if (f == l && nk == 0) return;  // one piece: the main kernel wrote the output
-    // only after an aborted main pass (PKV_ERRBIT_TIMEOUT is set) can these fail
-    if (f < 0 || l < f || l >= num_ctas || k0 < 0 || nk < 0 || dyn_base + k0 + nk + u > max_slots) return;
-    const int n_static = l - f + 1;
-    const int np = n_static + nk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % WPR;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * RPC + warp / WPR;
+    int u = 0, j = 0, b = 0, hg = 0, f = 0, np = 0, n_static = 0, k0 = 0;
+    if (row < rows) {
+        const int r = static_cast<int>(row);  // rows = units * HU stays far below 2^31
+        u = r / HU;
+        j = r - u * HU;
+        b = u / HG;
+        hg = u - b * HG;
+        const int ctx = context_lens[b];
+        const int4 ui = unit_info[u];
+        const int l = ui.y, nk = ui.w;
+        f = ui.x;
+        k0 = ui.z;
+        // nothing to do: an empty or invalid context (zero row written by the
+        // main pass), one piece (the main pass wrote the output), or unit_info
+        // left inconsistent by an aborted main pass (PKV_ERRBIT_TIMEOUT is set)
+        const bool work = context_ok(ctx, max_ctx, bs, max_blocks) && ctx != 0 && !(f == l && nk == 0) &&
+                          f >= 0 && l >= f && l < num_ctas && k0 >= 0 && nk >= 0 &&
+                          dyn_base + k0 + nk + u <= max_slots;
+        if (work) {
+            n_static = l - f + 1;
+            np = n_static + nk;
+        }
+    }
     auto row_of = [&](int k) -> int64_t {
         const int64_t slot = k < n_static ? static_cast<int64_t>(f + k) + u : dyn_base + k0 + (k - n_static) + u;
         return slot * HU + j;
     };
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float m_w = -INFINITY, l_w = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int kb = warp; kb < np; kb += kMergeWarps * kMergeInFlight) {
+    for (int kb = sub; kb < np; kb += WPR * kMergeInFlight) {
         float4 v[kMergeInFlight];
         float2 ml[kMergeInFlight];
 #pragma unroll
         for (int uu = 0; uu < kMergeInFlight; ++uu) {
-            const int k = kb + kMergeWarps * uu;
+            const int k = kb + WPR * uu;
             if (k < np) {
-                const int64_t row = row_of(k);
-                v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + row * kFastHeadDim) + lane);
-                ml[uu] = __ldg(ml_piece + row);
+                const int64_t r = row_of(k);
+                v[uu] = __ldg(reinterpret_cast<const float4 *>(o_piece + r * kFastHeadDim) + lane);
+                ml[uu] = __ldg(ml_piece + r);
             } else {
                 v[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
                 ml[uu] = make_float2(-INFINITY, 0.f);
@@ -1384,33 +1497,37 @@ stream_combine_kernel(T *__restrict__ out, const float *__restrict__ o_piece, co
         }
         m_w = mn;
     }
-    red[warp][lane] = acc;
-    if (lane == 0) wml[warp] = make_float2(m_w, l_w);
-    __syncthreads();
-    if (warp == 0) {
+    if constexpr (WPR > 1) {
+        red[warp][lane] = acc;
+        if (lane == 0) wml[warp] = make_float2(m_w, l_w);
+        __syncthreads();
+        if (sub != 0 || np == 0) return;
         float M = -INFINITY;
 #pragma unroll
-        for (int ww = 0; ww < kMergeWarps; ++ww) M = fmaxf(M, wml[ww].x);
-        float4 tt = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = 0.f;
+        for (int ww = 0; ww < WPR; ++ww) M = fmaxf(M, wml[warp + ww].x);
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        l_w = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int ww = 0; ww < kMergeWarps; ++ww) {
-                const float w = exp2f(wml[ww].x - M);
-                tt.x = fmaf(w, red[ww][lane].x, tt.x);
-                tt.y = fmaf(w, red[ww][lane].y, tt.y);
-                tt.z = fmaf(w, red[ww][lane].z, tt.z);
-                tt.w = fmaf(w, red[ww][lane].w, tt.w);
-                L = fmaf(w, wml[ww].y, L);
+            for (int ww = 0; ww < WPR; ++ww) {
+                const float w = exp2f(wml[warp + ww].x - M);
+                const float4 x = red[warp + ww][lane];
+                acc.x = fmaf(w, x.x, acc.x);
+                acc.y = fmaf(w, x.y, acc.y);
+                acc.z = fmaf(w, x.z, acc.z);
+                acc.w = fmaf(w, x.w, acc.w);
+                l_w = fmaf(w, wml[warp + ww].y, l_w);
             }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        T *dst = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * HU + j) * kFastHeadDim + 4 * lane;
-        dst[0] = from_f32<T>(tt.x * inv);
-        dst[1] = from_f32<T>(tt.y * inv);
-        dst[2] = from_f32<T>(tt.z * inv);
-        dst[3] = from_f32<T>(tt.w * inv);
+    } else if (np == 0) {
+        return;
     }
+    const float inv = l_w > 0.f ? 1.f / l_w : 0.f;
+    T *dst = out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hg) * HU + j) * kFastHeadDim + 4 * lane;
+    dst[0] = from_f32<T>(acc.x * inv);
+    dst[1] = from_f32<T>(acc.y * inv);
+    dst[2] = from_f32<T>(acc.z * inv);
+    dst[3] = from_f32<T>(acc.w * inv);
 }
 
 // ----------------------------------------------------------------------------- append (other paths)
@@ -1578,6 +1695,30 @@ template <typename T, int HPC, int STAGES, bool FP8> std::atomic<int> StreamLaun
 template <typename T, int HPC, int STAGES, bool FP8>
 std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES, FP8>::configured{0};
 
+// Warps per merge row: as many as keep the merge grid within about one wave.
+inline int merge_warps_per_row(int64_t rows) {
+    int wpr = kMergeWarps;
+    while (wpr > 1 && rows * wpr > static_cast<int64_t>(kMergeWaveCtas) * kMergeWarps) wpr >>= 1;
+    return wpr;
+}
+
+template <typename T>
+cudaError_t launch_stream_combine(const DecodeArgs &a, const Plan &p, int C, int HG, int HU) {
+    const int64_t rows = p.units * HU;
+    const int wpr = merge_warps_per_row(rows);
+    const int64_t rpc = kMergeWarps / wpr;
+    const dim3 grid(static_cast<unsigned>((rows + rpc - 1) / rpc));
+    auto kern = wpr == 8 ? stream_combine_kernel<T, 8>
+              : wpr == 4 ? stream_combine_kernel<T, 4>
+              : wpr == 2 ? stream_combine_kernel<T, 2>
+                         : stream_combine_kernel<T, 1>;
+    return launch_pdl(kPdlCombine, kern, grid, dim3(kMergeThreads), 0, a.stream, static_cast<T *>(a.out),
+                      static_cast<const float *>(a.o_part), static_cast<const float2 *>(a.ml_part),
+                      static_cast<const int4 *>(a.unit_info), a.context_lens, a.Hq, HG, HU, a.bs, a.max_blocks,
+                      a.max_ctx, C, static_cast<int64_t>(kMaxStreamCtas + p.units),
+                      static_cast<int64_t>(p.max_segments), rows);
+}
+
 template <typename T, int HPC, int STAGES, bool FP8>
 pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
     using L = StreamSmem<HPC, STAGES, FP8>;
@@ -1600,12 +1741,7 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
                                static_cast<T *>(const_cast<void *>(a.k_cache)),
                                static_cast<T *>(const_cast<void *>(a.v_cache)), a.k_scale, a.v_scale, a.err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    e = launch_pdl(kPdlCombine, stream_combine_kernel<T>, dim3(static_cast<unsigned>(p.units), HPC * G),
-                   dim3(kMergeThreads), 0, a.stream,
-                   static_cast<T *>(a.out), static_cast<const float *>(a.o_part),
-                   static_cast<const float2 *>(a.ml_part), static_cast<const int4 *>(a.unit_info), a.context_lens,
-                   a.Hq, HG, HPC * G, a.bs, a.max_blocks, a.max_ctx, C,
-                   static_cast<int64_t>(kMaxStreamCtas + p.units), static_cast<int64_t>(p.max_segments));
+    e = launch_stream_combine<T>(a, p, C, HG, HPC * G);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }

@@ -56,6 +56,24 @@ def test_append_fused_matches_oracle_step(pkv, orc, cuda_dev, dtype, Hq, Hkv, bs
     assert torch.count_nonzero(out[0]) == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,bs,ctx,B", [(32, 8, 16, 3000, 3), (16, 8, 16, 300, 5), (4, 1, 16, 1, 7),
+                                            (8, 2, 16, 17, 40), (16, 8, 256, 700, 6)])
+def test_append_fused_equal_lengths(pkv, orc, cuda_dev, Hq, Hkv, bs, ctx, B):
+    """Every sequence at max_ctx (the early-issue case): the stage holding
+    position ctx - 1 still appends before its copy, and the step matches the
+    oracle."""
+    cfg = wl.DecodeConfig("t", torch.bfloat16, Hq, Hkv, 128, bs, B, 1, ctx, None)
+    batch = wl.decode_batch(cfg, seed=ctx + 2 * B, device=cuda_dev, ctx_override=[ctx] * B, nan_tails=True,
+                            nan_unused=True)
+    kc0, vc0 = batch.k_cache.cpu(), batch.v_cache.cpu()
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    out = _append(pkv, batch, ctx, err)
+    ref, kr, vr, nerr = _oracle_step(orc, batch, kc0, vc0)
+    assert nerr == 0 and int(err.item()) == 0
+    assert torch.equal(_bits(batch.k_cache), _bits(kr)) and torch.equal(_bits(batch.v_cache), _bits(vr))
+    assert _max_err(out, ref) <= ATOL_16
+
+
 def test_append_equals_the_three_calls(pkv, cuda_dev):
     """Fused step == slot mapping + store + attention through the library, bit for bit."""
     cfg = wl.LONG_GQA_8K

@@ -82,6 +82,20 @@ def test_decode_fp8_matches_oracle(pkv, orc, cuda_dev, dtype, Hq, Hkv, bs):
     assert torch.count_nonzero(out[0]) == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,bs,ctx,B", [(32, 8, 16, 3000, 3), (8, 8, 256, 40, 3), (4, 1, 16, 1, 7),
+                                            (16, 8, 16, 700, 100)])
+def test_decode_fp8_equal_lengths(pkv, orc, cuda_dev, Hq, Hkv, bs, ctx, B):
+    """Every sequence at max_ctx (the early-issue case) over E4M3 caches."""
+    batch, kq, ks, vq, vs = _fp8_case(pkv, orc, cuda_dev, torch.bfloat16, Hq, Hkv, bs, [ctx] * B, seed=ctx + B)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    out = pkv.pkv_paged_attention_decode_fp8(batch.q, kq, vq, ks, vs, batch.block_tables, batch.context_lens,
+                                             batch.scale, ctx, err_flag=err)
+    ref, nerr = orc.paged_attention_decode_fp8(batch.q, kq, vq, ks, vs, batch.block_tables, batch.context_lens,
+                                               batch.scale)
+    assert nerr == 0 and int(err.item()) == 0
+    assert _max_err(out, ref) <= ATOL_16
+
+
 def test_decode_fp8_peaky_and_split_invariance(pkv, orc, cuda_dev):
     """A peaky softmax (q x 8) over long sequences: alone (spread over every
     CTA) and in a batch, against the oracle."""

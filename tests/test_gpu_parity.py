@@ -192,6 +192,52 @@ def test_decode_peaky_softmax_and_split_invariance(pkv, orc, cuda_dev):
         assert (one[0].float() - full[b].float()).abs().max().item() <= 1e-2
 
 
+EQUAL_CASES = [(32, 8, 16, 3000, 3), (16, 8, 16, 300, 5), (8, 8, 256, 40, 3), (4, 1, 16, 1, 7),
+               (64, 8, 32, 1000, 2), (8, 2, 16, 17, 40), (16, 8, 16, 700, 100)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("Hq,Hkv,bs,ctx,B", EQUAL_CASES)
+def test_decode_equal_lengths(pkv, orc, cuda_dev, dtype, Hq, Hkv, bs, ctx, B):
+    """Every sequence at max_ctx: the schedule the producer guesses from
+    max_ctx is the real one, and its first stages' copies leave before the
+    plan is computed.  Short units (no tail), one-token contexts, units split
+    over many CTAs and batches of up to 128 sequences all match the oracle."""
+    cfg = wl.DecodeConfig("t", dtype, Hq, Hkv, 128, bs, B, 1, ctx, None)
+    batch = wl.decode_batch(cfg, seed=ctx + B, device=cuda_dev, ctx_override=[ctx] * B, nan_tails=True,
+                            nan_unused=True)
+    err = _zero_err(cuda_dev)
+    out = pkv.pkv_paged_attention_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                                         batch.context_lens, batch.scale, ctx, err_flag=err)
+    ref, _ = orc.paged_attention_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                                        batch.context_lens, batch.scale)
+    assert int(err.item()) == 0
+    assert not torch.isnan(out).any()
+    assert _max_err(out, ref) <= ATOL_16
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(64, 16, 8), (40, 32, 8), (200, 32, 8), (512, 64, 8)])
+def test_decode_merge_row_layouts(pkv, orc, cuda_dev, B, Hq, Hkv):
+    """The piece merge shares a row among 8, 4, 2 or 1 warps depending on how
+    many (unit, query head) rows a launch has (1024, 1280, 6400 and 32768
+    rows here); every layout matches the oracle on split units."""
+    g = torch.Generator().manual_seed(B + Hq)
+    hi = 3000 if B < 100 else 600  # keeps the oracle's work to a few seconds
+    lens = torch.randint(1, hi, (B,), generator=g)
+    lens[:3] = torch.tensor([0, hi - 1, 1])
+    cfg = wl.DecodeConfig("t", torch.bfloat16, Hq, Hkv, 128, 16, B, 1, hi, None)
+    batch = wl.decode_batch(cfg, seed=B, device=cuda_dev, ctx_override=lens.tolist(), nan_tails=True)
+    err = _zero_err(cuda_dev)
+    out = pkv.pkv_paged_attention_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                                         batch.context_lens, batch.scale, hi, err_flag=err)
+    ref, _ = orc.paged_attention_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                                        batch.context_lens, batch.scale)
+    assert int(err.item()) == 0
+    assert not torch.isnan(out).any()
+    assert _max_err(out, ref) <= ATOL_16
+    assert torch.count_nonzero(out[0]) == 0
+
+
 def test_decode_fixed_partition_kernel_for_large_batches(pkv, orc, cuda_dev):
     """More than 1024 sequences use the tensor-core kernel with fixed partitions
     of the context (and the split-K combine for the long ones)."""
