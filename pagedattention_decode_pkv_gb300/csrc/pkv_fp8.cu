@@ -73,6 +73,65 @@ quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, floa
     }
 }
 
+// Vector form: one warp per (block, head) slice, 16-byte loads of VEC elements;
+// the slice (at most 32 * kQuantVecs vectors) stays in registers between the
+// max and the encode, so the cache is read once.  Needs d % VEC == 0 and
+// 16-byte aligned source rows (8-byte aligned code rows follow).
+constexpr int kQuantVecs = 8;  // vectors per lane: 16 tokens x 128 dims of a 16-bit cache
+
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_fp8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales,
+                        int64_t slices, int32_t bs, int32_t Hkv, int32_t d) {
+    constexpr int VEC = 16 / sizeof(T);
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int vpr = d / VEC;             // vectors per token row of one head
+    const int nv = bs * vpr;             // vectors per slice (<= 32 * kQuantVecs)
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kQuantThreads / 32);
+    for (int64_t sl = static_cast<int64_t>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5); sl < slices;
+         sl += warps) {
+        const int64_t blk = sl / Hkv;
+        const int h = static_cast<int>(sl - blk * Hkv);
+        uint4 v[kQuantVecs];
+        int64_t off[kQuantVecs];  // element offset of each vector
+#pragma unroll
+        for (int k = 0; k < kQuantVecs; ++k) {
+            const int i = lane + 32 * k;
+            const int t = i / vpr;
+            off[k] = ((blk * bs + t) * Hkv + h) * static_cast<int64_t>(d) + (i - t * vpr) * VEC;
+            v[k] = i < nv ? __ldg(reinterpret_cast<const uint4 *>(src + off[k])) : make_uint4(0, 0, 0, 0);
+        }
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < kQuantVecs; ++k) {
+            const T *x = reinterpret_cast<const T *>(&v[k]);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m = fmaxf(m, fabsf(widen(x[e])));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float s = __fdiv_rn(m, 448.f);
+        if (lane == 0) scales[sl] = s;
+#pragma unroll
+        for (int k = 0; k < kQuantVecs; ++k) {
+            if (lane + 32 * k >= nv) continue;
+            const T *x = reinterpret_cast<const T *>(&v[k]);
+            uint32_t w[VEC / 4];
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q)
+                w[q] = encode2(widen(x[4 * q]), widen(x[4 * q + 1]), s) |
+                       encode2(widen(x[4 * q + 2]), widen(x[4 * q + 3]), s) << 16;
+            if constexpr (VEC == 8) {
+                *reinterpret_cast<uint2 *>(codes + off[k]) = make_uint2(w[0], w[1]);
+            } else {
+                *reinterpret_cast<uint32_t *>(codes + off[k]) = w[0];
+            }
+        }
+    }
+}
+
 constexpr int kStoreThreads = 256;
 
 // One thread per (token, head, pair of dims).
@@ -134,10 +193,36 @@ extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, flo
     if (!src || !codes || !scales) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: NULL pointer");
     if (!aligned(src, dtype_bytes(dtype)) || !aligned(codes, 2) || !aligned(scales, 4))
         return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: misaligned buffers");
-    const dim3 grid(static_cast<unsigned>(num_blocks));
     auto s = static_cast<cudaStream_t>(stream);
     auto c = static_cast<uint8_t *>(codes);
     cudaError_t e;
+    const int vec = 16 / dtype_bytes(dtype);
+    if (head_dim % vec == 0 && aligned(src, 16) && aligned(codes, 8) &&
+        static_cast<int64_t>(block_size) * (head_dim / vec) <= 32 * kQuantVecs) {
+        const int64_t slices = static_cast<int64_t>(num_blocks) * num_kv_heads;
+        int64_t grid = (slices + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+        const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+        if (grid > cap) grid = cap;
+        const dim3 g(static_cast<unsigned>(grid));
+        switch (dtype) {
+        case PKV_BF16:
+            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<__nv_bfloat16>, g, dim3(kQuantThreads), 0, s,
+                           static_cast<const __nv_bfloat16 *>(src), c, scales, slices, block_size, num_kv_heads,
+                           head_dim);
+            break;
+        case PKV_F16:
+            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<__half>, g, dim3(kQuantThreads), 0, s,
+                           static_cast<const __half *>(src), c, scales, slices, block_size, num_kv_heads, head_dim);
+            break;
+        default:
+            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<float>, g, dim3(kQuantThreads), 0, s,
+                           static_cast<const float *>(src), c, scales, slices, block_size, num_kv_heads, head_dim);
+            break;
+        }
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize fp8 launch: %s", cudaGetErrorString(e));
+        return ok();
+    }
+    const dim3 grid(static_cast<unsigned>(num_blocks));
     switch (dtype) {
     case PKV_BF16:
         e = launch_pdl(kPdlStore, quantize_fp8_kernel<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, s,

@@ -17,11 +17,13 @@ def _max_err(out, ref):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
-def test_quantize_fp8_matches_oracle(pkv, orc, cuda_dev, dtype):
-    g = torch.Generator().manual_seed(50)
-    nb, bs, H, d = 24, 16, 8, 128
+@pytest.mark.parametrize("nb,bs,H,d", [(24, 16, 8, 128), (10, 16, 4, 72), (10, 16, 3, 36), (7, 32, 2, 128)])
+def test_quantize_fp8_matches_oracle(pkv, orc, cuda_dev, dtype, nb, bs, H, d):
+    """Vector kernel (16-byte loads, slice in registers) where the slice fits,
+    pair kernel otherwise (d = 36, 32-token blocks, fp32 rows of 128)."""
+    g = torch.Generator().manual_seed(50 + d)
     cache = torch.randn(nb, bs, H, d, generator=g) * torch.logspace(-3, 3, nb)[:, None, None, None]
-    cache[3, :, 2] = 0            # an all-zero (block, head): scale 0, codes +0
+    cache[3, :, H - 1] = 0        # an all-zero (block, head): scale 0, codes +0
     cache[5, 7, 1, 9] = float("nan")  # ignored by the max, stored as NaN
     cache = cache.to(dtype)
     codes, scales = pkv.pkv_quantize_kvcache_fp8(cache.to(cuda_dev))
