@@ -47,6 +47,7 @@ import pkv_workloads as wl  # noqa: E402
 METRIC = "paged decode-attention KV GB/s and % of GB300 HBM roofline; decode tokens/s"
 DEFAULT_CONFIG = "llama2-7b-layer-fp16"
 DECODE_CONFIGS = ["llama2-7b-layer-fp16", "qwen3-0.6b-gqa-bf16", "long-gqa-8k-bf16", "long-gqa-32k-bf16"]
+CSR_CONFIGS = ["csr-prefix-bf16"]
 DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
 HBM_FALLBACK_GBS = 6800.0
 
@@ -57,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=DECODE_CONFIGS, default=DEFAULT_CONFIG)
+    ap.add_argument("--config", choices=DECODE_CONFIGS + CSR_CONFIGS, default=DEFAULT_CONFIG)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="wall-clock budget of the oracle CPU-baseline sample")
@@ -862,6 +863,315 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# ----------------------------------------------------------------------------- CSR prefix-shared workload
+def csr_step_bytes(cfg: wl.CsrConfig, snap):
+    """Per-kernel bytes of one CSR pass: unique (written rows plus every page
+    row once: what HBM must move when shared pages are read once) and logical
+    (every row a sequence names).  Returns (unique, logical, unique tokens)."""
+    es = torch.tensor([], dtype=cfg.dtype).element_size()
+    S, T, nnz = cfg.num_seqs, snap.total_tokens, int(snap.block_table.numel())
+    row = cfg.num_heads * cfg.head_dim * es
+    n_shared = int(cfg.num_seqs * cfg.shared_fraction)
+    unique_tokens = T - max(n_shared - 1, 0) * cfg.prefix_tokens
+    idx = nnz * 4 + (S + 1) * 12                        # block table, seq_ptr, token_ptr
+    q_bytes = S * cfg.num_heads * cfg.head_dim * es
+    tables = int(snap.block_tables_2d.numel()) * 4 + S * 4
+    unique = {
+        "unpack_k": T * row + unique_tokens * row + idx,
+        "unpack_v": T * row + unique_tokens * row + idx,
+        "paged_attention_decode": unique_tokens * 2 * row + 2 * q_bytes + tables,
+    }
+    logical = {
+        "unpack_k": 2 * T * row + idx,
+        "unpack_v": 2 * T * row + idx,
+        "paged_attention_decode": T * 2 * row + 2 * q_bytes + tables,
+    }
+    return unique, logical, unique_tokens
+
+
+class CsrStep:
+    """One pass over a block-paged snapshot whose first half of the sequences
+    alias the same prefix pages: unpack of K and of V into contiguous
+    [total_tokens, H, d] buffers, and decode attention over the same pages
+    through the padded 2-D table (Hq == Hkv == H).  Byte counts per kernel:
+    logical (every row a sequence names) and unique (every page row once: what
+    HBM must move when the shared pages are read once)."""
+
+    def __init__(self, pkv, cfg: wl.CsrConfig, seed: int, device):
+        self.pkv, self.cfg, self.device = pkv, cfg, device
+        self.snap = s = wl.csr_snapshot(cfg, seed=seed, device=device)
+        H, d = cfg.num_heads, cfg.head_dim
+        es = torch.tensor([], dtype=cfg.dtype).element_size()
+        self.dt = pkv._DTYPE[cfg.dtype]
+        self.S, self.T, self.nnz = cfg.num_seqs, s.total_tokens, int(s.block_table.numel())
+        self.num_pages = int(s.k_pool.shape[0])
+        self.maxc = int(s.seq_lens.max())
+        self.out_k = torch.empty(self.T, H, d, dtype=cfg.dtype, device=device)
+        self.out_v = torch.empty_like(self.out_k)
+        self.out = torch.empty_like(s.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        ws = pkv.pkv_paged_attention_decode_workspace_size(self.S, H, H, d, cfg.page_size, self.maxc, cfg.dtype)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
+        self.bytes, self.logical, self.unique_tokens = csr_step_bytes(cfg, s)
+
+    def _unpack(self, stream_ptr, dst, pool, s) -> int:
+        L, p, c = self.pkv._lib, (lambda t: t.data_ptr()), self.cfg
+        return L.pkv_unpack_block_paged(p(dst), p(pool), p(s.block_table), p(s.seq_ptr), self.pkv.PKV_U32,
+                                        p(s.token_ptr), self.S, self.nnz, c.page_size, self.num_pages, c.num_heads,
+                                        c.head_dim, self.T, self.dt, p(self.err), stream_ptr)
+
+    def attention(self, stream_ptr) -> int:
+        L, p, c, s = self.pkv._lib, (lambda t: t.data_ptr()), self.cfg, self.snap
+        return L.pkv_paged_attention_decode(p(self.out), p(s.q), p(s.k_pool), p(s.v_pool), p(s.block_tables_2d),
+                                            s.block_tables_2d.shape[1], p(s.seq_lens), self.S, c.num_heads,
+                                            c.num_heads, c.head_dim, c.page_size, self.num_pages, self.maxc,
+                                            s.scale, self.dt, p(self.workspace), self.workspace.numel(),
+                                            p(self.err), stream_ptr)
+
+    def run(self, stream_ptr, events=None):
+        """Enqueue one pass (unpack K, unpack V, attention); events (4) bracket the kernels if given."""
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        s = self.snap
+        rec(0)
+        ok = self._unpack(stream_ptr, self.out_k, s.k_pool, s)
+        rec(1)
+        ok |= self._unpack(stream_ptr, self.out_v, s.v_pool, s)
+        rec(2)
+        ok |= self.attention(stream_ptr)
+        rec(3)
+        if ok != 0:
+            raise RuntimeError("pkv call failed: " + self.pkv._lib.pkv_last_error_string().decode())
+
+    # pipelined end-to-end loop: per-step inputs are q and the index buffers; the pools are resident
+    def input_sets(self):
+        if not hasattr(self, "_sets"):
+            from dataclasses import replace
+
+            s = self.snap
+            s1 = replace(s, q=s.q.clone(), block_table=s.block_table.clone(), seq_ptr=s.seq_ptr.clone(),
+                         token_ptr=s.token_ptr.clone(), seq_lens=s.seq_lens.clone(),
+                         block_tables_2d=s.block_tables_2d.clone())
+            self._sets = [(s, None, self.out), (s1, None, torch.empty_like(self.out))]
+        return self._sets
+
+    def run_set(self, stream_ptr, k: int):
+        keep = (self.snap, self.out)
+        self.snap, _, self.out = self.input_sets()[k]
+        try:
+            self.run(stream_ptr)
+        finally:
+            self.snap, self.out = keep
+
+    def host_inputs(self, k: int = 0):
+        s = self.input_sets()[k][0]
+        dev = [s.q, s.block_table, s.seq_ptr, s.token_ptr, s.seq_lens, s.block_tables_2d]
+        return list(zip([t.cpu().pin_memory() for t in dev], dev))
+
+
+def time_csr_kernels(step: CsrStep, steps: int, world: int, stream):
+    """Per-call times of the three kernels: eager launches with events between
+    them, a 512 MB L2-evicting read before every pass (outside the events)."""
+    ptr = ctypes.c_void_p(stream.cuda_stream)
+    evict = torch.ones(L2_EVICT_BYTES // 4, dtype=torch.float32, device=step.device)
+    sink = torch.empty((), dtype=torch.float32, device=step.device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step.run(ptr)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        for i in range(steps):
+            torch.sum(evict, dim=0, out=sink)
+            step.run(ptr, evs[i])
+        torch.cuda.synchronize()
+        barrier(world)
+    names = ["unpack_k", "unpack_v", "paged_attention_decode"]
+    return {n: statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, n in enumerate(names)}
+
+
+def csr_oracle_run(s, step_bytes_total: int, max_seqs: int, budget_s: float):
+    """The oracle on whole sequences of the snapshot, one at a time (each
+    sequence's pages gathered into a compact pool first, outside the clock):
+    unpack of K and V and decode attention.  Returns (GB/s, seconds,
+    sequences, bytes), the bytes being the sequences' share of the pass's
+    unique bytes (their tokens over all tokens)."""
+    import oracle as orc
+
+    orc.build()
+    bt, sp, lens = s.block_table.cpu().to(torch.int64), s.seq_ptr.cpu().to(torch.int64), s.seq_lens.cpu()
+    S = int(lens.numel())
+    done, t, tokens = 0, 0.0, 0
+    while done < min(max_seqs, S) and t < budget_s:
+        pages = bt[sp[done]:sp[done + 1]]
+        n = int(lens[done])
+        kc = s.k_pool[pages.to(s.k_pool.device)].cpu()
+        vc = s.v_pool[pages.to(s.v_pool.device)].cpu()
+        local = torch.arange(pages.numel(), dtype=torch.int32)
+        seq_ptr = torch.tensor([0, pages.numel()], dtype=torch.int32)
+        token_ptr = torch.tensor([0, n], dtype=torch.int64)
+        q = s.q[done:done + 1].cpu()
+        t0 = time.perf_counter()
+        for pool in (kc, vc):
+            orc.unpack_block_paged(pool, local, seq_ptr, token_ptr, index_dtype=torch.int32)
+        orc.paged_attention_decode(q, kc, vc, local[None, :], torch.tensor([n], dtype=torch.int32), s.scale)
+        t += time.perf_counter() - t0
+        tokens += n
+        done += 1
+    nbytes = step_bytes_total * tokens / s.total_tokens
+    return nbytes / t / 1e9, t, done, nbytes
+
+
+def run_csr(args, world, rank, local):
+    """Bench line of the prefix-shared CSR workload: unpack K and V plus decode
+    attention over the snapshot's pages, per step."""
+    import pagedattention_decode_pkv_gb300 as pkv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = wl.CONFIGS[args.config]
+    step = CsrStep(pkv, cfg, seed=args.seed + rank, device=device)
+    stream = torch.cuda.Stream(device)
+    ptr = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step.run(ptr)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, (tw0, tw1) = time_graphs(step, args.steps, world)
+    clocks = sampler.summary(tw0, tw1)
+    sampler.stop()
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    if err:
+        raise RuntimeError(f"device error bits {err:#x} during the benchmark")
+    per = time_csr_kernels(step, args.steps, world, stream)
+    io, h2d, d2h = e2e_io(step)
+    e2e_ms, _ = time_graphs(step, args.steps, world, io)
+
+    total_ms_max = reduce_max(total_ms, world, device)
+    e2e_ms_max = reduce_max(e2e_ms, world, device)
+    all_bytes = reduce_sum(sum(step.bytes.values()) * args.steps, world, device)
+    all_logical = reduce_sum(sum(step.logical.values()) * args.steps, world, device)
+    value = all_bytes / (total_ms_max * 1e-3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    unpack_ms = reduce_max((per["unpack_k"] + per["unpack_v"]) / 2, world, device)
+    unpack_gbs = step.bytes["unpack_k"] / (unpack_ms * 1e-3) / 1e9
+    attn_ms = reduce_max(per["paged_attention_decode"], world, device)
+
+    cpu_baseline = None
+    if world == 1 and not args.skip_cpu_baseline:
+        gbs, secs, nseq, nbytes = csr_oracle_run(step.snap, sum(step.bytes.values()), step.S, args.cpu_budget_s)
+        cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                        "sample": f"first {nseq} of {step.S} sequences, each unpacked (K and V) and attended alone "
+                                  f"in {secs:.1f} s, single-threaded C oracle in binary64; bytes are those "
+                                  f"sequences' token share of the pass's unique bytes ({nbytes / 1e9:.3f} GB)"}
+
+    if rank != 0:
+        return 0
+    per_us = {k: round(v * 1e3, 2) for k, v in per.items()}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
+        "data": "synthetic (seeded N(0,1) pools and q, randomly permuted pages, half the sequences aliasing one "
+                "1024-token prefix)",
+        "config": {
+            "workload": cfg.name, "description": cfg.description, "num_seqs": step.S,
+            "num_heads": cfg.num_heads, "head_dim": cfg.head_dim, "page_size": cfg.page_size,
+            "total_tokens": step.T, "unique_tokens": step.unique_tokens, "nnz": step.nnz,
+            "pages": step.num_pages,
+            "step": "unpack K + unpack V (u32 CSR index buffers) + paged_attention_decode (+combine) over the "
+                    "padded table",
+            "step_bytes": sum(step.bytes.values()), "step_bytes_logical": sum(step.logical.values()),
+            "l2": f"outputs of {2 * step.out_k.numel() * step.out_k.element_size() / 1e9:.2f} GB per step vs "
+                  "129 MB L2; no flush",
+            "parallelism": f"replicas x{world} (independent snapshots per rank, no data-path collective)",
+        },
+        "value_logical": round(all_logical / (total_ms_max * 1e-3) / 1e9, 2),
+        "kernel_us": per_us,
+        "kernel_gbs": {k: round(step.bytes[k] / (per[k] * 1e-3) / 1e9, 1) for k in per},
+        "kernel_gbs_logical": {k: round(step.logical[k] / (per[k] * 1e-3) / 1e9, 1) for k in per},
+        "roofline": {"kernel": "pkv_unpack_block_paged (per role)", "bound": "hbm",
+                     "achieved": round(unpack_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(unpack_gbs / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "us_per_call": round(unpack_ms * 1e3, 2)},
+        "attention": {"us_per_call": round(attn_ms * 1e3, 2),
+                      "gbs_unique": round(step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9, 1),
+                      "gbs_logical": round(step.logical["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9, 1),
+                      "decode_tokens_per_s": round(step.S / (attn_ms * 1e-3), 1)},
+        "cpu_baseline": cpu_baseline,
+        "e2e": {"value": round(all_bytes / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms_max / args.steps, 4)},
+        "gpu_launches": 4 * args.steps,
+        "timing": {"value": f"CUDA graphs of {STEPS_PER_GRAPH} passes replayed until `steps` passes ran between "
+                            "two CUDA events; value counts unique bytes (each page row read once, every output "
+                            "row written), value_logical every row a sequence names",
+                   "kernel_us": "second pass: eager passes with CUDA events between the kernels, a 512 MB read "
+                                "before each pass (outside the events) evicts L2",
+                   "e2e": "graphs of the same passes as a pipelined loop runs them: q and the index buffers copied "
+                          "from pinned host memory each pass (two device input sets, copies on a second stream), "
+                          "the attention output and error flag read back"},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+
+def run_reference_csr(args, world, rank):
+    """The oracle as it stands on the CSR workload: two sequences per step,
+    each unpacked (K and V) and attended alone; no library call."""
+    if rank != 0:
+        return 0
+    cfg = wl.CONFIGS[args.config]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    snap = wl.csr_snapshot(cfg, seed=args.seed, device=device)
+    unique, _, _ = csr_step_bytes(cfg, snap)
+    total = sum(unique.values())
+    per_step = 2
+    t, nbytes = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        sub = csr_sub_snapshot(snap, i * per_step % cfg.num_seqs, per_step)
+        _, dt, _, nb = csr_oracle_run(sub, total * sub.total_tokens / snap.total_tokens, per_step, 1e9)
+        if i >= args.warmup:
+            t += dt
+            nbytes += nb
+    value = nbytes / t / 1e9
+    sample = (f"{per_step} sequences of the {cfg.name} snapshot per step, each unpacked (K and V) and attended "
+              "alone; single-threaded C oracle in binary64; bytes are their token share of the pass's unique bytes")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
+        "data": "synthetic (seeded N(0,1), randomly permuted pages, aliased prefix)",
+        "config": {"workload": cfg.name, "description": cfg.description, "num_seqs": cfg.num_seqs,
+                   "l2": "bounded CPU sample; no GPU work"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def csr_sub_snapshot(snap, first: int, count: int):
+    """Sequences [first, first + count) of a CSR snapshot as a snapshot of
+    their own (same pools; index buffers rebased)."""
+    from dataclasses import replace
+
+    sp = snap.seq_ptr.cpu().to(torch.int64)
+    lens = snap.seq_lens.cpu()[first:first + count]
+    bt = snap.block_table.cpu()[sp[first]:sp[first + count]]
+    new_sp = (sp[first:first + count + 1] - sp[first]).to(snap.seq_ptr.dtype)
+    tp = torch.zeros(count + 1, dtype=torch.int64)
+    tp[1:] = torch.cumsum(lens.to(torch.int64), 0)
+    return replace(snap, block_table=bt, seq_ptr=new_sp, token_ptr=tp, seq_lens=lens,
+                   block_tables_2d=snap.block_tables_2d.cpu()[first:first + count],
+                   q=snap.q[first:first + count])
+
 def run_profile_calls(args, local):
     """The workload's attention calls only, for an ncu capture of one launch."""
     import pagedattention_decode_pkv_gb300 as pkv
@@ -890,6 +1200,12 @@ def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_init(args)
     try:
+        if args.config in CSR_CONFIGS:
+            if args.impl == "reference":
+                return run_reference_csr(args, world, rank)
+            if args.profile_calls:
+                raise SystemExit("--profile-calls takes a decode workload")
+            return run_csr(args, world, rank, local)
         if args.impl == "reference":
             return run_reference(args, world, rank)
         if args.profile_calls:
