@@ -10,70 +10,125 @@
 //     out[cu_q[b] + i, h] = softmax_{t <= p}(scale * q . K[t]) . V[t],
 // query head h reading KV head h / (Hq / H_kv).
 //
-// Design (mma.sync, FlashAttention-2 style).  A CTA owns 64 query rows of one
-// KV head: 64 / G positions x the G query heads of the group, so every K/V
-// byte it stages serves all G heads.  A producer warp streams 16-token K and V
-// tiles of that head through a TMA -> shared-memory ring (the decode path's
-// 3-D tensor map with one head per box, 128-byte swizzle).  The Q rows sit in
-// shared memory (swizzled 256-byte rows), which keeps the consumers at 128
-// registers and three CTAs per SM.  Four consumer warps take 16 rows each
-// and, per stage, compute S = Q K^T (16 MMAs in four independent chains:
-// ldmatrix of Q as A and of K as B), the online softmax on the accumulators
-// (row statistics over the quad of lanes sharing a row), and O += P V (16
-// MMAs: P re-used from the accumulator layout as the A operand, V through
-// ldmatrix.trans).  Grid (B, H_kv, query tiles) with the tile index counted
-// from the end of each sequence, so the longest tiles (most keys) launch
-// first.
+// Design (fifth-generation tensor cores, FlashAttention style).  A CTA owns
+// 128 query rows of one KV head: 128 / G positions x the G query heads of the
+// group, so every K/V byte it stages serves all G heads.  Keys go by blocks of
+// 128.  Per block j:
+//   * a producer warp copies K_j and V_j (the head's rows of the pages that
+//     hold keys 128j .. 128j + 127) into a two-stage ring with TMA, in chunks of
+//     gcd(block_size, 128) tokens per 64-dim half, 128-byte swizzled;
+//   * an MMA warp issues S_j = Q K_j^T (M = 128 rows, N = 128 keys, eight
+//     K = 16 steps over the head dimension) into one of two TMEM buffers, and,
+//     one block behind, O += P_{j-1} V_{j-1} (N = 128 dims, eight K = 16 steps
+//     over the keys; V is the MN-major B operand) into a TMEM accumulator;
+//   * four softmax warps, one query row per thread, read the row of S_j from
+//     TMEM, mask it (causal, keys of missing pages), keep the row's running
+//     maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m) as
+//     16-bit values into a shared-memory tile (K-major A operand of the PV MMA).
+// The reference maximum m of a row moves only when the block's maximum exceeds
+// it by more than 2^8 (log2 units), and then O's row is rescaled in TMEM;
+// otherwise P is computed against the older m (values up to 256), which keeps
+// the result the plain softmax.  The row sum adds the same rounded 16-bit P
+// values the PV MMA multiplies, so the weights of the V rows sum to one (a
+// single dominant key gives its V row exactly, wherever m stands).  The last
+// PV's accumulator, divided by the row sum, is the output row.
+// Grid (B, H_kv, query tiles) with the tile index counted from the end of each
+// sequence, so the longest tiles (most keys) launch first.  Every wait is
+// bounded (PKV_ERRBIT_TIMEOUT), and the CTA waits for its own copies and MMAs
+// before it frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+#include <type_traits>
+
 #include "pkv_internal.h"
 #include "pkv_pdl.cuh"
+#include "pkv_tc.cuh"
 #include "pkv_tma.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kPreRows = 64;          // query rows (position x head) per CTA
-constexpr int kPreWarps = 4;          // consumer warps, 16 rows each
-constexpr int kPreStages = 6;         // K/V ring depth
-constexpr int kPreTile = 2 * kStageTokens * 128;  // one head's 16 tokens of K (or V): 4 KB
+constexpr int kPreRows = 128;        // query rows (position x head) per CTA = TMEM lanes = MMA M
+constexpr int kPreKeys = 128;        // keys per block = the S MMA's N
+constexpr int kPreStages = 2;        // K/V ring depth (blocks)
+constexpr int kPreSoftmaxWarps = 4;  // one query row per thread
+constexpr int kPreThreads = (kPreSoftmaxWarps + 2) * 32;  // + producer warp + MMA warp
+constexpr int kPreHalf = kPreKeys * 128;                   // one 64-dim half of a [128 rows][128 dims] tile
+constexpr int kPreTileBytes = 2 * kPreHalf;                // 32 KB
+constexpr uint32_t kPreTmemCols = 512;                      // S0, S1, O (128 columns each), rounded up
 constexpr uint64_t kPreDeadlineNs = 2000000000ull;
 constexpr float kPreLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8 between rescales
+
+// Sum of the two 16-bit values packed in w (low and high half), in f32.
+template <typename T> __device__ __forceinline__ float pair_sum(uint32_t w);
+template <> __device__ __forceinline__ float pair_sum<__nv_bfloat16>(uint32_t w) {
+    return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+}
+template <> __device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __low2float(h) + __high2float(h);
+}
 
 struct PreSmem {
-    static constexpr int kStageBytes = 2 * kPreTile;           // K then V
-    static constexpr int kQOffset = kPreStages * kStageBytes;   // Q rows [64][256 B], chunks swizzled by row
-    static constexpr int kIdOffset = kQOffset + kPreRows * 256;  // int32 block id per ring slot (-1: skipped)
-    static constexpr int kBarOffset = kIdOffset + 16 * kPreStages;
-    static constexpr int kBytes = kBarOffset + 16 * kPreStages;
+    static constexpr int kQ = 0;                                         // [2 halves][128 rows][128 B]
+    static constexpr int kP = kQ + kPreTileBytes;                        // same layout
+    static constexpr int kKV = kP + kPreTileBytes;                       // stage s: K at +64 KB s, V at +32 KB
+    static constexpr int kKeys = kKV + kPreStages * 2 * kPreTileBytes;   // int32 [stage][8 chunks] valid keys
+    static constexpr int kBar = kKeys + 128;                             // mbarriers, 8 bytes each
+    static constexpr int kTmemSlot = kBar + 128;
+    static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
 };
+// mbarrier indices
+constexpr int kBarKvFull = 0;   // [2] producer: expect_tx + the copies' bytes
+constexpr int kBarKvEmpty = 2;  // [2] MMA commit after the block's PV
+constexpr int kBarSFull = 4;    // [2] MMA commit after S = Q K^T
+constexpr int kBarSFree = 6;    // [2] 128 softmax threads have read S
+constexpr int kBarPFull = 8;    // 128 softmax threads wrote P (and rescaled O)
+constexpr int kBarODone = 9;    // MMA commit after O += P V
+constexpr int kBarQFull = 10;   // 128 softmax threads wrote Q
+constexpr int kBarFinal = 11;   // MMA commit: every MMA of the CTA has completed
+constexpr int kNumBars = 12;
+static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
 
 template <typename T>
-__global__ void __launch_bounds__((kPreWarps + 1) * 32, 3)
+__global__ void __launch_bounds__(kPreThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                int32_t max_blocks, const int32_t *__restrict__ starts, const int32_t *__restrict__ cu_q,
-               int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, float scale_log2,
+               int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, int32_t box_rows, float scale_log2,
                int32_t *__restrict__ err_flag) {
     using L = PreSmem;
     using H = Half16<T>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const int b = blockIdx.x, kh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    int32_t *ids = reinterpret_cast<int32_t *>(smem + L::kIdOffset);
-    const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
-    const uint32_t tiles = smem_u32(smem);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kPreStages; ++i) {
-            mbar_init(bar0 + 8 * i, 1);
-            mbar_init(bar0 + 8 * (kPreStages + i), kPreWarps);
+    int32_t *kv_keys = reinterpret_cast<int32_t *>(smem + L::kKeys);
+    const uint32_t bar0 = smem_u32(smem + L::kBar);
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    const uint32_t sQ = smem_u32(smem + L::kQ), sP = smem_u32(smem + L::kP), sKV = smem_u32(smem + L::kKV);
+    if (warp == kPreSoftmaxWarps && lane == 0) {
+        for (int s = 0; s < kPreStages; ++s) {
+            mbar_init(bar(kBarKvFull + s), 1);
+            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarSFull + s), 1);
+            mbar_init(bar(kBarSFree + s), kPreRows);
         }
+        mbar_init(bar(kBarPFull), kPreRows);
+        mbar_init(bar(kBarODone), 1);
+        mbar_init(bar(kBarQFull), kPreRows);
+        mbar_init(bar(kBarFinal), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
     }
     pdl_wait();
     pdl_trigger();
@@ -95,237 +150,267 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         return;
     }
+    // From here on the CTA holds TMEM: every path goes to the common exit below.
+    if (warp == kPreSoftmaxWarps + 1) tmem_alloc(smem_u32(smem + L::kTmemSlot), kPreTmemCols);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
     const int q0 = tile * positions;                          // first query index of the tile
     const int last_pos = start + min(n, q0 + positions) - 1;  // the tile's last position
-    const int nstages = last_pos / kStageTokens + 1;
+    const int nblk = last_pos / kPreKeys + 1;
     const uint64_t deadline = global_ns() + kPreDeadlineNs;
+    bool timed_out = false;
 
-    if (warp == kPreWarps) {
+    if (warp == kPreSoftmaxWarps) {
         // ------------------------------------------------------------ producer warp
+        // Block j's keys come in chunks of box_rows (= gcd(block_size, 128)) keys:
+        // lane l < 128 / box_rows takes chunk l, whose rows are consecutive in one
+        // page.  Chunks at or past the end of the span, or of a page whose id is
+        // out of range, are not copied; kv_keys[stage][l] gives the consumers the
+        // chunk's number of valid keys.
         const int32_t *row = block_tables + static_cast<int64_t>(b) * max_blocks;
-        bool aborted = false, bad = false;
-        for (int s0 = 0; s0 < nstages && !aborted; s0 += 32) {
-            const int s = s0 + lane;
-            int id = -1;
-            if (s < nstages) id = row[s * kStageTokens / bs];
-            const int cnt = min(32, nstages - s0);
-            for (int j = 0; j < cnt; ++j) {
-                const int i = s0 + j, slot = i % kPreStages;
-                int ok = 1;
-                if (lane == 0 && i >= kPreStages)
-                    ok = mbar_wait(bar0 + 8 * (kPreStages + slot), ((i / kPreStages) - 1) & 1, deadline) ? 1 : 0;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    aborted = true;
-                    break;
-                }
-                const int bid = __shfl_sync(0xffffffffu, id, j);
-                if (lane == 0) {
-                    const uint32_t full = bar0 + 8 * slot;
-                    if (bid >= 0 && bid < num_blocks) {
-                        ids[slot] = bid;
-                        const int slot_row = bid * bs + (i * kStageTokens) % bs;
-                        const uint32_t dst = tiles + slot * L::kStageBytes;
-                        mbar_arrive_expect_tx(full, L::kStageBytes);
-                        tma_load_3d(dst, &tm_k, 0, slot_row, 2 * kh, full);
-                        tma_load_3d(dst + kPreTile, &tm_v, 0, slot_row, 2 * kh, full);
-                    } else {
-                        bad = true;
-                        ids[slot] = -1;
-                        mbar_arrive(full);  // nothing to load: every key of the stage is masked
-                    }
-                }
-                __syncwarp();
+        const int nch = kPreKeys / box_rows;
+        const uint32_t chunk_bytes = static_cast<uint32_t>(box_rows) * 128;  // one 64-dim half of a chunk
+        bool bad = false;
+        int issued = 0;
+        for (int j = 0; j < nblk; ++j) {
+            const int s = j % kPreStages;
+            int ok = 1;
+            if (lane == 0 && j >= kPreStages) ok = mbar_wait(bar(kBarKvEmpty + s), ((j / kPreStages) - 1) & 1, deadline);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                timed_out = true;
+                break;
             }
+            const int key0 = j * kPreKeys + lane * box_rows;
+            int id = -1, keys = 0;
+            if (lane < nch && key0 < total) {  // key0 / bs < ceil(total / bs) <= max_blocks
+                id = row[key0 / bs];
+                if (id < 0 || id >= num_blocks) {
+                    bad = true;
+                } else {
+                    const int64_t left = total - key0;
+                    keys = left < box_rows ? static_cast<int>(left) : box_rows;
+                }
+            }
+            if (lane < nch) kv_keys[s * 8 + lane] = keys;
+            const uint32_t full = bar(kBarKvFull + s);
+            const unsigned loaded = __ballot_sync(0xffffffffu, keys > 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(loaded)) * 4u * chunk_bytes);
+            __syncwarp();
+            if (keys > 0) {
+                const int slot_row = id * bs + key0 % bs;
+                const uint32_t kdst = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + lane * chunk_bytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_3d(kdst + h * kPreHalf, &tm_k, 0, slot_row, 2 * kh + h, full);
+                    tma_load_3d(kdst + kPreTileBytes + h * kPreHalf, &tm_v, 0, slot_row, 2 * kh + h, full);
+                }
+            }
+            issued = j + 1;
         }
+        bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
-            if (aborted && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
             if (bad && err_flag && kh == 0 && tile == tiles_b - 1) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
             // no bulk copy may still be writing shared memory when the CTA exits
-            const int issued = nstages;
-            for (int i = issued - kPreStages > 0 ? issued - kPreStages : 0; i < issued; ++i)
-                if (!mbar_wait(bar0 + 8 * (i % kPreStages), (i / kPreStages) & 1, deadline) && err_flag)
-                    atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+            for (int j = issued - kPreStages > 0 ? issued - kPreStages : 0; j < issued; ++j)
+                if (!mbar_wait(bar(kBarKvFull + j % kPreStages), (j / kPreStages) & 1, deadline)) timed_out = true;
         }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumer warps
-    const int g = lane >> 2, t = lane & 3;
-    // rows of this warp: r = 16 warp + g (and + 8) -> position index r / G, head r % G
-    const int r0 = 16 * warp + g, r1 = r0 + 8;
-    const int pos0 = start + q0 + r0 / G, pos1 = start + q0 + r1 / G;  // positions of the two rows
-    const bool live0 = q0 + r0 / G < n, live1 = q0 + r1 / G < n;
-    const int64_t qrow0 = (static_cast<int64_t>(q_begin) + q0 + r0 / G) * Hq + kh * G + r0 % G;
-    const int64_t qrow1 = (static_cast<int64_t>(q_begin) + q0 + r1 / G) * Hq + kh * G + r1 % G;
-    // Q rows of this warp into shared memory (zeros past the sequence): lane l
-    // copies half l & 1 of row l >> 1; 16-byte chunk c of row r sits at c ^ (r & 7)
-    const uint32_t qs = smem_u32(smem + L::kQOffset);
-    {
-        const int rw = lane >> 1, hf = lane & 1, r = 16 * warp + rw;
-        const bool live = q0 + r / G < n;
-        const int4 *src = reinterpret_cast<const int4 *>(
-            q + ((static_cast<int64_t>(q_begin) + q0 + r / G) * Hq + kh * G + r % G) * kFastHeadDim);
+    } else if (warp == kPreSoftmaxWarps + 1) {
+        // ------------------------------------------------------------ MMA warp
+        // S_j = Q K_j^T into TMEM columns [128 (j % 2), +128); one block behind,
+        // O (+)= P_{j-1} V_{j-1} into columns [256, 384).
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = umma_idesc_f16(kBf16, kPreRows, kPreKeys, false);
+            constexpr uint32_t kIdescO = umma_idesc_f16(kBf16, kPreRows, kFastHeadDim, true);
+            bool ok = mbar_wait(bar(kBarQFull), 0, deadline);
+            for (int j = 0; ok && j <= nblk; ++j) {
+                if (j < nblk) {
+                    const int s = j % kPreStages;
+                    ok = mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
+                    if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, deadline);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kt = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            const int c = 8 * hf + c8;
-            const int4 v = live ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(qs + r * 256 + ((c ^ (r & 7)) << 4)),
-                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
+                    for (int k = 0; k < kFastHeadDim / 16; ++k) {  // 16 dims (32 bytes) per step
+                        const uint32_t off = (k >> 2) * kPreHalf + (k & 3) * 32;
+                        umma_f16(tmem + (j & 1) * kPreKeys, umma_desc_sw128(sQ + off, 16, 1024),
+                                 umma_desc_sw128(kt + off, 16, 1024), kIdescS, k > 0);
+                    }
+                    umma_commit(bar(kBarSFull + (j & 1)));
+                }
+                if (j >= 1) {
+                    const int pj = j - 1, s = pj % kPreStages;
+                    ok = mbar_wait(bar(kBarPFull), pj & 1, deadline);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vt = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + kPreTileBytes;
+#pragma unroll
+                    for (int k = 0; k < kPreKeys / 16; ++k) {  // 16 keys (two 8-row groups) per step
+                        const uint32_t aoff = (k >> 2) * kPreHalf + (k & 3) * 32;
+                        umma_f16(tmem + 2 * kPreKeys, umma_desc_sw128(sP + aoff, 16, 1024),
+                                 umma_desc_sw128(vt + k * 2048, kPreHalf, 1024), kIdescO, (pj > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar(kBarODone));
+                    umma_commit(bar(kBarKvEmpty + s));
+                }
+            }
+            if (!ok) timed_out = true;
+            umma_commit(bar(kBarFinal));  // arrives once every MMA issued above has completed
+            if (!mbar_wait(bar(kBarFinal), 0, deadline)) timed_out = true;
         }
         __syncwarp();
-    }
-    uint32_t q_off[8];  // A fragments by ldmatrix: rows (lane & 7) + 8 ((lane >> 3) & 1), dims 16kc + 8 (lane >> 4)
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        // Thread r owns query row r: position index r / G, head r % G of the group.
+        const int r = threadIdx.x;
+        const int pi = r / G, hd = r - pi * G;
+        const bool live = q0 + pi < n;
+        const int pos = start + q0 + pi;
+        const int64_t qrow = (static_cast<int64_t>(q_begin) + q0 + pi) * Hq + kh * G + hd;
+        {  // Q row into shared memory (zeros past the sequence)
+            const int4 *src = reinterpret_cast<const int4 *>(q + qrow * kFastHeadDim);
 #pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-        const int r = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1), c = 2 * kc + (lane >> 4);
-        q_off[kc] = qs + r * 256 + ((c ^ (r & 7)) << 4);
-    }
-    // ldmatrix lane addresses inside a stage: K (B operand, non-transposed): matrix
-    // m = lane >> 3 covers keys 8 (m >> 1) .. +7 and dims 16kc + 8 (m & 1) .. +7;
-    // V (B operand, transposed): keys 8 (m & 1) .. +7, dims 8 (2j + (m >> 1)) .. +7.
-    const int mi = lane >> 3, rr = lane & 7;
-    uint32_t k_off[8], v_off[8];
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-        const int key = 8 * (mi >> 1) + rr, c16 = 2 * kc + (mi & 1);
-        k_off[kc] = ((c16 >> 3) * kStageTokens + key) * 128 + (((c16 & 7) ^ (key & 7)) << 4);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int key = 8 * (mi & 1) + rr, c16 = 2 * j + (mi >> 1);
-        v_off[j] = ((c16 >> 3) * kStageTokens + key) * 128 + (((c16 & 7) ^ (key & 7)) << 4);
-    }
-    float o[16][4];
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    for (int i = 0; i < nstages; ++i) {
-        const int slot = i % kPreStages;
-        if (!mbar_wait(bar0 + 8 * slot, (i / kPreStages) & 1, deadline)) {
-            if (lane == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
-            return;
-        }
-        const uint32_t kt = tiles + slot * L::kStageBytes, vt = kt + kPreTile;
-        const int kbase = i * kStageTokens;
-        const bool skipped = ids[slot] < 0;
-        if (!skipped) {
-            // keys at or past the end of the sequence may hold anything, NaN
-            // included: zero this stage's V rows there so that 0 * row stays 0
-            const int64_t left = total - kbase;
-            const int nvalid = left < kStageTokens ? static_cast<int>(left) : kStageTokens;
-            if (nvalid < kStageTokens) {
-                // all four consumer warps zero the same rows; each writes zeros only
-                for (int idx = lane; idx < (kStageTokens - nvalid) * 16; idx += 32) {
-                    const int tok = nvalid + (idx >> 4), half = (idx >> 3) & 1, chunk = idx & 7;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                                     vt + (half * kStageTokens + tok) * 128 + chunk * 16),
-                                 "r"(0)
-                                 : "memory");
-                }
-                __syncwarp();
-            }
-            // four independent accumulation chains (key halves x even / odd k-steps)
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int kc = 0; kc < 8; kc += 2) {
-                uint32_t bk[4], bk2[4], qa[4], qb[4];
-                ldsm_x4(q_off[kc], qa);
-                ldsm_x4(q_off[kc + 1], qb);
-                ldsm_x4(kt + k_off[kc], bk);  // (keys 0-7: dims lo, hi), (keys 8-15: dims lo, hi)
-                ldsm_x4(kt + k_off[kc + 1], bk2);
-                H::mma(sc[0], qa, bk[0], bk[1]);
-                H::mma(sc[1], qa, bk[2], bk[3]);
-                H::mma(sd[0], qb, bk2[0], bk2[1]);
-                H::mma(sd[1], qb, bk2[2], bk2[3]);
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
-            // scores of keys kbase + 8 nt + 2t + {0, 1}, rows pos0 / pos1; causal mask
-            float x[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = kbase + 8 * nt + 2 * t + e;
-                    x[nt][e] = (live0 && key <= pos0) ? sc[nt][e] * scale_log2 : -INFINITY;
-                    x[nt][2 + e] = (live1 && key <= pos1) ? sc[nt][2 + e] * scale_log2 : -INFINITY;
-                }
-            float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-            float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-#pragma unroll
-            for (int sh = 1; sh < 4; sh <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float a0 = fast_exp2(m0 - base0), a1 = fast_exp2(m1 - base1);
-            float p[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                p[nt][0] = fast_exp2(x[nt][0] - base0);
-                p[nt][1] = fast_exp2(x[nt][1] - base0);
-                p[nt][2] = fast_exp2(x[nt][2] - base1);
-                p[nt][3] = fast_exp2(x[nt][3] - base1);
-            }
-            m0 = mn0;
-            m1 = mn1;
-            l0 = l0 * a0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-            l1 = l1 * a1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-#pragma unroll
-            for (int dt = 0; dt < 16; ++dt) {
-                o[dt][0] *= a0;
-                o[dt][1] *= a0;
-                o[dt][2] *= a1;
-                o[dt][3] *= a1;
-            }
-            // P as the A operand (rows g / g+8, keys 2t.. and 8+2t..)
-            uint32_t pa[4];
-            pa[0] = H::pack(p[0][0], p[0][1]);
-            pa[1] = H::pack(p[0][2], p[0][3]);
-            pa[2] = H::pack(p[1][0], p[1][1]);
-            pa[3] = H::pack(p[1][2], p[1][3]);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t bv[4];
-                ldsm_x4_trans(vt + v_off[j], bv);  // dims 16j .. +7: (keys 0-7, 8-15); dims 16j+8 ..: same
-                H::mma(o[2 * j], pa, bv[0], bv[1]);
-                H::mma(o[2 * j + 1], pa, bv[2], bv[3]);
+            for (int c = 0; c < 16; ++c) {
+                const int4 v = live ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + (c >> 3) * kPreHalf + r * 128 +
+                                                                               (((c & 7) ^ (r & 7)) << 4)),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(bar(kBarQFull));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8 * (kPreStages + slot));
-    }
+        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
+        float m_ref = -INFINITY, l_sum = 0.f;
+        for (int j = 0; j < nblk; ++j) {
+            const int s = j % kPreStages;
+            bool ok = mbar_wait(bar(kBarSFull + (j & 1)), (j >> 1) & 1, deadline) &&
+                      mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
+            if (!__all_sync(0xffffffffu, ok)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            float x[kPreKeys];
 #pragma unroll
-    for (int sh = 1; sh < 4; sh <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
-    }
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    // C fragment: rows g / g+8, dims 8 dt + 2t, +1
+            for (int c0 = 0; c0 < kPreKeys; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(trow + (j & 1) * kPreKeys + c0, v);
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-        const int d = 8 * dt + 2 * t;
-        if (live0) {
-            T *dst = out + qrow0 * kFastHeadDim + d;
-            dst[0] = from_f32<T>(o[dt][0] * inv0);
-            dst[1] = from_f32<T>(o[dt][1] * inv0);
+                for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kBarSFree + (j & 1)));
+            // Valid keys of each 16-key group: causal limit and the chunk's copied keys.
+            int lim[8];
+            {
+                const int causal = live ? pos - j * kPreKeys : -1;  // keys k <= causal are visible
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int ch = (16 * g) / box_rows, off = 16 * g - ch * box_rows;
+                    const int copied = kv_keys[s * 8 + ch] - off;  // valid keys of the group, from its first
+                    const int c = causal - 16 * g;
+                    lim[g] = min(c, min(copied, 16) - 1);      // keys 16g + i valid for i <= lim[g]
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kPreKeys; ++k) {
+                x[k] = (k & 15) <= lim[k >> 4] ? x[k] * scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[k]);
+            }
+            float a = 1.f;
+            bool resc = false;
+            if (mx > m_ref + kRescaleThreshold) {  // also the row's first visible key (m_ref = -inf)
+                if (m_ref != -INFINITY) {
+                    a = fast_exp2(m_ref - mx);
+                    resc = true;
+                }
+                m_ref = mx;
+            }
+            const float base = m_ref == -INFINITY ? 0.f : m_ref;
+            float sum = 0.f;
+            uint32_t pk[kPreKeys / 2];
+#pragma unroll
+            for (int i = 0; i < kPreKeys / 2; ++i) {
+                pk[i] = H::pack(fast_exp2(x[2 * i] - base), fast_exp2(x[2 * i + 1] - base));
+                sum += pair_sum<T>(pk[i]);  // the rounded P the PV MMA uses: the weights sum to 1
+            }
+            l_sum = l_sum * a + sum;
+            // The PV of block j - 1 has read P and updated O before P and O change.
+            ok = j == 0 || mbar_wait(bar(kBarODone), (j - 1) & 1, deadline);
+            if (!__all_sync(0xffffffffu, ok)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, resc)) {  // TMEM access is warp-wide; a = 1 leaves a row as it is
+#pragma unroll
+                for (int c0 = 0; c0 < kFastHeadDim; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(trow + 2 * kPreKeys + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                    tmem_st32(trow + 2 * kPreKeys + c0, v);
+                }
+                tmem_wait_st();
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c)  // P row: keys 8c .. 8c + 7
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sP + (c >> 3) * kPreHalf + r * 128 +
+                                                                               (((c & 7) ^ (r & 7)) << 4)),
+                             "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                             : "memory");
+            {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
+                const int g = r >> 4, ch = (16 * g) / box_rows;
+                if ((r & 15) >= kv_keys[s * 8 + ch] - (16 * g - ch * box_rows)) {
+                    const uint32_t vrow = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + kPreTileBytes + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + (c >> 3) * kPreHalf +
+                                                                                       (c & 7) * 16),
+                                     "r"(0)
+                                     : "memory");
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(bar(kBarPFull));
         }
-        if (live1) {
-            T *dst = out + qrow1 * kFastHeadDim + d;
-            dst[0] = from_f32<T>(o[dt][2] * inv1);
-            dst[1] = from_f32<T>(o[dt][3] * inv1);
+        // Epilogue: O row / row sum once the last PV is done.
+        bool ok = !timed_out && mbar_wait(bar(kBarODone), (nblk - 1) & 1, deadline);
+        if (__all_sync(0xffffffffu, ok)) {
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            T *dst = out + qrow * kFastHeadDim;
+#pragma unroll
+            for (int c0 = 0; c0 < kFastHeadDim; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(trow + 2 * kPreKeys + c0, v);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = H::pack(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<uint4 *>(dst + c0 + 8 * i) =
+                            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+        } else {
+            timed_out = true;
         }
     }
+    // Common exit: copies landed (producer), MMAs completed (MMA warp), TMEM reads done.
+    if (timed_out && err_flag) atomicOr(err_flag, PKV_ERRBIT_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kPreSoftmaxWarps + 1) tmem_dealloc(tmem, kPreTmemCols);
 }
 
 template <typename K>
@@ -345,19 +430,22 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
                           const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
                           const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
                           int32_t num_blocks, float scale, int32_t *err, cudaStream_t stream) {
+    // chunk = gcd(block_size, 128): a power of two from 16 to 128 that divides the block
+    int box_rows = kPreKeys;
+    while (bs % box_rows) box_rows >>= 1;
     CUtensorMap mk, mv;
     const int64_t slots = static_cast<int64_t>(num_blocks) * bs;
-    pkv_status st = make_kv_map(&mk, k_cache, Half16<T>::kTmaType, slots, Hkv, 1);
+    pkv_status st = make_kv_map_box(&mk, k_cache, Half16<T>::kTmaType, slots, Hkv, box_rows, 1);
     if (st != PKV_OK) return st;
-    st = make_kv_map(&mv, v_cache, Half16<T>::kTmaType, slots, Hkv, 1);
+    st = make_kv_map_box(&mv, v_cache, Half16<T>::kTmaType, slots, Hkv, box_rows, 1);
     if (st != PKV_OK) return st;
     cudaError_t e = ensure_smem_once(prefill_kernel<T>, PreSmem::kAlloc);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
     const int G = Hq / Hkv, positions = kPreRows / G;
     const int tiles = (max_q_len + positions - 1) / positions;
-    e = launch_pdl(kPdlDecode, prefill_kernel<T>, dim3(B, Hkv, tiles), dim3((kPreWarps + 1) * 32), PreSmem::kAlloc,
-                   stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q), block_tables, max_blocks, starts,
-                   cu_q, Hq, G, bs, num_blocks, scale * kPreLog2e, err);
+    e = launch_pdl(kPdlDecode, prefill_kernel<T>, dim3(B, Hkv, tiles), dim3(kPreThreads), PreSmem::kAlloc, stream,
+                   mk, mv, static_cast<T *>(out), static_cast<const T *>(q), block_tables, max_blocks, starts, cu_q,
+                   Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
@@ -392,8 +480,8 @@ extern "C" pkv_status pkv_paged_attention_prefill(void *out, const void *q, cons
                                               "block_size a multiple of 16");
     if (!out || !q || !starts || !cu_q || !block_tables || !k_cache || !v_cache || num_blocks == 0)
         return set_error(PKV_ERR_INVALID_ARG, "prefill: NULL pointer or empty pool");
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4))
-        return set_error(PKV_ERR_UNSUPPORTED, "prefill: pools must be 16-byte and q/out 4-byte aligned");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return set_error(PKV_ERR_UNSUPPORTED, "prefill: pools, q and out must be 16-byte aligned");
     const int positions = kPreRows / G;
     if ((max_q_len + positions - 1) / positions > 65535)
         return set_error(PKV_ERR_UNSUPPORTED, "prefill: max_q_len too large for one launch");

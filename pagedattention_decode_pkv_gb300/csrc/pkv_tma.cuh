@@ -216,20 +216,27 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Pool [num_slots, Hkv, 128] viewed as (64 elements, num_slots, 2*Hkv half-rows).
-pkv_status make_kv_map(CUtensorMap *map, const void *pool, CUtensorMapDataType type, int64_t num_slots,
-                       int Hkv, int hpc) {
+// Pool [num_slots, Hkv, 128] viewed as (64 elements, num_slots, 2*Hkv half-rows);
+// a box is box_rows slots of box_halves consecutive half-rows.
+pkv_status make_kv_map_box(CUtensorMap *map, const void *pool, CUtensorMapDataType type, int64_t num_slots,
+                           int Hkv, int box_rows, int box_halves) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled entry point unavailable");
+    if (!fn) return set_error(PKV_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_slots), static_cast<cuuint64_t>(2 * Hkv)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Hkv) * kFastHeadDim * 2, 128};
-    const cuuint32_t box[3] = {64, kStageTokens, static_cast<cuuint32_t>(2 * hpc)};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_halves)};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, type, 3, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    if (r != CUDA_SUCCESS) return set_error(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return PKV_OK;
+}
+
+// The decode boxes: kStageTokens slots of hpc heads (both halves of each).
+pkv_status make_kv_map(CUtensorMap *map, const void *pool, CUtensorMapDataType type, int64_t num_slots,
+                       int Hkv, int hpc) {
+    return make_kv_map_box(map, pool, type, num_slots, Hkv, kStageTokens, 2 * hpc);
 }
 
 }  // namespace

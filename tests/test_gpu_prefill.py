@@ -30,12 +30,14 @@ def _case(dtype, Hq, Hkv, bs, spans, seed, cuda_dev, q_gain=1.0):
     return batch, q, starts, cu.to(cuda_dev), max(ns)
 
 
-SPANS = [(0, 100), (37, 64), (512, 16), (5, 1), (0, 1), (1000, 200), (16, 48)]
+# (start, new tokens): short and long spans, spans that end on and across
+# 128-key block boundaries, and one-token spans
+SPANS = [(0, 100), (37, 64), (512, 16), (5, 1), (0, 1), (1000, 200), (16, 48), (127, 130), (128, 128), (0, 257)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (4, 1)])
-@pytest.mark.parametrize("bs", [16, 256])
+@pytest.mark.parametrize("bs", [16, 64, 256])
 def test_prefill_matches_oracle(pkv, orc, cuda_dev, dtype, Hq, Hkv, bs):
     batch, q, starts, cu, mq = _case(dtype, Hq, Hkv, bs, SPANS, seed=Hq + Hkv + bs, cuda_dev=cuda_dev)
     err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
