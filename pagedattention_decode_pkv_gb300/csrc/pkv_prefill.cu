@@ -20,11 +20,15 @@
 //   * an MMA warp issues S_j = Q K_j^T (M = 128 rows, N = 128 keys, eight
 //     K = 16 steps over the head dimension) into one of two TMEM buffers, and,
 //     one block behind, O += P_{j-1} V_{j-1} (N = 128 dims, eight K = 16 steps
-//     over the keys; V is the MN-major B operand) into a TMEM accumulator;
+//     over the keys; P is the A operand straight from TMEM, V the MN-major B
+//     operand) into a TMEM accumulator;
 //   * four softmax warps, one query row per thread, read the row of S_j from
 //     TMEM, mask it (causal, keys of missing pages), keep the row's running
 //     maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m) as
-//     16-bit values into a shared-memory tile (K-major A operand of the PV MMA).
+//     16-bit pairs into one of two TMEM buffers.  With S and P both
+//     double-buffered, the softmax of block j waits only for the PV of block
+//     j - 2 (its P buffer), and for the PV of block j - 1 only when it has to
+//     rescale O.
 // The reference maximum m of a row moves only when the block's maximum exceeds
 // it by more than 2^8 (log2 units), and then O's row is rescaled in TMEM;
 // otherwise P is computed against the older m (values up to 256), which keeps
@@ -32,8 +36,10 @@
 // values the PV MMA multiplies, so the weights of the V rows sum to one (a
 // single dominant key gives its V row exactly, wherever m stands).  The last
 // PV's accumulator, divided by the row sum, is the output row.
-// Grid (B, H_kv, query tiles) with the tile index counted from the end of each
-// sequence, so the longest tiles (most keys) launch first.  Every wait is
+// Grid (query tiles, H_kv, B), tiles fastest: the tiles of one (sequence, KV
+// head) run side by side and read its pages while they are in L2, and the tile
+// index counts from the end of the sequence, so the longest tiles (most keys)
+// launch first.  Every wait is
 // bounded (PKV_ERRBIT_TIMEOUT), and the CTA waits for its own copies and MMAs
 // before it frees TMEM and exits.
 #include <cuda.h>
@@ -54,12 +60,13 @@ namespace {
 
 constexpr int kPreRows = 128;        // query rows (position x head) per CTA = TMEM lanes = MMA M
 constexpr int kPreKeys = 128;        // keys per block = the S MMA's N
-constexpr int kPreStages = 2;        // K/V ring depth (blocks)
+constexpr int kPreStages = 3;        // K/V ring depth (blocks)
 constexpr int kPreSoftmaxWarps = 4;  // one query row per thread
 constexpr int kPreThreads = (kPreSoftmaxWarps + 2) * 32;  // + producer warp + MMA warp
 constexpr int kPreHalf = kPreKeys * 128;                   // one 64-dim half of a [128 rows][128 dims] tile
 constexpr int kPreTileBytes = 2 * kPreHalf;                // 32 KB
-constexpr uint32_t kPreTmemCols = 512;                      // S0, S1, O (128 columns each), rounded up
+constexpr uint32_t kPreTmemCols = 512;  // S0, S1, O (128 columns each), P0, P1 (64 columns each)
+constexpr uint32_t kTmemO = 2 * 128, kTmemP = 3 * 128;  // column offsets (S_b at 128 b, P_b at kTmemP + 64 b)
 constexpr uint64_t kPreDeadlineNs = 2000000000ull;
 constexpr float kPreLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8 between rescales
@@ -77,8 +84,7 @@ template <> __device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
 
 struct PreSmem {
     static constexpr int kQ = 0;                                         // [2 halves][128 rows][128 B]
-    static constexpr int kP = kQ + kPreTileBytes;                        // same layout
-    static constexpr int kKV = kP + kPreTileBytes;                       // stage s: K at +64 KB s, V at +32 KB
+    static constexpr int kKV = kQ + kPreTileBytes;                       // stage s: K at +64 KB s, V at +32 KB
     static constexpr int kKeys = kKV + kPreStages * 2 * kPreTileBytes;   // int32 [stage][8 chunks] valid keys
     static constexpr int kBar = kKeys + 128;                             // mbarriers, 8 bytes each
     static constexpr int kTmemSlot = kBar + 128;
@@ -86,16 +92,17 @@ struct PreSmem {
     static constexpr int kAlloc = kBytes + 1024;
 };
 // mbarrier indices
-constexpr int kBarKvFull = 0;   // [2] producer: expect_tx + the copies' bytes
-constexpr int kBarKvEmpty = 2;  // [2] MMA commit after the block's PV
-constexpr int kBarSFull = 4;    // [2] MMA commit after S = Q K^T
-constexpr int kBarSFree = 6;    // [2] 128 softmax threads have read S
-constexpr int kBarPFull = 8;    // 128 softmax threads wrote P (and rescaled O)
-constexpr int kBarODone = 9;    // MMA commit after O += P V
-constexpr int kBarQFull = 10;   // 128 softmax threads wrote Q
-constexpr int kBarFinal = 11;   // MMA commit: every MMA of the CTA has completed
-constexpr int kNumBars = 12;
+constexpr int kBarKvFull = 0;                          // [kPreStages] producer: expect_tx + the copies' bytes
+constexpr int kBarKvEmpty = kBarKvFull + kPreStages;   // [kPreStages] MMA commit after the block's PV
+constexpr int kBarSFull = kBarKvEmpty + kPreStages;    // [2] MMA commit after S = Q K^T
+constexpr int kBarSFree = kBarSFull + 2;               // [2] 128 softmax threads have read S
+constexpr int kBarPFull = kBarSFree + 2;               // [2] by block parity: softmax threads wrote P (rescaled O)
+constexpr int kBarODone = kBarPFull + 2;               // [2] by block parity: MMA commit after O += P V
+constexpr int kBarQFull = kBarODone + 2;               // 128 softmax threads wrote Q
+constexpr int kBarFinal = kBarQFull + 1;               // MMA commit: every MMA of the CTA has completed
+constexpr int kNumBars = kBarFinal + 1;
 static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
+static_assert(kPreStages * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
 
 template <typename T>
 __global__ void __launch_bounds__(kPreThreads, 1)
@@ -107,23 +114,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     using L = PreSmem;
     using H = Half16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    const int b = blockIdx.x, kh = blockIdx.y;
+    const int b = blockIdx.z, kh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t *kv_keys = reinterpret_cast<int32_t *>(smem + L::kKeys);
     const uint32_t bar0 = smem_u32(smem + L::kBar);
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-    const uint32_t sQ = smem_u32(smem + L::kQ), sP = smem_u32(smem + L::kP), sKV = smem_u32(smem + L::kKV);
+    const uint32_t sQ = smem_u32(smem + L::kQ), sKV = smem_u32(smem + L::kKV);
     if (warp == kPreSoftmaxWarps && lane == 0) {
-        for (int s = 0; s < kPreStages; ++s) {
+        for (int s = 0; s < kPreStages; ++s) {  // per K/V stage
             mbar_init(bar(kBarKvFull + s), 1);
             mbar_init(bar(kBarKvEmpty + s), 1);
-            mbar_init(bar(kBarSFull + s), 1);
-            mbar_init(bar(kBarSFree + s), kPreRows);
         }
-        mbar_init(bar(kBarPFull), kPreRows);
-        mbar_init(bar(kBarODone), 1);
+        for (int p = 0; p < 2; ++p) {  // per S / P buffer (block parity)
+            mbar_init(bar(kBarSFull + p), 1);
+            mbar_init(bar(kBarSFree + p), kPreRows);
+            mbar_init(bar(kBarPFull + p), kPreRows);
+            mbar_init(bar(kBarODone + p), 1);
+        }
         mbar_init(bar(kBarQFull), kPreRows);
         mbar_init(bar(kBarFinal), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -135,8 +144,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int q_begin = cu_q[b], n = cu_q[b + 1] - q_begin, start = starts[b];
     const int positions = kPreRows / G;                       // query positions per tile
     const int tiles_b = n > 0 ? (n + positions - 1) / positions : 0;
-    const int tile = tiles_b - 1 - static_cast<int>(blockIdx.z);  // the last tiles (most keys) launch first
-    if ((n < 0 || tiles_b > static_cast<int>(gridDim.z)) && blockIdx.z == 0 && kh == 0 && threadIdx.x == 0 &&
+    const int tile = tiles_b - 1 - static_cast<int>(blockIdx.x);  // the last tiles (most keys) launch first
+    if ((n < 0 || tiles_b > static_cast<int>(gridDim.x)) && blockIdx.x == 0 && kh == 0 && threadIdx.x == 0 &&
         err_flag)  // cu_q decreasing, or more new tokens than max_q_len: rows left unwritten
         atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
     if (tile < 0) return;
@@ -243,17 +252,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 }
                 if (j >= 1) {
                     const int pj = j - 1, s = pj % kPreStages;
-                    ok = mbar_wait(bar(kBarPFull), pj & 1, deadline);
+                    ok = mbar_wait(bar(kBarPFull + (pj & 1)), (pj >> 1) & 1, deadline);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vt = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + kPreTileBytes;
 #pragma unroll
-                    for (int k = 0; k < kPreKeys / 16; ++k) {  // 16 keys (two 8-row groups) per step
-                        const uint32_t aoff = (k >> 2) * kPreHalf + (k & 3) * 32;
-                        umma_f16(tmem + 2 * kPreKeys, umma_desc_sw128(sP + aoff, 16, 1024),
-                                 umma_desc_sw128(vt + k * 2048, kPreHalf, 1024), kIdescO, (pj > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(bar(kBarODone));
+                    for (int k = 0; k < kPreKeys / 16; ++k)  // 16 keys per step: 8 P columns, two 8-row V groups
+                        umma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + 64 * (pj & 1) + 8 * k,
+                                        umma_desc_sw128(vt + k * 2048, kPreHalf, 1024), kIdescO,
+                                        (pj > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(bar(kBarODone + (pj & 1)));
                     umma_commit(bar(kBarKvEmpty + s));
                 }
             }
@@ -340,30 +348,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 sum += pair_sum<T>(pk[i]);  // the rounded P the PV MMA uses: the weights sum to 1
             }
             l_sum = l_sum * a + sum;
-            // The PV of block j - 1 has read P and updated O before P and O change.
-            ok = j == 0 || mbar_wait(bar(kBarODone), (j - 1) & 1, deadline);
+            // P buffer j & 1 was last read by the PV of block j - 2.
+            ok = j < 2 || mbar_wait(bar(kBarODone + (j & 1)), ((j - 2) >> 1) & 1, deadline);
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+            if (any_resc)  // O changes only after the PV of block j - 1 has added to it
+                ok = ok && (j == 0 || mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, deadline));
             if (!__all_sync(0xffffffffu, ok)) {
                 timed_out = true;
                 break;
             }
             tc_fence_after();
-            if (__any_sync(0xffffffffu, resc)) {  // TMEM access is warp-wide; a = 1 leaves a row as it is
+            if (any_resc) {  // TMEM access is warp-wide; a = 1 leaves a row as it is
 #pragma unroll
                 for (int c0 = 0; c0 < kFastHeadDim; c0 += 32) {
                     uint32_t v[32];
-                    tmem_ld32(trow + 2 * kPreKeys + c0, v);
+                    tmem_ld32(trow + kTmemO + c0, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-                    tmem_st32(trow + 2 * kPreKeys + c0, v);
+                    tmem_st32(trow + kTmemO + c0, v);
                 }
-                tmem_wait_st();
             }
 #pragma unroll
-            for (int c = 0; c < 16; ++c)  // P row: keys 8c .. 8c + 7
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sP + (c >> 3) * kPreHalf + r * 128 +
-                                                                               (((c & 7) ^ (r & 7)) << 4)),
-                             "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                             : "memory");
+            for (int c0 = 0; c0 < kPreKeys / 2; c0 += 32) {  // P row: column c holds keys 2c, 2c + 1
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = pk[c0 + i];
+                tmem_st32(trow + kTmemP + 64 * (j & 1) + c0, v);
+            }
+            tmem_wait_st();
             {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
                 const int g = r >> 4, ch = (16 * g) / box_rows;
                 if ((r & 15) >= kv_keys[s * 8 + ch] - (16 * g - ch * box_rows)) {
@@ -376,12 +388,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                                      : "memory");
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows
             tc_fence_before();
-            mbar_arrive(bar(kBarPFull));
+            mbar_arrive(bar(kBarPFull + (j & 1)));
         }
         // Epilogue: O row / row sum once the last PV is done.
-        bool ok = !timed_out && mbar_wait(bar(kBarODone), (nblk - 1) & 1, deadline);
+        bool ok = !timed_out && mbar_wait(bar(kBarODone + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1, deadline);
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -389,7 +401,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int c0 = 0; c0 < kFastHeadDim; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld32(trow + 2 * kPreKeys + c0, v);
+                tmem_ld32(trow + kTmemO + c0, v);
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -443,7 +455,7 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
     const int G = Hq / Hkv, positions = kPreRows / G;
     const int tiles = (max_q_len + positions - 1) / positions;
-    e = launch_pdl(kPdlDecode, prefill_kernel<T>, dim3(B, Hkv, tiles), dim3(kPreThreads), PreSmem::kAlloc, stream,
+    e = launch_pdl(kPdlDecode, prefill_kernel<T>, dim3(tiles, Hkv, B), dim3(kPreThreads), PreSmem::kAlloc, stream,
                    mk, mv, static_cast<T *>(out), static_cast<const T *>(q), block_tables, max_blocks, starts, cu_q,
                    Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -482,9 +494,6 @@ extern "C" pkv_status pkv_paged_attention_prefill(void *out, const void *q, cons
         return set_error(PKV_ERR_INVALID_ARG, "prefill: NULL pointer or empty pool");
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
         return set_error(PKV_ERR_UNSUPPORTED, "prefill: pools, q and out must be 16-byte aligned");
-    const int positions = kPreRows / G;
-    if ((max_q_len + positions - 1) / positions > 65535)
-        return set_error(PKV_ERR_UNSUPPORTED, "prefill: max_q_len too large for one launch");
     auto s = static_cast<cudaStream_t>(stream);
     pkv_status st = dtype == PKV_BF16
                         ? launch_prefill<__nv_bfloat16>(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,

@@ -52,6 +52,16 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A's rows in TMEM lanes, two 16-bit K-elements
+// per 32-bit column (the even one in the low half), K / 2 columns.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // The mbarrier at `bar` receives one arrival when every tcgen05 operation the
 // calling thread issued before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
