@@ -154,3 +154,25 @@ def test_binding_refuses_cpu_tensors(pkv):
         pkv.pkv_paged_attention_decode(t, torch.zeros(1, 4, 2, 4), torch.zeros(1, 4, 2, 4),
                                        torch.zeros(2, 1, dtype=torch.int32), torch.ones(2, dtype=torch.int32),
                                        1.0, 4)
+
+
+def test_prefill_argument_errors_are_synchronous(pkv):
+    """The prefill entry rejects bad shapes and alignments before any CUDA call
+    (the pointers below are never dereferenced)."""
+    lib = pkv._lib
+    P = ctypes.c_void_p
+    good, odd = P(0x10000), P(0x10008)  # 16-byte aligned / only 8-byte aligned
+
+    def call(out=good, q=good, Hq=32, Hkv=8, d=128, bs=16, dtype=pkv.PKV_BF16):
+        return lib.pkv_paged_attention_prefill(out, q, good, good, good, 4, good, good, 2, 64, Hq, Hkv, d, bs,
+                                               100, 0.1, dtype, None, None)
+
+    assert call(Hq=30) == pkv.PKV_ERR_INVALID_ARG and b"multiple" in lib.pkv_last_error_string()
+    assert call(d=64) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(bs=24) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(Hq=128) == pkv.PKV_ERR_UNSUPPORTED  # G = 16
+    assert call(dtype=pkv.PKV_F32) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(q=odd) == pkv.PKV_ERR_UNSUPPORTED and b"aligned" in lib.pkv_last_error_string()
+    assert call(out=odd) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_paged_attention_prefill(None, None, None, None, None, 4, None, None, 0, 64, 32, 8, 128, 16, 100,
+                                           0.1, pkv.PKV_BF16, None, None) == pkv.PKV_OK  # empty batch
