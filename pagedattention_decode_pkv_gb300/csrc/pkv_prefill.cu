@@ -13,22 +13,23 @@
 // Design (fifth-generation tensor cores, FlashAttention style).  A CTA owns
 // 128 query rows of one KV head: 128 / G positions x the G query heads of the
 // group, so every K/V byte it stages serves all G heads.  Keys go by blocks of
-// 128.  Per block j:
+// KEYS (128, or 64 with two CTAs per SM; see launch_prefill_any).  Per block j:
 //   * a producer warp copies K_j and V_j (the head's rows of the pages that
-//     hold keys 128j .. 128j + 127) into a two-stage ring with TMA, in chunks of
-//     gcd(block_size, 128) tokens per 64-dim half, 128-byte swizzled;
-//   * an MMA warp issues S_j = Q K_j^T (M = 128 rows, N = 128 keys, eight
-//     K = 16 steps over the head dimension) into one of two TMEM buffers, and,
-//     one block behind, O += P_{j-1} V_{j-1} (N = 128 dims, eight K = 16 steps
-//     over the keys; P is the A operand straight from TMEM, V the MN-major B
-//     operand) into a TMEM accumulator;
+//     hold keys KEYS j .. KEYS j + KEYS - 1) into a ring of stages with TMA, in
+//     chunks of gcd(block_size, KEYS) tokens per 64-dim half, 128-byte
+//     swizzled;
+//   * an MMA warp issues S_j = Q K_j^T (M = 128 rows, N = KEYS, eight K = 16
+//     steps over the head dimension) into one of two TMEM buffers, and, one
+//     block behind, O += P_{j-1} V_{j-1} (N = 128 dims, K = 16 steps over the
+//     keys; P is the A operand straight from TMEM, V the MN-major B operand)
+//     into a TMEM accumulator;
 //   * four softmax warps, one query row per thread, read the row of S_j from
 //     TMEM, mask it (causal, keys of missing pages), keep the row's running
 //     maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m) as
-//     16-bit pairs into one of two TMEM buffers.  With S and P both
-//     double-buffered, the softmax of block j waits only for the PV of block
-//     j - 2 (its P buffer), and for the PV of block j - 1 only when it has to
-//     rescale O.
+//     16-bit pairs over the S_j they read.  The MMA warp writes S_{j+2} into
+//     that buffer once the PV of block j has read P_j, so the softmax never
+//     waits for a P buffer, and waits for the PV of block j - 1 only when it
+//     has to rescale O.
 // The reference maximum m of a row moves only when the block's maximum exceeds
 // it by more than 2^8 (log2 units), and then O's row is rescaled in TMEM;
 // otherwise P is computed against the older m (values up to 256), which keeps
@@ -39,9 +40,8 @@
 // Grid (query tiles, H_kv, B), tiles fastest: the tiles of one (sequence, KV
 // head) run side by side and read its pages while they are in L2, and the tile
 // index counts from the end of the sequence, so the longest tiles (most keys)
-// launch first.  Every wait is
-// bounded (PKV_ERRBIT_TIMEOUT), and the CTA waits for its own copies and MMAs
-// before it frees TMEM and exits.
+// launch first.  Every wait is bounded (PKV_ERRBIT_TIMEOUT), and the CTA waits
+// for its own copies and MMAs before it frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,14 +59,10 @@ namespace pkv {
 namespace {
 
 constexpr int kPreRows = 128;        // query rows (position x head) per CTA = TMEM lanes = MMA M
-constexpr int kPreKeys = 128;        // keys per block = the S MMA's N
-constexpr int kPreStages = 3;        // K/V ring depth (blocks)
 constexpr int kPreSoftmaxWarps = 4;  // one query row per thread
 constexpr int kPreThreads = (kPreSoftmaxWarps + 2) * 32;  // + producer warp + MMA warp
-constexpr int kPreHalf = kPreKeys * 128;                   // one 64-dim half of a [128 rows][128 dims] tile
-constexpr int kPreTileBytes = 2 * kPreHalf;                // 32 KB
-constexpr uint32_t kPreTmemCols = 512;  // S0, S1, O (128 columns each), P0, P1 (64 columns each)
-constexpr uint32_t kTmemO = 2 * 128, kTmemP = 3 * 128;  // column offsets (S_b at 128 b, P_b at kTmemP + 64 b)
+constexpr int kQHalf = kPreRows * 128;         // one 64-dim half of the Q tile [128 rows][128 dims]
+constexpr int kQTileBytes = 2 * kQHalf;        // 32 KB
 constexpr uint64_t kPreDeadlineNs = 2000000000ull;
 constexpr float kPreLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8 between rescales
@@ -82,43 +78,65 @@ template <> __device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
     return __low2float(h) + __high2float(h);
 }
 
-struct PreSmem {
-    static constexpr int kQ = 0;                                         // [2 halves][128 rows][128 B]
-    static constexpr int kKV = kQ + kPreTileBytes;                       // stage s: K at +64 KB s, V at +32 KB
-    static constexpr int kKeys = kKV + kPreStages * 2 * kPreTileBytes;   // int32 [stage][8 chunks] valid keys
-    static constexpr int kBar = kKeys + 128;                             // mbarriers, 8 bytes each
+// Per block size (KEYS keys per block, the S MMA's N) and ring depth: the K/V
+// tiles, the shared-memory layout, TMEM columns and mbarrier indices.
+//   KEYS = 128, 3 stages: 230 KB of shared memory, one CTA per SM.
+//   KEYS = 64, 2 stages: 97 KB, two CTAs per SM (eight softmax warps).
+// TMEM: buffers 0 and 1 at columns KEYS b hold S_j (KEYS columns) and then
+// P_j (KEYS / 2 columns of 16-bit pairs, written over the S it came from); O
+// at 2 KEYS.
+template <int KEYS, int STAGES>
+struct PreCfg {
+    static constexpr int kKvHalf = KEYS * 128;        // one 64-dim half of a K or V tile [KEYS][128 dims]
+    static constexpr int kKvTileBytes = 2 * kKvHalf;
+    static constexpr int kStageBytes = 2 * kKvTileBytes;  // K then V
+    static constexpr uint32_t kTmemO = 2 * KEYS;
+    static constexpr uint32_t kTmemCols = KEYS == 64 ? 256 : 512;  // the power of two >= 2 KEYS + 128
+    static constexpr int kMinBlocks = KEYS == 64 ? 2 : 1;         // CTAs per SM
+    // shared memory
+    static constexpr int kQ = 0;                                   // [2 halves][128 rows][128 B]
+    static constexpr int kKV = kQ + kQTileBytes;                   // stage s: K [2][KEYS][128 B], then V
+    static constexpr int kKeysOff = kKV + STAGES * kStageBytes;   // int32 [stage][8 chunks] valid keys
+    static constexpr int kBar = kKeysOff + 128;                    // mbarriers, 8 bytes each
     static constexpr int kTmemSlot = kBar + 128;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
+    // mbarrier indices
+    static constexpr int kBarKvFull = 0;                      // [STAGES] producer: expect_tx + the copies' bytes
+    static constexpr int kBarKvEmpty = kBarKvFull + STAGES;   // [STAGES] MMA commit after the block's PV
+    static constexpr int kBarSFull = kBarKvEmpty + STAGES;    // [2] MMA commit after S = Q K^T
+    static constexpr int kBarPFull = kBarSFull + 2;           // [2] by block parity: softmax wrote P (rescaled O)
+    static constexpr int kBarODone = kBarPFull + 2;           // [2] by block parity: MMA commit after O += P V
+    static constexpr int kBarQFull = kBarODone + 2;           // 128 softmax threads wrote Q
+    static constexpr int kBarFinal = kBarQFull + 1;           // MMA commit: every MMA of the CTA has completed
+    static constexpr int kNumBars = kBarFinal + 1;
+    static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
+    static_assert(STAGES * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
+    static_assert(2 * KEYS + 128 <= static_cast<int>(kTmemCols), "S0, S1 and O fit the TMEM allocation");
+    static_assert(kAlloc * kMinBlocks <= 227 * 1024 - 1024 * (kMinBlocks - 1), "shared memory per SM");
 };
-// mbarrier indices
-constexpr int kBarKvFull = 0;                          // [kPreStages] producer: expect_tx + the copies' bytes
-constexpr int kBarKvEmpty = kBarKvFull + kPreStages;   // [kPreStages] MMA commit after the block's PV
-constexpr int kBarSFull = kBarKvEmpty + kPreStages;    // [2] MMA commit after S = Q K^T
-constexpr int kBarSFree = kBarSFull + 2;               // [2] 128 softmax threads have read S
-constexpr int kBarPFull = kBarSFree + 2;               // [2] by block parity: softmax threads wrote P (rescaled O)
-constexpr int kBarODone = kBarPFull + 2;               // [2] by block parity: MMA commit after O += P V
-constexpr int kBarQFull = kBarODone + 2;               // 128 softmax threads wrote Q
-constexpr int kBarFinal = kBarQFull + 1;               // MMA commit: every MMA of the CTA has completed
-constexpr int kNumBars = kBarFinal + 1;
-static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
-static_assert(kPreStages * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
 
-template <typename T>
-__global__ void __launch_bounds__(kPreThreads, 1)
+template <typename T, int KEYS, int STAGES>
+__global__ void __launch_bounds__(kPreThreads, (KEYS == 64 ? 2 : 1))
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                int32_t max_blocks, const int32_t *__restrict__ starts, const int32_t *__restrict__ cu_q,
                int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, int32_t box_rows, float scale_log2,
                int32_t *__restrict__ err_flag) {
-    using L = PreSmem;
+    using L = PreCfg<KEYS, STAGES>;
+    constexpr int kPreKeys = KEYS, kPreStages = STAGES;
+    constexpr int kKvHalf = L::kKvHalf, kKvTileBytes = L::kKvTileBytes, kStageBytes = L::kStageBytes;
+    constexpr uint32_t kTmemO = L::kTmemO, kPreTmemCols = L::kTmemCols;
+    constexpr int kBarKvFull = L::kBarKvFull, kBarKvEmpty = L::kBarKvEmpty, kBarSFull = L::kBarSFull;
+    constexpr int kBarPFull = L::kBarPFull, kBarODone = L::kBarODone, kBarQFull = L::kBarQFull;
+    constexpr int kBarFinal = L::kBarFinal;
     using H = Half16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     const int b = blockIdx.z, kh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    int32_t *kv_keys = reinterpret_cast<int32_t *>(smem + L::kKeys);
+    int32_t *kv_keys = reinterpret_cast<int32_t *>(smem + L::kKeysOff);
     const uint32_t bar0 = smem_u32(smem + L::kBar);
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     const uint32_t sQ = smem_u32(smem + L::kQ), sKV = smem_u32(smem + L::kKV);
@@ -129,7 +147,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         for (int p = 0; p < 2; ++p) {  // per S / P buffer (block parity)
             mbar_init(bar(kBarSFull + p), 1);
-            mbar_init(bar(kBarSFree + p), kPreRows);
             mbar_init(bar(kBarPFull + p), kPreRows);
             mbar_init(bar(kBarODone + p), 1);
         }
@@ -210,11 +227,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             __syncwarp();
             if (keys > 0) {
                 const int slot_row = id * bs + key0 % bs;
-                const uint32_t kdst = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + lane * chunk_bytes;
+                const uint32_t kdst = sKV + static_cast<uint32_t>(s) * kStageBytes + lane * chunk_bytes;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    tma_load_3d(kdst + h * kPreHalf, &tm_k, 0, slot_row, 2 * kh + h, full);
-                    tma_load_3d(kdst + kPreTileBytes + h * kPreHalf, &tm_v, 0, slot_row, 2 * kh + h, full);
+                    tma_load_3d(kdst + h * kKvHalf, &tm_k, 0, slot_row, 2 * kh + h, full);
+                    tma_load_3d(kdst + kKvTileBytes + h * kKvHalf, &tm_v, 0, slot_row, 2 * kh + h, full);
                 }
             }
             issued = j + 1;
@@ -238,15 +255,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 if (j < nblk) {
                     const int s = j % kPreStages;
                     ok = mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
-                    if (ok && j >= 2) ok = mbar_wait(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, deadline);
+                    // buffer j & 1 holds P_{j-2} until the PV of block j - 2 has read it
+                    if (ok && j >= 2) ok = mbar_wait(bar(kBarODone + (j & 1)), ((j - 2) >> 1) & 1, deadline);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kt = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes;
+                    const uint32_t kt = sKV + static_cast<uint32_t>(s) * kStageBytes;
 #pragma unroll
                     for (int k = 0; k < kFastHeadDim / 16; ++k) {  // 16 dims (32 bytes) per step
-                        const uint32_t off = (k >> 2) * kPreHalf + (k & 3) * 32;
-                        umma_f16(tmem + (j & 1) * kPreKeys, umma_desc_sw128(sQ + off, 16, 1024),
-                                 umma_desc_sw128(kt + off, 16, 1024), kIdescS, k > 0);
+                        const uint32_t koff = (k & 3) * 32;
+                        umma_f16(tmem + (j & 1) * kPreKeys, umma_desc_sw128(sQ + (k >> 2) * kQHalf + koff, 16, 1024),
+                                 umma_desc_sw128(kt + (k >> 2) * kKvHalf + koff, 16, 1024), kIdescS, k > 0);
                     }
                     umma_commit(bar(kBarSFull + (j & 1)));
                 }
@@ -255,11 +273,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     ok = mbar_wait(bar(kBarPFull + (pj & 1)), (pj >> 1) & 1, deadline);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vt = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + kPreTileBytes;
+                    const uint32_t vt = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes;
 #pragma unroll
                     for (int k = 0; k < kPreKeys / 16; ++k)  // 16 keys per step: 8 P columns, two 8-row V groups
-                        umma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + 64 * (pj & 1) + 8 * k,
-                                        umma_desc_sw128(vt + k * 2048, kPreHalf, 1024), kIdescO,
+                        umma_f16_tmem_a(tmem + kTmemO, tmem + (pj & 1) * kPreKeys + 8 * k,
+                                        umma_desc_sw128(vt + k * 2048, kKvHalf, 1024), kIdescO,
                                         (pj > 0 || k > 0) ? 1u : 0u);
                     umma_commit(bar(kBarODone + (pj & 1)));
                     umma_commit(bar(kBarKvEmpty + s));
@@ -283,7 +301,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int4 v = live ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + (c >> 3) * kPreHalf + r * 128 +
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + (c >> 3) * kQHalf + r * 128 +
                                                                                (((c & 7) ^ (r & 7)) << 4)),
                              "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                              : "memory");
@@ -310,14 +328,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
             }
-            tc_fence_before();
-            mbar_arrive(bar(kBarSFree + (j & 1)));
             // Valid keys of each 16-key group: causal limit and the chunk's copied keys.
-            int lim[8];
+            int lim[kPreKeys / 16];
             {
                 const int causal = live ? pos - j * kPreKeys : -1;  // keys k <= causal are visible
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
+                for (int g = 0; g < kPreKeys / 16; ++g) {
                     const int ch = (16 * g) / box_rows, off = 16 * g - ch * box_rows;
                     const int copied = kv_keys[s * 8 + ch] - off;  // valid keys of the group, from its first
                     const int c = causal - 16 * g;
@@ -348,16 +364,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 sum += pair_sum<T>(pk[i]);  // the rounded P the PV MMA uses: the weights sum to 1
             }
             l_sum = l_sum * a + sum;
-            // P buffer j & 1 was last read by the PV of block j - 2.
-            ok = j < 2 || mbar_wait(bar(kBarODone + (j & 1)), ((j - 2) >> 1) & 1, deadline);
             const bool any_resc = __any_sync(0xffffffffu, resc);
-            if (any_resc)  // O changes only after the PV of block j - 1 has added to it
-                ok = ok && (j == 0 || mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, deadline));
-            if (!__all_sync(0xffffffffu, ok)) {
-                timed_out = true;
-                break;
+            if (any_resc) {  // O changes only after the PV of block j - 1 has added to it
+                ok = j == 0 || mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, deadline);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
             if (any_resc) {  // TMEM access is warp-wide; a = 1 leaves a row as it is
 #pragma unroll
                 for (int c0 = 0; c0 < kFastHeadDim; c0 += 32) {
@@ -368,21 +383,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     tmem_st32(trow + kTmemO + c0, v);
                 }
             }
+            // P row over the S it came from (this thread's own columns, read
+            // above): column c holds keys 2c, 2c + 1
 #pragma unroll
-            for (int c0 = 0; c0 < kPreKeys / 2; c0 += 32) {  // P row: column c holds keys 2c, 2c + 1
+            for (int c0 = 0; c0 < kPreKeys / 2; c0 += 32) {
                 uint32_t v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = pk[c0 + i];
-                tmem_st32(trow + kTmemP + 64 * (j & 1) + c0, v);
+                tmem_st32(trow + (j & 1) * kPreKeys + c0, v);
             }
             tmem_wait_st();
-            {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
+            if (r < kPreKeys) {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
                 const int g = r >> 4, ch = (16 * g) / box_rows;
                 if ((r & 15) >= kv_keys[s * 8 + ch] - (16 * g - ch * box_rows)) {
-                    const uint32_t vrow = sKV + static_cast<uint32_t>(s) * 2 * kPreTileBytes + kPreTileBytes + r * 128;
+                    const uint32_t vrow = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes + r * 128;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + (c >> 3) * kPreHalf +
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + (c >> 3) * kKvHalf +
                                                                                        (c & 7) * 16),
                                      "r"(0)
                                      : "memory");
@@ -425,25 +442,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (warp == kPreSoftmaxWarps + 1) tmem_dealloc(tmem, kPreTmemCols);
 }
 
-template <typename K>
-cudaError_t ensure_smem_once(K kernel, int bytes) {
+template <typename T, int KEYS, int STAGES>
+cudaError_t prefill_smem_once() {  // one flag per instantiation (they share a function type)
     static int done_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_dev == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(prefill_kernel<T, KEYS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PreCfg<KEYS, STAGES>::kAlloc);
     if (e == cudaSuccess) done_dev = dev;
     return e;
 }
 
-template <typename T>
+template <typename T, int KEYS, int STAGES>
 pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
                           const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
                           int32_t num_blocks, float scale, int32_t *err, cudaStream_t stream) {
-    // chunk = gcd(block_size, 128): a power of two from 16 to 128 that divides the block
-    int box_rows = kPreKeys;
+    // chunk = gcd(block_size, KEYS): a power of two from 16 to KEYS that divides the block
+    int box_rows = KEYS;
     while (bs % box_rows) box_rows >>= 1;
     CUtensorMap mk, mv;
     const int64_t slots = static_cast<int64_t>(num_blocks) * bs;
@@ -451,15 +469,39 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     if (st != PKV_OK) return st;
     st = make_kv_map_box(&mv, v_cache, Half16<T>::kTmaType, slots, Hkv, box_rows, 1);
     if (st != PKV_OK) return st;
-    cudaError_t e = ensure_smem_once(prefill_kernel<T>, PreSmem::kAlloc);
+    cudaError_t e = prefill_smem_once<T, KEYS, STAGES>();
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
     const int G = Hq / Hkv, positions = kPreRows / G;
     const int tiles = (max_q_len + positions - 1) / positions;
-    e = launch_pdl(kPdlDecode, prefill_kernel<T>, dim3(tiles, Hkv, B), dim3(kPreThreads), PreSmem::kAlloc, stream,
-                   mk, mv, static_cast<T *>(out), static_cast<const T *>(q), block_tables, max_blocks, starts, cu_q,
-                   Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
+    e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES>, dim3(tiles, Hkv, B), dim3(kPreThreads),
+                   PreCfg<KEYS, STAGES>::kAlloc, stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q),
+                   block_tables, max_blocks, starts, cu_q, Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PKV_OK;
+}
+
+// Configuration: 64-key blocks with two CTAs per SM keep eight softmax warps
+// per SM busy and win when the grid is many waves deep; 128-key blocks (three
+// stages, one CTA per SM) halve the per-block costs and the wave tail, and win
+// for contexts that can reach 16k tokens or grids under 16 waves of two-CTA
+// slots.  Measured on GB300 (TFLOP/s, 128 vs 64 keys): LLaMA-shaped layer
+// (8192 CTAs, contexts <= 4k) 425 vs 500, Qwen3-shaped (8192 CTAs, <= 8k) 515 vs
+// 593, 8 x 8192 (1024 CTAs) 524 vs 477, 8 x 32768 635 vs 497.
+constexpr int64_t kLongContextTokens = 16384;
+constexpr int64_t kManyCtas = 16 * 2 * 152;
+
+template <typename T>
+pkv_status launch_prefill_any(void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
+                              const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
+                              int32_t num_blocks, float scale, int32_t *err, cudaStream_t stream) {
+    const int positions = kPreRows / (Hq / Hkv);
+    const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((max_q_len + positions - 1) / positions);
+    if (static_cast<int64_t>(max_blocks) * bs >= kLongContextTokens || ctas < kManyCtas)
+        return launch_prefill<T, 128, 3>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B,
+                                         max_q_len, Hq, Hkv, bs, num_blocks, scale, err, stream);
+    return launch_prefill<T, 64, 2>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B, max_q_len,
+                                    Hq, Hkv, bs, num_blocks, scale, err, stream);
 }
 
 }  // namespace
@@ -496,10 +538,10 @@ extern "C" pkv_status pkv_paged_attention_prefill(void *out, const void *q, cons
         return set_error(PKV_ERR_UNSUPPORTED, "prefill: pools, q and out must be 16-byte aligned");
     auto s = static_cast<cudaStream_t>(stream);
     pkv_status st = dtype == PKV_BF16
-                        ? launch_prefill<__nv_bfloat16>(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                        ? launch_prefill_any<__nv_bfloat16>(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                                         starts, cu_q, num_seqs, max_q_len, num_q_heads, num_kv_heads,
                                                         block_size, num_blocks, scale, err_flag, s)
-                        : launch_prefill<__half>(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, starts,
+                        : launch_prefill_any<__half>(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, starts,
                                                  cu_q, num_seqs, max_q_len, num_q_heads, num_kv_heads, block_size,
                                                  num_blocks, scale, err_flag, s);
     if (st != PKV_OK) return st;
