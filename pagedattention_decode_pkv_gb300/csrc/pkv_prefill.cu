@@ -340,11 +340,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     lim[g] = min(c, min(copied, 16) - 1);      // keys 16g + i valid for i <= lim[g]
                 }
             }
-            float mx = -INFINITY;
+            bool open = true;  // every key of the block visible to this row
 #pragma unroll
-            for (int k = 0; k < kPreKeys; ++k) {
-                x[k] = (k & 15) <= lim[k >> 4] ? x[k] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[k]);
+            for (int g = 0; g < kPreKeys / 16; ++g) open = open && lim[g] >= 15;
+            float mx = -INFINITY;
+            if (__all_sync(0xffffffffu, open)) {  // blocks below the diagonal: no mask
+#pragma unroll
+                for (int k = 0; k < kPreKeys; ++k) {
+                    x[k] *= scale_log2;
+                    mx = fmaxf(mx, x[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPreKeys; ++k) {
+                    x[k] = (k & 15) <= lim[k >> 4] ? x[k] * scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[k]);
+                }
             }
             float a = 1.f;
             bool resc = false;
