@@ -116,7 +116,7 @@ struct PreCfg {
     static_assert(kAlloc * kMinBlocks <= 227 * 1024 - 1024 * (kMinBlocks - 1), "shared memory per SM");
 };
 
-template <typename T, int KEYS, int STAGES>
+template <typename T, int KEYS, int STAGES, bool POS>
 __global__ void __launch_bounds__(kPreThreads, (KEYS == 64 ? 2 : 1))
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
@@ -343,20 +343,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             bool open = true;  // every key of the block visible to this row
 #pragma unroll
             for (int g = 0; g < kPreKeys / 16; ++g) open = open && lim[g] >= 15;
+            // x = the scaled score (POS: the raw score, scaled inside the exponent
+            // below; a positive scale keeps the maximum where it is), -inf if masked
+            const float xs = POS ? 1.f : scale_log2;
             float mx = -INFINITY;
             if (__all_sync(0xffffffffu, open)) {  // blocks below the diagonal: no mask
 #pragma unroll
                 for (int k = 0; k < kPreKeys; ++k) {
-                    x[k] *= scale_log2;
+                    if (!POS) x[k] *= xs;
                     mx = fmaxf(mx, x[k]);
                 }
             } else {
 #pragma unroll
                 for (int k = 0; k < kPreKeys; ++k) {
-                    x[k] = (k & 15) <= lim[k >> 4] ? x[k] * scale_log2 : -INFINITY;
+                    x[k] = (k & 15) <= lim[k >> 4] ? x[k] * xs : -INFINITY;
                     mx = fmaxf(mx, x[k]);
                 }
             }
+            if (POS) mx *= scale_log2;
             float a = 1.f;
             bool resc = false;
             if (mx > m_ref + kRescaleThreshold) {  // also the row's first visible key (m_ref = -inf)
@@ -371,7 +375,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             uint32_t pk[kPreKeys / 2];
 #pragma unroll
             for (int i = 0; i < kPreKeys / 2; ++i) {
-                pk[i] = H::pack(fast_exp2(x[2 * i] - base), fast_exp2(x[2 * i + 1] - base));
+                const float e0 = POS ? fmaf(x[2 * i], scale_log2, -base) : x[2 * i] - base;
+                const float e1 = POS ? fmaf(x[2 * i + 1], scale_log2, -base) : x[2 * i + 1] - base;
+                pk[i] = H::pack(fast_exp2(e0), fast_exp2(e1));
                 sum += pair_sum<T>(pk[i]);  // the rounded P the PV MMA uses: the weights sum to 1
             }
             l_sum = l_sum * a + sum;
@@ -453,20 +459,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (warp == kPreSoftmaxWarps + 1) tmem_dealloc(tmem, kPreTmemCols);
 }
 
-template <typename T, int KEYS, int STAGES>
+template <typename T, int KEYS, int STAGES, bool POS>
 cudaError_t prefill_smem_once() {  // one flag per instantiation (they share a function type)
     static int done_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_dev == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(prefill_kernel<T, KEYS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel<T, KEYS, STAGES, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              PreCfg<KEYS, STAGES>::kAlloc);
     if (e == cudaSuccess) done_dev = dev;
     return e;
 }
 
-template <typename T, int KEYS, int STAGES>
+template <typename T, int KEYS, int STAGES, bool POS>
 pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
                           const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
@@ -480,11 +486,11 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     if (st != PKV_OK) return st;
     st = make_kv_map_box(&mv, v_cache, Half16<T>::kTmaType, slots, Hkv, box_rows, 1);
     if (st != PKV_OK) return st;
-    cudaError_t e = prefill_smem_once<T, KEYS, STAGES>();
+    cudaError_t e = prefill_smem_once<T, KEYS, STAGES, POS>();
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
     const int G = Hq / Hkv, positions = kPreRows / G;
     const int tiles = (max_q_len + positions - 1) / positions;
-    e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES>, dim3(tiles, Hkv, B), dim3(kPreThreads),
+    e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES, POS>, dim3(tiles, Hkv, B), dim3(kPreThreads),
                    PreCfg<KEYS, STAGES>::kAlloc, stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q),
                    block_tables, max_blocks, starts, cu_q, Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -508,11 +514,19 @@ pkv_status launch_prefill_any(void *out, const void *q, const void *k_cache, con
                               int32_t num_blocks, float scale, int32_t *err, cudaStream_t stream) {
     const int positions = kPreRows / (Hq / Hkv);
     const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((max_q_len + positions - 1) / positions);
-    if (static_cast<int64_t>(max_blocks) * bs >= kLongContextTokens || ctas < kManyCtas)
-        return launch_prefill<T, 128, 3>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B,
-                                         max_q_len, Hq, Hkv, bs, num_blocks, scale, err, stream);
-    return launch_prefill<T, 64, 2>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B, max_q_len,
-                                    Hq, Hkv, bs, num_blocks, scale, err, stream);
+    // A positive scale (the usual 1/sqrt(d)) moves into the exponent's argument.
+#define PKV_PREFILL_LAUNCH(KEYS, STAGES)                                                                            \
+    (scale > 0.f ? launch_prefill<T, KEYS, STAGES, true>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, \
+                                                         cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, scale, err,    \
+                                                         stream)                                                     \
+                 : launch_prefill<T, KEYS, STAGES, false>(out, q, k_cache, v_cache, block_tables, max_blocks, starts,\
+                                                          cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, scale, err,   \
+                                                          stream))
+    const pkv_status st = static_cast<int64_t>(max_blocks) * bs >= kLongContextTokens || ctas < kManyCtas
+                              ? PKV_PREFILL_LAUNCH(128, 3)
+                              : PKV_PREFILL_LAUNCH(64, 2);
+#undef PKV_PREFILL_LAUNCH
+    return st;
 }
 
 }  // namespace

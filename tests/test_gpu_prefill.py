@@ -159,3 +159,18 @@ def test_prefill_large_sampled_rows(pkv, orc, cuda_dev):
                                             batch.block_tables.cpu()[seqs], st, c1, batch.scale)
     assert nerr == 0
     assert _max_err(out[torch.tensor(rows, device=cuda_dev)], ref) <= ATOL_16
+
+
+@pytest.mark.parametrize("mode", ["narrow", "deep"])
+def test_prefill_negative_scale(pkv, orc, cuda_dev, mode):
+    """A non-positive scale takes the kernel variant that scales each score
+    before the maximum (a positive scale is folded into the exponent)."""
+    spans = [(0, 100), (300, 70), (17, 1)]
+    batch, q, starts, cu, mq = _case(torch.bfloat16, 16, 8, 16, spans, seed=74, cuda_dev=cuda_dev)
+    scale = -0.7 * batch.scale
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    out = pkv.pkv_paged_attention_prefill(q, batch.k_cache, batch.v_cache, batch.block_tables, starts, cu, scale,
+                                          _max_q(mode, mq, len(spans), 16, 8), err_flag=err)
+    ref, nerr = orc.paged_attention_prefill(q, batch.k_cache, batch.v_cache, batch.block_tables, starts, cu, scale)
+    assert nerr == 0 and int(err.item()) == 0
+    assert _max_err(out, ref) <= ATOL_16
