@@ -61,6 +61,9 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
 /* Width of the CSR index buffers ("BlockTableIndexType" U32 / U64). */
 typedef enum pkv_index_type { PKV_U32 = 0, PKV_U64 = 1 } pkv_index_type;
 
+/* Quantization scheme tags ("Block-Paged KV Cache", Quantization compatibility). */
+enum { PKV_QUANT_NONE = 0x00, PKV_QUANT_PER_TENSOR = 0x01, PKV_QUANT_PER_CHANNEL = 0x02, PKV_QUANT_PER_BLOCK = 0x03 };
+
 /* Bits OR-ed into *err_flag by the kernels. */
 #define PKV_ERRBIT_SLOT_RANGE   0x01 /* store: slot not -1 and outside [0, num_slots) */
 #define PKV_ERRBIT_BLOCK_RANGE  0x02 /* a used block-table entry outside [0, num_blocks) */
@@ -287,6 +290,27 @@ PKV_API pkv_status pkv_unpack_block_paged(void *out, const void *page_pool, cons
 PKV_API pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void *block_table,
                                       pkv_index_type index_type, int64_t num_seqs, int64_t nnz,
                                       int64_t num_pages);
+
+/*
+ * pkv_validate_quantization_compatibility -- "Block-Paged KV Cache",
+ * Quantization compatibility: whether a quantization scheme's scales fit the
+ * block-paged layout (host only, no pointers).
+ *   scheme_tag  PKV_QUANT_NONE (0x00), PKV_QUANT_PER_TENSOR (0x01),
+ *               PKV_QUANT_PER_CHANNEL (0x02), PKV_QUANT_PER_BLOCK (0x03,
+ *               per-block-affine)
+ *   axis        the axis the scales run along (0 is the paged axis)
+ *   block_size  elements per scale block (per-block-affine only)
+ *   page_size   tokens per page
+ * Per-block-affine is valid only along axis 0 with block_size == page_size,
+ * so a shared page carries its own scales; per-channel scales along the paged
+ * axis are refused; no-scale and per-tensor schemes always fit (the page
+ * states only the first two rules; the rest is this library's reading).
+ * Returns PKV_OK, or PKV_ERR_INVALID_ARG naming the broken rule (also for an
+ * unknown tag or page_size <= 0).  The library's fp8 and int8 caches keep one
+ * scale per (block, KV head): per-block-affine with block_size == page_size.
+ */
+PKV_API pkv_status pkv_validate_quantization_compatibility(int32_t scheme_tag, int32_t axis, int32_t block_size,
+                                                   int32_t page_size);
 
 /*
  * pkv_validate_token_ptr -- host check that token_ptr (host int64 [num_seqs+1])

@@ -62,6 +62,8 @@ def _load():
             lib.orc_paged_attention_decode.restype = i64
             lib.orc_validate_index_buffers.argtypes = [vp, vp, ctypes.c_int, i64, i64, u64]
             lib.orc_validate_index_buffers.restype = ctypes.c_int
+            lib.orc_quantization_compatible.argtypes = [ctypes.c_int] * 4
+            lib.orc_quantization_compatible.restype = ctypes.c_int
             lib.orc_element_offset.argtypes = [i64, i64, i64, i64, i64, u64, i64, i64, vp, vp,
                                                ctypes.c_int, i64]
             lib.orc_element_offset.restype = i64
@@ -250,6 +252,12 @@ def validate_index_buffers(seq_ptr, block_table, num_pages: int, index_dtype=tor
     bt = _cpu(torch.as_tensor(block_table), tdt)
     return _load().orc_validate_index_buffers(_ptr(sp), _ptr(bt), int(is_u64), sp.numel() - 1,
                                               bt.numel(), num_pages)
+
+
+def quantization_compatible(scheme_tag: int, axis: int, block_size: int, page_size: int) -> int:
+    """0 when the quantization scheme fits the block-paged layout, else the
+    broken rule (1..4, see orc_quantization_compatible)."""
+    return _load().orc_quantization_compatible(scheme_tag, axis, block_size, page_size)
 
 
 def element_offset(seq, token, head, dim, page_size, num_pages, num_heads, head_dim,

@@ -237,6 +237,33 @@ static uint64_t load_index(const void *buf, int64_t k, int is_u64)
     return v;
 }
 
+/*
+ * [P1] "Quantization compatibility": the block-paged layout reuses the
+ * quantization schemes with one rule.  Per-block-affine scales (scheme tag
+ * 0x03) must run along axis 0, the paged axis, with block_size == page_size,
+ * so scales stay per page slot; per-channel scales (0x02) along the paged axis
+ * are refused (the page's printed cases).  Reading where the page is silent:
+ * a tag with no per-position scales (0x00 none, 0x01 per-tensor) is
+ * compatible, per-channel along another axis is compatible, and any other tag
+ * is refused.  Returns 0 when compatible, else 1 (per-block-affine off the
+ * paged axis), 2 (per-block-affine with block_size != page_size),
+ * 3 (per-channel on the paged axis), 4 (unknown tag).
+ */
+int orc_quantization_compatible(int scheme_tag, int axis, int block_size, int page_size) {
+    switch (scheme_tag) {
+    case 0x00:
+    case 0x01:
+        return 0;
+    case 0x02:
+        return axis == 0 ? 3 : 0;
+    case 0x03:
+        if (axis != 0) return 1;
+        return block_size == page_size ? 0 : 2;
+    default:
+        return 4;
+    }
+}
+
 /* [P1] "Validating the storage invariants": seq_ptr[0] == 0; seq_ptr is
  * non-decreasing; seq_ptr[num_seqs] == len(block_table); every block_table
  * entry < num_pages.  The empty batch (num_seqs == 0, seq_ptr == [0]) is

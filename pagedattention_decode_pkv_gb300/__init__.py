@@ -54,6 +54,7 @@ _SIGS = {
     "pkv_unpack_block_paged": ([_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _i32, _i64, _i32, _i64, _i32, _i32, _i64,
                                 ctypes.c_int, _vp, _vp], ctypes.c_int),
     "pkv_validate_index_buffers": ([_vp, _vp, ctypes.c_int, _i64, _i64, _i64], ctypes.c_int),
+    "pkv_validate_quantization_compatibility": ([_i32, _i32, _i32, _i32], ctypes.c_int),
     "pkv_validate_token_ptr": ([_vp, _vp, ctypes.c_int, _i64, _i32, _i64], ctypes.c_int),
     "pkv_validate_block_paged_shape": ([_vp, _i32, _i32, _i32], ctypes.c_int),
     "pkv_block_paged_element_offset": ([_i64, _i64, _i64, _i64, _i32, _i64, _i32, _i32, _vp, _vp, ctypes.c_int,
@@ -282,6 +283,16 @@ def pkv_validate_index_buffers(seq_ptr, block_table, num_pages: int, index_dtype
     bt = _host_index(block_table, sp.dtype)
     _check(_lib.pkv_validate_index_buffers(_ptr(sp), _ptr(bt) if bt.numel() else None, _INDEX[sp.dtype],
                                            sp.numel() - 1, bt.numel(), num_pages))
+
+
+QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL, QUANT_PER_BLOCK = 0x00, 0x01, 0x02, 0x03
+
+
+def pkv_validate_quantization_compatibility(scheme_tag: int, axis: int, block_size: int, page_size: int):
+    """Raises PkvError unless the scheme's scales fit the block-paged layout:
+    per-block-affine along the paged axis (0) with block_size == page_size;
+    per-channel not along the paged axis."""
+    _check(_lib.pkv_validate_quantization_compatibility(scheme_tag, axis, block_size, page_size))
 
 
 def pkv_validate_token_ptr(token_ptr, seq_ptr, page_size: int, total_tokens: int, index_dtype=None):

@@ -69,6 +69,35 @@ extern "C" pkv_status pkv_validate_index_buffers(const void *seq_ptr, const void
     return ok();
 }
 
+// "Block-Paged KV Cache", Quantization compatibility: quantization schemes
+// carry over to the block-paged layout except where scales would straddle
+// pages.  Per-block-affine scales must run along the paged axis (0) over
+// exactly one page; per-channel scales must not run along the paged axis.
+extern "C" pkv_status pkv_validate_quantization_compatibility(int32_t scheme_tag, int32_t axis,
+                                                              int32_t block_size, int32_t page_size) {
+    if (page_size <= 0) return set_error(PKV_ERR_INVALID_ARG, "page_size must be positive");
+    switch (scheme_tag) {
+    case PKV_QUANT_NONE:
+    case PKV_QUANT_PER_TENSOR:
+        return ok();
+    case PKV_QUANT_PER_CHANNEL:
+        if (axis == 0)
+            return set_error(PKV_ERR_INVALID_ARG, "per-channel scales cannot run along the paged axis");
+        return ok();
+    case PKV_QUANT_PER_BLOCK:
+        if (axis != 0)
+            return set_error(PKV_ERR_INVALID_ARG, "per-block-affine scales must run along the paged axis (0), not %d",
+                             (int)axis);
+        if (block_size != page_size)
+            return set_error(PKV_ERR_INVALID_ARG,
+                             "per-block-affine block_size (%d) must equal page_size (%d): scales stay per page slot",
+                             (int)block_size, (int)page_size);
+        return ok();
+    default:
+        return set_error(PKV_ERR_INVALID_ARG, "unknown quantization scheme tag 0x%02x", (unsigned)scheme_tag);
+    }
+}
+
 extern "C" pkv_status pkv_validate_token_ptr(const int64_t *token_ptr, const void *seq_ptr,
                                              pkv_index_type index_type, int64_t num_seqs,
                                              int32_t page_size, int64_t total_tokens) {

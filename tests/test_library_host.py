@@ -176,3 +176,21 @@ def test_prefill_argument_errors_are_synchronous(pkv):
     assert call(out=odd) == pkv.PKV_ERR_UNSUPPORTED
     assert lib.pkv_paged_attention_prefill(None, None, None, None, None, 4, None, None, 0, 64, 32, 8, 128, 16, 100,
                                            0.1, pkv.PKV_BF16, None, None) == pkv.PKV_OK  # empty batch
+
+
+def test_quantization_compatibility_matches_the_page_and_the_oracle(pkv, orc):
+    g = load_golden("quantization_cases.json")
+    for c in g["cases"]:
+        st = pkv._lib.pkv_validate_quantization_compatibility(g["scheme_tags"][c["scheme"]], c["axis"],
+                                                              c["block_size"], g["page_size"])
+        assert (st == pkv.PKV_OK) == c["valid"], c["note"]
+    for tag in range(0, 6):
+        for axis in range(0, 4):
+            for bsz in (1, 4, 8, 16):
+                for ps in (4, 16):
+                    st = pkv._lib.pkv_validate_quantization_compatibility(tag, axis, bsz, ps)
+                    assert (st == pkv.PKV_OK) == (orc.quantization_compatible(tag, axis, bsz, ps) == 0)
+    pkv.pkv_validate_quantization_compatibility(pkv.QUANT_PER_BLOCK, 0, 16, 16)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_validate_quantization_compatibility(pkv.QUANT_PER_BLOCK, 0, 8, 16)
+    assert pkv._lib.pkv_validate_quantization_compatibility(3, 0, 4, 0) == pkv.PKV_ERR_INVALID_ARG

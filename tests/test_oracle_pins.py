@@ -546,3 +546,23 @@ def test_prefill_bad_inputs_zero_rows_and_count(orc):
     st3 = torch.tensor([-1, 0], dtype=torch.int32)  # a negative start: zero rows, counted
     out, err = orc.paged_attention_prefill(q, kc, vc, bt, st3, cu, 0.5)
     assert err == 1 and torch.count_nonzero(out[:3]) == 0
+
+
+def test_quantization_compatibility_printed_cases(orc):
+    """The page's three printed cases (page_size 4): per-block-affine along
+    axis 0 with block_size == page_size fits; block_size 8 does not; per-channel
+    along the paged axis does not."""
+    g = load_golden("quantization_cases.json")
+    for c in g["cases"]:
+        code = orc.quantization_compatible(g["scheme_tags"][c["scheme"]], c["axis"], c["block_size"], g["page_size"])
+        assert (code == 0) == c["valid"], c["note"]
+
+
+def test_quantization_compatibility_each_rule(orc):
+    assert orc.quantization_compatible(0x03, 1, 4, 4) == 1   # per-block-affine off the paged axis
+    assert orc.quantization_compatible(0x03, 0, 2, 4) == 2   # block_size != page_size
+    assert orc.quantization_compatible(0x02, 0, 4, 4) == 3   # per-channel on the paged axis
+    assert orc.quantization_compatible(0x02, 2, 4, 4) == 0   # per-channel along heads
+    assert orc.quantization_compatible(0x01, 0, 1, 4) == 0   # per-tensor
+    assert orc.quantization_compatible(0x00, 0, 1, 4) == 0   # none
+    assert orc.quantization_compatible(0x07, 0, 4, 4) == 4   # unknown tag
