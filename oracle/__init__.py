@@ -74,14 +74,16 @@ def _load():
             lib.orc_e4m3_decode.restype = dbl
             lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
             lib.orc_e4m3_encode.restype = ctypes.c_uint8
-            lib.orc_quantize_kvcache_fp8.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int]
-            lib.orc_quantize_kvcache_fp8.restype = None
-            lib.orc_store_kvcache_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
-                                                  ctypes.c_int]
-            lib.orc_store_kvcache_fp8.restype = i64
-            lib.orc_paged_attention_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
-                                                           i32, i32, i32, i32, dbl, ctypes.c_int]
-            lib.orc_paged_attention_decode_fp8.restype = i64
+            lib.orc_int8_encode.argtypes = [ctypes.c_float]
+            lib.orc_int8_encode.restype = ctypes.c_int8
+            lib.orc_quantize_kvcache_q8.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
+            lib.orc_quantize_kvcache_q8.restype = None
+            lib.orc_store_kvcache_q8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                 ctypes.c_int, ctypes.c_int]
+            lib.orc_store_kvcache_q8.restype = i64
+            lib.orc_paged_attention_decode_q8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                          i32, i32, i32, i32, dbl, ctypes.c_int, ctypes.c_int]
+            lib.orc_paged_attention_decode_q8.restype = i64
             lib.orc_paged_attention_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                                         i32, i32, dbl, ctypes.c_int]
             lib.orc_paged_attention_prefill.restype = i64
@@ -184,32 +186,35 @@ def e4m3_encode(x: float) -> int:
     return int(_load().orc_e4m3_encode(x))
 
 
-def quantize_kvcache_fp8(cache):
-    """[num_blocks, bs, H, d] cache -> (uint8 codes of the same shape, float32
-    scales [num_blocks, H]); per (block, head) s = max|x| / 448."""
+_Q8 = {"fp8": (0, torch.uint8), "int8": (1, torch.int8)}  # code format, code dtype
+
+
+def _quantize_q8(cache, fmt):
+    code, cdt = _Q8[fmt]
     src = _cpu(cache)
     nb, bs, H, d = src.shape
-    codes = torch.empty(nb, bs, H, d, dtype=torch.uint8)
+    codes = torch.empty(nb, bs, H, d, dtype=cdt)
     scales = torch.empty(nb, H, dtype=torch.float32)
-    _load().orc_quantize_kvcache_fp8(_ptr(src), _ptr(codes), _ptr(scales), nb, bs, H, d, _DTYPE_CODE[src.dtype])
+    _load().orc_quantize_kvcache_q8(_ptr(src), _ptr(codes), _ptr(scales), nb, bs, H, d, _DTYPE_CODE[src.dtype],
+                                    code)
     return codes, scales
 
 
-def store_kvcache_fp8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping):
-    """fp8 "Step 1" on CPU copies of the code caches; returns (k_codes,
-    v_codes, error count)."""
+def _store_q8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping, fmt):
+    code, cdt = _Q8[fmt]
     key, value = _cpu(key), _cpu(value)
     kc, vc = _cpu(k_codes).clone(), _cpu(v_codes).clone()
+    assert kc.dtype == cdt and vc.dtype == cdt
     ks, vs = _cpu(k_scale, torch.float32), _cpu(v_scale, torch.float32)
     sm = _cpu(slot_mapping, torch.int32)
     nb, bs, H, d = kc.shape
-    err = _load().orc_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(sm),
-                                        sm.numel(), H, d, bs, nb * bs, _DTYPE_CODE[key.dtype])
+    err = _load().orc_store_kvcache_q8(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(sm),
+                                       sm.numel(), H, d, bs, nb * bs, _DTYPE_CODE[key.dtype], code)
     return kc, vc, err
 
 
-def paged_attention_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float):
-    """Binary64 output [B, Hq, d] and error count over an fp8 cache."""
+def _attention_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, fmt):
+    code, cdt = _Q8[fmt]
     q = _cpu(q)
     kc, vc = _cpu(k_codes), _cpu(v_codes)
     ks, vs = _cpu(k_scale, torch.float32), _cpu(v_scale, torch.float32)
@@ -217,12 +222,51 @@ def paged_attention_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tabl
     cl = _cpu(context_lens, torch.int32)
     B, Hq, d = q.shape
     nb, bs, Hkv, d2 = kc.shape
-    assert d2 == d and Hq % Hkv == 0 and kc.dtype == torch.uint8
+    assert d2 == d and Hq % Hkv == 0 and kc.dtype == cdt and vc.dtype == cdt
     out = torch.empty(B, Hq, d, dtype=torch.float64)
-    err = _load().orc_paged_attention_decode_fp8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
-                                                 _ptr(bt), bt.shape[1] if bt.dim() == 2 else 0, _ptr(cl), B, Hq,
-                                                 Hkv, d, bs, nb, float(scale), _DTYPE_CODE[q.dtype])
+    err = _load().orc_paged_attention_decode_q8(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                                _ptr(bt), bt.shape[1] if bt.dim() == 2 else 0, _ptr(cl), B, Hq,
+                                                Hkv, d, bs, nb, float(scale), _DTYPE_CODE[q.dtype], code)
     return out, err
+
+
+def quantize_kvcache_fp8(cache):
+    """[num_blocks, bs, H, d] cache -> (uint8 E4M3 codes of the same shape,
+    float32 scales [num_blocks, H]); per (block, head) s = max|x| / 448."""
+    return _quantize_q8(cache, "fp8")
+
+
+def store_kvcache_fp8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping):
+    """fp8 "Step 1" on CPU copies of the code caches; returns (k_codes,
+    v_codes, error count)."""
+    return _store_q8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping, "fp8")
+
+
+def paged_attention_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float):
+    """Binary64 output [B, Hq, d] and error count over an fp8 cache."""
+    return _attention_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, "fp8")
+
+
+def int8_encode(x: float) -> int:
+    """binary32 -> int8 code: round to nearest even, clamp to [-127, 127], NaN -> 0."""
+    return int(_load().orc_int8_encode(x))
+
+
+def quantize_kvcache_int8(cache):
+    """[num_blocks, bs, H, d] cache -> (int8 codes of the same shape, float32
+    scales [num_blocks, H]); per (block, head) s = max|x| / 127."""
+    return _quantize_q8(cache, "int8")
+
+
+def store_kvcache_int8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping):
+    """int8 "Step 1" on CPU copies of the code caches; returns (k_codes,
+    v_codes, error count)."""
+    return _store_q8(key, value, k_codes, v_codes, k_scale, v_scale, slot_mapping, "int8")
+
+
+def paged_attention_decode_int8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float):
+    """Binary64 output [B, Hq, d] and error count over an int8 cache."""
+    return _attention_q8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, "int8")
 
 
 def paged_attention_prefill(q, k_cache, v_cache, block_tables, starts, cu_q, scale: float):

@@ -394,20 +394,51 @@ uint8_t orc_e4m3_encode(float x)
     return (uint8_t)(sign | ((E + 7) << 3) | ((int)(v / ldexp(1.0, E - 3)) - 8));
 }
 
+/* ---------------------------------------------------------------------------
+ * [P1] "Quantization compatibility" names int8 caches beside fp8 ones, with
+ * symmetric per-block-affine scales.  Readings: a code is a signed byte c in
+ * [-127, 127] standing for scale * c; the scale of a (block, KV head) is
+ * max |x| / 127; encoding rounds x / scale to the nearest integer, ties to
+ * even, and clamps to [-127, 127]; NaN encodes as 0.
+ * ------------------------------------------------------------------------- */
+
+/* binary32 -> int8 code (as above). */
+int8_t orc_int8_encode(float y)
+{
+    double r;
+    if (isnan(y)) return 0;
+    r = rint((double)y);  /* y is a binary32 value: exact in binary64, rint ties to even */
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int8_t)r;
+}
+
+/* Code formats of the quantized caches. */
+enum { Q8_E4M3 = 0, Q8_INT8 = 1 };
+
+/* The largest magnitude of a format: the per-block scale is max |x| / this. */
+static float q8_max(int fmt) { return fmt == Q8_INT8 ? 127.0f : 448.0f; }
+
+static double q8_decode(uint8_t code, int fmt)
+{
+    return fmt == Q8_INT8 ? (double)(int8_t)code : orc_e4m3_decode(code);
+}
+
 /* The code of x stored with scale s: encode(x / s), the division in binary32
  * (the precision the kernels use); a zero scale stores +0. */
-static uint8_t encode_scaled(double x, float s)
+static uint8_t encode_scaled(double x, float s, int fmt)
 {
     if (s == 0.0f) return 0;
+    if (fmt == Q8_INT8) return (uint8_t)orc_int8_encode((float)x / s);
     return orc_e4m3_encode((float)x / s);
 }
 
 /* Quantizes a [num_blocks, bs, H_kv, d] cache of `dtype`: per (block, head),
- * s = max |x| / 448 in binary32 (NaN entries ignored), then every element
- * becomes encode(x / s).  Writes codes [num_blocks, bs, H_kv, d] and scales
- * [num_blocks, H_kv]. */
-void orc_quantize_kvcache_fp8(const void *src, uint8_t *codes, float *scales, int64_t num_blocks,
-                              int64_t bs, int64_t num_kv_heads, int64_t head_dim, int dtype)
+ * s = max |x| / 448 (E4M3) or / 127 (int8) in binary32 (NaN entries ignored),
+ * then every element becomes encode(x / s).  Writes codes
+ * [num_blocks, bs, H_kv, d] and scales [num_blocks, H_kv]. */
+void orc_quantize_kvcache_q8(const void *src, uint8_t *codes, float *scales, int64_t num_blocks,
+                             int64_t bs, int64_t num_kv_heads, int64_t head_dim, int dtype, int fmt)
 {
     build_f16_table();
     for (int64_t blk = 0; blk < num_blocks; ++blk) {
@@ -418,25 +449,25 @@ void orc_quantize_kvcache_fp8(const void *src, uint8_t *codes, float *scales, in
                     float a = (float)fabs(load_elem(src, ((blk * bs + t) * num_kv_heads + h) * head_dim + i, dtype));
                     if (a > amax) amax = a;
                 }
-            float s = amax / 448.0f;
+            float s = amax / q8_max(fmt);
             scales[blk * num_kv_heads + h] = s;
             for (int64_t t = 0; t < bs; ++t)
                 for (int64_t i = 0; i < head_dim; ++i) {
                     int64_t idx = ((blk * bs + t) * num_kv_heads + h) * head_dim + i;
-                    codes[idx] = encode_scaled(load_elem(src, idx, dtype), s);
+                    codes[idx] = encode_scaled(load_elem(src, idx, dtype), s, fmt);
                 }
         }
     }
 }
 
-/* [P3] "Step 1" for an fp8 cache: row slot_mapping[i] of the code caches
+/* [P3] "Step 1" for a quantized cache: row slot_mapping[i] of the code caches
  * receives encode(key[i] / s) per element, s the scale of the row's block and
  * head (slot / bs); -1 is skipped, other slots outside [0, num_slots) are
  * counted and skipped.  key/value are [num_tokens, H_kv, d] of `dtype`. */
-int64_t orc_store_kvcache_fp8(const void *key, const void *value, uint8_t *k_codes, uint8_t *v_codes,
-                              const float *k_scale, const float *v_scale, const int32_t *slot_mapping,
-                              int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim, int64_t bs,
-                              int64_t num_slots, int dtype)
+int64_t orc_store_kvcache_q8(const void *key, const void *value, uint8_t *k_codes, uint8_t *v_codes,
+                             const float *k_scale, const float *v_scale, const int32_t *slot_mapping,
+                             int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim, int64_t bs,
+                             int64_t num_slots, int dtype, int fmt)
 {
     int64_t errors = 0;
     build_f16_table();
@@ -449,22 +480,22 @@ int64_t orc_store_kvcache_fp8(const void *key, const void *value, uint8_t *k_cod
             for (int64_t d = 0; d < head_dim; ++d) {
                 int64_t src = (i * num_kv_heads + h) * head_dim + d;
                 int64_t dst = (slot * num_kv_heads + h) * head_dim + d;
-                k_codes[dst] = encode_scaled(load_elem(key, src, dtype), sk);
-                v_codes[dst] = encode_scaled(load_elem(value, src, dtype), sv);
+                k_codes[dst] = encode_scaled(load_elem(key, src, dtype), sk, fmt);
+                v_codes[dst] = encode_scaled(load_elem(value, src, dtype), sv, fmt);
             }
         }
     }
     return errors;
 }
 
-/* [P3] "Step 2" over an fp8 cache: as orc_paged_attention_decode, with every
- * K/V element read as scale[block][kv head] * decode(code) in binary64. */
-int64_t orc_paged_attention_decode_fp8(double *out, const void *q, const uint8_t *k_codes,
-                                       const uint8_t *v_codes, const float *k_scale, const float *v_scale,
-                                       const int32_t *block_tables, int32_t max_blocks,
-                                       const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                                       int32_t num_kv_heads, int32_t head_dim, int32_t bs, int32_t num_blocks,
-                                       double scale, int q_dtype)
+/* [P3] "Step 2" over a quantized cache: as orc_paged_attention_decode, with
+ * every K/V element read as scale[block][kv head] * decode(code) in binary64. */
+int64_t orc_paged_attention_decode_q8(double *out, const void *q, const uint8_t *k_codes,
+                                      const uint8_t *v_codes, const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables, int32_t max_blocks,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t bs, int32_t num_blocks,
+                                      double scale, int q_dtype, int fmt)
 {
     int64_t errors = 0;
     int32_t group = num_q_heads / num_kv_heads;
@@ -498,7 +529,7 @@ int64_t orc_paged_attention_decode_fp8(double *out, const void *q, const uint8_t
                 double sk = k_scale[(int64_t)phys * num_kv_heads + g];
                 double s = 0.0;
                 for (int32_t i = 0; i < head_dim; ++i)
-                    s += load_elem(q, q_base + i, q_dtype) * (sk * orc_e4m3_decode(k_codes[k_base + i]));
+                    s += load_elem(q, q_base + i, q_dtype) * (sk * q8_decode(k_codes[k_base + i], fmt));
                 scores[t] = scale * s;
                 if (scores[t] > m) m = scores[t];
             }
@@ -517,7 +548,7 @@ int64_t orc_paged_attention_decode_fp8(double *out, const void *q, const uint8_t
                 double sv = v_scale[(int64_t)phys * num_kv_heads + g];
                 double p = scores[t] / l;
                 for (int32_t i = 0; i < head_dim; ++i)
-                    o[i] += p * (sv * orc_e4m3_decode(v_codes[v_base + i]));
+                    o[i] += p * (sv * q8_decode(v_codes[v_base + i], fmt));
             }
         }
         free(scores);

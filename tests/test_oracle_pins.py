@@ -476,6 +476,76 @@ def test_attention_fp8_matches_sdpa_on_dequantized_kv(orc):
     torch.testing.assert_close(out, _sdpa_reference(q, Ks, Vs, Hq, Hkv, d ** -0.5), atol=1e-12, rtol=1e-12)
 
 
+def _int8_restatement(y):
+    """torch's round (half to even) and clamp: the int8 code of binary32 values y."""
+    r = torch.round(y.float()).clamp(-127, 127)
+    return torch.where(torch.isnan(y), torch.zeros_like(r), r).to(torch.int8)
+
+
+def test_int8_encode_rounds_half_even_and_clamps(orc):
+    halves = torch.arange(-130, 131, dtype=torch.float32) + 0.5
+    g = torch.Generator().manual_seed(11)
+    rnd = torch.empty(20000).uniform_(-140, 140, generator=g)
+    xs = torch.cat([halves, torch.nextafter(halves, torch.full_like(halves, 1e9)),
+                    torch.nextafter(halves, torch.full_like(halves, -1e9)), rnd,
+                    torch.tensor([0.0, -0.0, 1e30, -1e30, float("inf"), float("-inf"), float("nan")])])
+    got = torch.tensor([orc.int8_encode(float(x)) for x in xs], dtype=torch.int8)
+    assert torch.equal(got, _int8_restatement(xs))
+    for x, code in [(0.5, 0), (1.5, 2), (2.5, 2), (-2.5, -2), (126.5, 126), (127.5, 127), (-127.5, -127),
+                    (float("nan"), 0)]:
+        assert orc.int8_encode(x) == code, x
+
+
+def test_quantize_and_store_int8_match_a_torch_restatement(orc):
+    """Per (block, head) s = max|x| / 127, codes = round(x / s) (binary32
+    division, ties to even) clamped to [-127, 127], against torch; the store
+    writes the same codes at the slots."""
+    g = torch.Generator().manual_seed(12)
+    nb, bs, H, d = 5, 4, 2, 8
+    cache = (torch.randn(nb, bs, H, d, generator=g) * 3).to(torch.float16)
+    cache[2, :, 1] = 0  # an all-zero (block, head): scale 0, codes 0
+    codes, scales = orc.quantize_kvcache_int8(cache)
+    amax = cache.float().abs().amax(dim=(1, 3))
+    assert codes.dtype == torch.int8 and torch.equal(scales, amax / 127.0)
+    safe = torch.where(scales == 0, torch.ones_like(scales), scales)
+    want = _int8_restatement(cache.float() / safe[:, None, :, None])
+    want[2, :, 1] = 0
+    assert torch.equal(codes, want)
+    assert codes.abs().amax() == 127  # each block's largest element maps to +-127
+    key = (torch.randn(3, H, d, generator=g) * 4).to(torch.float16)  # some beyond 127 s: clamped
+    value = (torch.randn(3, H, d, generator=g) * 2).to(torch.float16)
+    slots = torch.tensor([9, -1, 17], dtype=torch.int32)
+    kc, vc, err = orc.store_kvcache_int8(key, value, codes, codes, scales, scales, slots)
+    assert err == 0
+    for i, slot in ((0, 9), (2, 17)):  # slot 9 is block 2, whose head 1 has scale 0
+        blk = slot // bs
+        want_k = _int8_restatement(key[i].float() / safe[blk][:, None])
+        want_k[scales[blk] == 0] = 0
+        assert torch.equal(kc.reshape(-1, H, d)[slot], want_k)
+    others = [s for s in range(nb * bs) if s not in (9, 17)]
+    assert torch.equal(kc.reshape(-1, H, d)[others], codes.reshape(-1, H, d)[others])
+
+
+def test_attention_int8_matches_sdpa_on_dequantized_kv(orc):
+    """The int8 attention equals SDPA (binary64) over K/V dequantized as
+    scale * code and stored contiguously."""
+    bs, Hq, Hkv, d, nb = 4, 4, 2, 8, 12
+    q, kc, vc, bt, cl, _, _ = _paged_case(bs, Hq, Hkv, d, [1, bs, 2 * bs + 3], nb, seed=13)
+    kq, ks = orc.quantize_kvcache_int8(kc)
+    vq, vs = orc.quantize_kvcache_int8(vc)
+    out, err = orc.paged_attention_decode_int8(q, kq, vq, ks, vs, bt, cl, d ** -0.5)
+    assert err == 0
+    dk = kq.double() * ks.double()[:, None, :, None]
+    dv = vq.double() * vs.double()[:, None, :, None]
+    Ks, Vs = [], []
+    for b in range(3):
+        n = int(cl[b])
+        rows = [(int(bt[b, t // bs]), t % bs) for t in range(n)]
+        Ks.append(torch.stack([dk[p, o] for p, o in rows]))
+        Vs.append(torch.stack([dv[p, o] for p, o in rows]))
+    torch.testing.assert_close(out, _sdpa_reference(q, Ks, Vs, Hq, Hkv, d ** -0.5), atol=1e-12, rtol=1e-12)
+
+
 # --------------------------------------------------------------------------- varlen / chunked prefill
 def _prefill_case(bs, Hq, Hkv, d, spans, nb, seed, dtype=torch.float32):
     """spans: (start, n) per sequence; contiguous K/V of length start + n are
