@@ -64,7 +64,7 @@ def parse_args(argv=None):
                     help="wall-clock budget of the oracle CPU-baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true",
                     help="omit the oracle timing (for profiler runs)")
-    ap.add_argument("--profile-calls", choices=["decode", "fp8", "prefill"], default=None,
+    ap.add_argument("--profile-calls", choices=["decode", "fp8", "int8", "prefill"], default=None,
                     help="profiler driver: run --steps decode-attention calls (16-bit or E4M3 caches) of the "
                          "workload back to back, eagerly, and exit without timing")
     return ap.parse_args(argv)
@@ -131,9 +131,10 @@ def step_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> dict:
     }
 
 
-def fp8_attention_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> int:
-    """Algorithmic bytes of decode attention over E4M3 caches: one byte per K/V
-    element, a K and a V scale per (block, head), q, out and the tables."""
+def code8_attention_bytes(cfg: wl.DecodeConfig, ctx: torch.Tensor, nnz: int) -> int:
+    """Algorithmic bytes of decode attention over 8-bit (E4M3 or int8) caches:
+    one byte per K/V element, a K and a V scale per (block, head), q, out and
+    the tables."""
     es = torch.tensor([], dtype=cfg.dtype).element_size()
     B, T = int(ctx.numel()), int(ctx.to(torch.int64).sum())
     return (T * 2 * cfg.num_kv_heads * cfg.head_dim + 2 * B * cfg.num_q_heads * cfg.head_dim * es + nnz * 4 + B * 4
@@ -363,19 +364,23 @@ class DecodeStep:
                                             b.scale, self.dt, p(self.workspace), self.workspace.numel(),
                                             p(self.err), stream_ptr)
 
-    def make_fp8(self):
-        """E4M3 copies of the caches (per-(block, head) scales) for the fp8 pass."""
-        self.kq, self.ks = self.pkv.pkv_quantize_kvcache_fp8(self.batch.k_cache)
-        self.vq, self.vs = self.pkv.pkv_quantize_kvcache_fp8(self.batch.v_cache)
+    def make_codes(self, fmt: str):
+        """8-bit copies of the caches (fmt "fp8" = E4M3 or "int8"; per-(block,
+        head) scales) for the 8-bit passes; one format is held at a time."""
+        self.kq = self.vq = None
+        quant = getattr(self.pkv, "pkv_quantize_kvcache_" + fmt)
+        self.kq, self.ks = quant(self.batch.k_cache)
+        self.vq, self.vs = quant(self.batch.v_cache)
+        self.code_fmt = fmt
 
-    def fp8_attention(self, stream_ptr) -> int:
-        """Enqueue the decode-attention call over the E4M3 caches."""
+    def code8_attention(self, stream_ptr) -> int:
+        """Enqueue the decode-attention call over the 8-bit caches of make_codes."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
-        return L.pkv_paged_attention_decode_fp8(p(self.out), p(b.q), p(self.kq), p(self.vq), p(self.ks), p(self.vs),
-                                                p(b.block_tables), b.block_tables.shape[1], p(b.context_lens),
-                                                self.B, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
-                                                self.nb, b.max_context_len, b.scale, self.dt, p(self.workspace),
-                                                self.workspace.numel(), p(self.err), stream_ptr)
+        fn = getattr(L, "pkv_paged_attention_decode_" + self.code_fmt)
+        return fn(p(self.out), p(b.q), p(self.kq), p(self.vq), p(self.ks), p(self.vs), p(b.block_tables),
+                  b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads, c.num_kv_heads, c.head_dim,
+                  c.block_size, self.nb, b.max_context_len, b.scale, self.dt, p(self.workspace),
+                  self.workspace.numel(), p(self.err), stream_ptr)
 
     def fused_step(self, stream_ptr) -> int:
         """Enqueue the fused decode step (append the new K/V rows, then attend)."""
@@ -763,11 +768,13 @@ def run_ours(args, world, rank, local):
     sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
     fused_ms, _ = time_attention_sustained(step, args.steps, world, step.fused_step)
     sep_ms, _ = time_attention_sustained(step, args.steps, world, step.separate_step)
-    step.make_fp8()
-    fp8_bytes = fp8_attention_bytes(cfg, step.batch.context_lens.cpu(), step.snap.nnz)
-    fp8_ms, _ = time_attention_sustained(step, args.steps, world, step.fp8_attention)
-    fp8_tok_s = reduce_sum(cfg.batch / (fp8_ms * 1e-3), world, device)
-    fp8_ms = reduce_max(fp8_ms, world, device)
+    code8_bytes = code8_attention_bytes(cfg, step.batch.context_lens.cpu(), step.snap.nnz)
+    code8 = {}
+    for fmt in ("fp8", "int8"):
+        step.make_codes(fmt)
+        ms, _ = time_attention_sustained(step, args.steps, world, step.code8_attention)
+        code8[fmt] = (reduce_max(ms, world, device), reduce_sum(cfg.batch / (ms * 1e-3), world, device))
+    step.kq = step.vq = None
     pre_ms, pre_flops, pre_q = time_prefill(step, max(10, args.steps // 20), world)
     pre_ms = reduce_max(pre_ms, world, device)
     alloc_us = time_host_allocator(pkv, step)
@@ -848,14 +855,15 @@ def run_ours(args, world, rank, local):
             "separate_us": round(sep_ms * 1e3, 2),
             "fused_tokens_per_s": round(fused_tok_s, 1),
             "fused_kv_gbs": round(step.bytes["paged_attention_decode"] / (fused_ms * 1e-3) / 1e9, 1)},
-        "decode_fp8": {
-            "what": "pkv_paged_attention_decode_fp8 over E4M3 copies of the caches (one fp32 scale per block and "
-                    "KV head), back to back in CUDA graphs like the roofline pass",
-            "us_per_call": round(fp8_ms * 1e3, 2),
-            "gbs": round(fp8_bytes / (fp8_ms * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(fp8_bytes / (fp8_ms * 1e-3) / 1e9 / peak, 4),
-            "tokens_per_s": round(fp8_tok_s, 1),
-            "speedup_vs_16bit": round(sus_ms / fp8_ms, 3)},
+        **{f"decode_{fmt}": {
+            "what": f"pkv_paged_attention_decode_{fmt} over {name} copies of the caches (one fp32 scale per block "
+                    "and KV head), back to back in CUDA graphs like the roofline pass",
+            "us_per_call": round(code8[fmt][0] * 1e3, 2),
+            "gbs": round(code8_bytes / (code8[fmt][0] * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(code8_bytes / (code8[fmt][0] * 1e-3) / 1e9 / peak, 4),
+            "tokens_per_s": round(code8[fmt][1], 1),
+            "speedup_vs_16bit": round(sus_ms / code8[fmt][0], 3)}
+           for fmt, name in (("fp8", "E4M3"), ("int8", "int8"))},
         "prefill": {
             "what": f"pkv_paged_attention_prefill: each sequence's last min(ctx, {PREFILL_NEW_TOKENS}) positions as a "
                     "prefill chunk over its own paged context (causal), back to back in CUDA graphs",
@@ -1207,9 +1215,9 @@ def run_profile_calls(args, local):
     torch.cuda.set_device(device)
     step = DecodeStep(pkv, wl.CONFIGS[args.config], seed=args.seed, device=device)
     call = step.attention
-    if args.profile_calls == "fp8":
-        step.make_fp8()
-        call = step.fp8_attention
+    if args.profile_calls in ("fp8", "int8"):
+        step.make_codes(args.profile_calls)
+        call = step.code8_attention
     elif args.profile_calls == "prefill":
         call = prefill_call(step)[0]
     ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)

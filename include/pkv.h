@@ -431,6 +431,39 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, cons
                                                   size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
+ * int8 paged caches -- "Block-Paged KV Cache", Quantization compatibility
+ * names int8 caches beside fp8 ones under the same placement rule.  This
+ * library's reading (symmetric): the caches hold signed bytes c in
+ * [-127, 127], [num_blocks, block_size, num_kv_heads, head_dim], with the
+ * k_scale / v_scale layout of the fp8 caches, a stored value being scale * c.
+ * The scale of a (block, head) is max|x| / 127 (binary32, NaN ignored).
+ * Encoding divides by the scale in binary32, rounds to the nearest integer
+ * (ties to even), clamps to +-127 and stores NaN as 0; a zero scale stores 0.
+ *
+ * pkv_quantize_kvcache_int8, pkv_store_kvcache_int8 and
+ * pkv_paged_attention_decode_int8 take the arguments, and have the
+ * ownership, shape limits, errors and device error bits, of their fp8
+ * counterparts above; only the code format differs.  Codes are widened
+ * exactly to f16 for the products.
+ */
+PKV_API pkv_status pkv_quantize_kvcache_int8(const void *src, void *codes, float *scales, int32_t num_blocks,
+                                             int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                             pkv_dtype dtype, void *stream);
+PKV_API pkv_status pkv_store_kvcache_int8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                          const float *k_scale, const float *v_scale, const int32_t *slot_mapping,
+                                          int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                          int64_t num_slots, int32_t block_size, pkv_dtype dtype,
+                                          int32_t *err_flag, void *stream);
+PKV_API pkv_status pkv_paged_attention_decode_int8(void *out, const void *q, const void *k_cache,
+                                                   const void *v_cache, const float *k_scale, const float *v_scale,
+                                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                   const int32_t *context_lens, int32_t num_seqs,
+                                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                   int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                                   float scale, pkv_dtype dtype, void *workspace,
+                                                   size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
  * Host block allocator -- which physical block of the pool each sequence
  * owns ("Paged KV Cache - AI infra interview lesson": Walk the Shapes First;
  * Append slots during decode; Separate allocation, sharing and release).

@@ -66,6 +66,11 @@ _SIGS = {
                                _vp], ctypes.c_int),
     "pkv_paged_attention_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                         _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
+    "pkv_quantize_kvcache_int8": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_int, _vp], ctypes.c_int),
+    "pkv_store_kvcache_int8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i64, _i32, ctypes.c_int, _vp,
+                                _vp], ctypes.c_int),
+    "pkv_paged_attention_decode_int8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                         _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
     "pkv_allocator_create": ([_i32, _i32, _vp], ctypes.c_int),
     "pkv_allocator_destroy": ([_vp], None),
     "pkv_allocator_add_sequence": ([_vp, _i64, _i64, _vp], ctypes.c_int),
@@ -343,47 +348,46 @@ def pkv_paged_attention_prefill(q, k_cache, v_cache, block_tables, starts, cu_q,
     return out
 
 
-# ----------------------------------------------------------------------------- fp8 (E4M3) caches
-def pkv_quantize_kvcache_fp8(cache, *, codes=None, scales=None, stream=None):
-    """[num_blocks, bs, Hkv, d] cache -> (uint8 E4M3 codes of the same shape,
-    float32 scales [num_blocks, Hkv]); per (block, head) s = max|x| / 448."""
+# ----------------------------------------------------------------------------- 8-bit (E4M3 / int8) caches
+# Code caches: E4M3 as torch.uint8 bytes, int8 as torch.int8.
+_CODES = {"fp8": torch.uint8, "int8": torch.int8}
+
+
+def _quantize_codes(fmt, cache, codes, scales, stream):
     dev = _dev(cache, codes, scales)
     if cache.dtype not in _DTYPE or cache.dim() != 4:
         raise ValueError("cache: [num_blocks, bs, Hkv, d] of float32/float16/bfloat16")
     nb, bs, H, d = cache.shape
     if codes is None:
-        codes = torch.empty(cache.shape, dtype=torch.uint8, device=dev)
+        codes = torch.empty(cache.shape, dtype=_CODES[fmt], device=dev)
     if scales is None:
         scales = torch.empty(nb, H, dtype=torch.float32, device=dev)
-    _want(codes, torch.uint8, "codes")
+    _want(codes, _CODES[fmt], "codes")
     _want(scales, torch.float32, "scales")
+    fn = getattr(_lib, "pkv_quantize_kvcache_" + fmt)
     with torch.cuda.device(dev):
-        _check(_lib.pkv_quantize_kvcache_fp8(_ptr(cache), _ptr(codes), _ptr(scales), nb, bs, H, d,
-                                             _DTYPE[cache.dtype], _stream(dev, stream)))
+        _check(fn(_ptr(cache), _ptr(codes), _ptr(scales), nb, bs, H, d, _DTYPE[cache.dtype], _stream(dev, stream)))
     return codes, scales
 
 
-def pkv_store_kvcache_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, *, err_flag=None,
-                          stream=None):
-    """Writes encode(key[i] / s) into row slot_mapping[i] of the code caches (in place)."""
+def _store_codes(fmt, key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag, stream):
     dev = _dev(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag)
     _want(slot_mapping, torch.int32, "slot_mapping")
-    _want(k_cache, torch.uint8, "k_cache")
-    _want(v_cache, torch.uint8, "v_cache")
+    _want(k_cache, _CODES[fmt], "k_cache")
+    _want(v_cache, _CODES[fmt], "v_cache")
     nb, bs, H, d = k_cache.shape
+    fn = getattr(_lib, "pkv_store_kvcache_" + fmt)
     with torch.cuda.device(dev):
-        _check(_lib.pkv_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                          _ptr(v_scale), _ptr(slot_mapping), slot_mapping.numel(), H, d, nb * bs, bs,
-                                          _DTYPE[key.dtype], _ptr(err_flag), _stream(dev, stream)))
+        _check(fn(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                  _ptr(slot_mapping), slot_mapping.numel(), H, d, nb * bs, bs, _DTYPE[key.dtype], _ptr(err_flag),
+                  _stream(dev, stream)))
 
 
-def pkv_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                                   scale: float, max_context_len: int, *, out=None, workspace=None, err_flag=None,
-                                   stream=None):
-    """Decode attention over E4M3 code caches with per-(block, head) scales."""
+def _attention_codes(fmt, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                     max_context_len, out, workspace, err_flag, stream):
     dev = _dev(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, workspace, err_flag)
-    _want(k_cache, torch.uint8, "k_cache")
-    _want(v_cache, torch.uint8, "v_cache")
+    _want(k_cache, _CODES[fmt], "k_cache")
+    _want(v_cache, _CODES[fmt], "v_cache")
     _want(k_scale, torch.float32, "k_scale")
     _want(v_scale, torch.float32, "v_scale")
     _want(block_tables, torch.int32, "block_tables")
@@ -395,13 +399,53 @@ def pkv_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_
     ws = pkv_paged_attention_decode_workspace_size(B, Hq, Hkv, d, bs, max_context_len, q.dtype) if B else 0
     if ws and workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    fn = getattr(_lib, "pkv_paged_attention_decode_" + fmt)
     with torch.cuda.device(dev):
-        _check(_lib.pkv_paged_attention_decode_fp8(
-            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-            block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale),
-            _DTYPE[q.dtype], _ptr(workspace) if ws else None,
-            workspace.numel() * workspace.element_size() if ws else 0, _ptr(err_flag), _stream(dev, stream)))
+        _check(fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                  block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale),
+                  _DTYPE[q.dtype], _ptr(workspace) if ws else None,
+                  workspace.numel() * workspace.element_size() if ws else 0, _ptr(err_flag), _stream(dev, stream)))
     return out
+
+
+def pkv_quantize_kvcache_fp8(cache, *, codes=None, scales=None, stream=None):
+    """[num_blocks, bs, Hkv, d] cache -> (uint8 E4M3 codes of the same shape,
+    float32 scales [num_blocks, Hkv]); per (block, head) s = max|x| / 448."""
+    return _quantize_codes("fp8", cache, codes, scales, stream)
+
+
+def pkv_store_kvcache_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, *, err_flag=None,
+                          stream=None):
+    """Writes encode(key[i] / s) into row slot_mapping[i] of the E4M3 code caches (in place)."""
+    _store_codes("fp8", key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag, stream)
+
+
+def pkv_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                   scale: float, max_context_len: int, *, out=None, workspace=None, err_flag=None,
+                                   stream=None):
+    """Decode attention over E4M3 code caches with per-(block, head) scales."""
+    return _attention_codes("fp8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                            max_context_len, out, workspace, err_flag, stream)
+
+
+def pkv_quantize_kvcache_int8(cache, *, codes=None, scales=None, stream=None):
+    """[num_blocks, bs, Hkv, d] cache -> (int8 codes of the same shape, float32
+    scales [num_blocks, Hkv]); per (block, head) s = max|x| / 127."""
+    return _quantize_codes("int8", cache, codes, scales, stream)
+
+
+def pkv_store_kvcache_int8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, *, err_flag=None,
+                           stream=None):
+    """Writes encode(key[i] / s) into row slot_mapping[i] of the int8 code caches (in place)."""
+    _store_codes("int8", key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag, stream)
+
+
+def pkv_paged_attention_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                    scale: float, max_context_len: int, *, out=None, workspace=None, err_flag=None,
+                                    stream=None):
+    """Decode attention over int8 code caches with per-(block, head) scales."""
+    return _attention_codes("int8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                            max_context_len, out, workspace, err_flag, stream)
 
 
 # ----------------------------------------------------------------------------- host block allocator

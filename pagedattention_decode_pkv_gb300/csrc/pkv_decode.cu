@@ -652,16 +652,16 @@ constexpr int kFlagLast = 1 << 9;    // last stage of a piece: flush it
 constexpr int kFlagWhole = 1 << 10;  // the piece is the whole unit: write the final output
 constexpr int kFlagAppend = 1 << 11; // the stage holds the step's new token: append its K/V first
 
-// FP8: the cache holds E4M3 codes, one 128-byte row per (token, head), and a
-// per-stage ring holds the (block, head) scales of K and V.
-template <int HPC, int STAGES, bool FP8 = false>
+// C8: the cache holds 8-bit codes (E4M3 or int8), one 128-byte row per (token,
+// head), and a per-stage ring holds the (block, head) scales of K and V.
+template <int HPC, int STAGES, bool C8 = false>
 struct StreamSmem {
-    static constexpr int kTileBytes = FP8 ? HPC * kStageTokens * 128 : HPC * 2 * kStageTokens * 128;
+    static constexpr int kTileBytes = C8 ? HPC * kStageTokens * 128 : HPC * 2 * kStageTokens * 128;
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kTilesBytes = STAGES * kStageBytes;
     static constexpr int kScaleOffset = kTilesBytes;
-    static constexpr int kBatchScaleOffset = kScaleOffset + (FP8 ? STAGES * 2 * HPC * 4 : 0);  // [2][32][2][HPC]
-    static constexpr int kCtxOffset = kBatchScaleOffset + (FP8 ? 2 * 32 * 2 * HPC * 4 : 0);  // int32 ctx per sequence
+    static constexpr int kBatchScaleOffset = kScaleOffset + (C8 ? STAGES * 2 * HPC * 4 : 0);  // [2][32][2][HPC]
+    static constexpr int kCtxOffset = kBatchScaleOffset + (C8 ? 2 * 32 * 2 * HPC * 4 : 0);  // int32 ctx per sequence
     static constexpr int kPrefOffset = kCtxOffset + 4 * kMaxStreamSeqs;   // int64 stage prefix per sequence
     static constexpr int kSPrefOffset = kPrefOffset + 8 * (kMaxStreamSeqs + 16);  // int64 static-part prefix
     static constexpr int kInfoOffset = kSPrefOffset + 8 * (kMaxStreamSeqs + 16);
@@ -701,8 +701,8 @@ __device__ __forceinline__ void locate_stage(Pre pre, int B, int HG, int64_t s, 
     st = static_cast<int>(off - hg * n);
 }
 
-template <typename T, int HPC, int STAGES, bool FP8>
-__global__ void __launch_bounds__((HPC + 1) * 32, FP8 ? 3 : 2)
+template <typename T, int HPC, int STAGES, int FMT>
+__global__ void __launch_bounds__((HPC + 1) * 32, FMT != kCode16 ? 3 : 2)
 decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                      int32_t max_blocks, const int32_t *__restrict__ context_lens, int32_t B, int32_t Hq,
@@ -712,8 +712,9 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      const T *__restrict__ new_k, const T *__restrict__ new_v, T *k_cache_w, T *v_cache_w,
                      const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                      int32_t *__restrict__ err_flag) {
-    using L = StreamSmem<HPC, STAGES, FP8>;
-    using H = Half16<typename std::conditional<FP8, __half, T>::type>;  // FP8 tiles are widened to f16
+    constexpr bool C8 = FMT != kCode16;  // 8-bit codes (E4M3 or int8) with per-(block, head) scales
+    using L = StreamSmem<HPC, STAGES, C8>;
+    using H = Half16<typename std::conditional<C8, __half, T>::type>;  // 8-bit tiles are widened to f16
     const int c = blockIdx.x, C = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     extern __shared__ uint8_t smem_raw[];
@@ -725,8 +726,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const uint32_t bar0 = smem_u32(smem + L::kBarOffset);  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(STAGES+s)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlagOffset);
     const uint32_t tiles = smem_u32(smem);
-    float *scl = reinterpret_cast<float *>(smem + L::kScaleOffset);  // FP8: [STAGES][2][HPC] K / V scales
-    float *bscl = reinterpret_cast<float *>(smem + L::kBatchScaleOffset);  // FP8: [2 batches][32][2][HPC]
+    float *scl = reinterpret_cast<float *>(smem + L::kScaleOffset);  // C8: [STAGES][2][HPC] K / V scales
+    float *bscl = reinterpret_cast<float *>(smem + L::kBatchScaleOffset);  // C8: [2 batches][32][2][HPC]
     auto pre_all = [&](int b) { return pref[b]; };
     auto pre_static = [&](int b) { return spref[b]; };
     auto pre_tail = [&](int b) { return pref[b] - spref[b]; };
@@ -822,7 +823,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const int row = __shfl_sync(0xffffffffu, e_row, e);
                 if (lane == 0) {
                     const uint32_t full = bar0 + 8 * e, dst = tiles + e * L::kStageBytes;
-                    const int z = FP8 ? hg * HPC : 2 * hg * HPC;
+                    const int z = C8 ? hg * HPC : 2 * hg * HPC;
                     mbar_expect_tx(full, L::kStageBytes);
                     if (kKvEvictFirst) {
                         tma_load_3d_hint(dst, &tm_k, 0, id * bs + row, z, full, kv_policy);
@@ -903,7 +904,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         bool bad = false;
         // Stage sb + lane of a batch [sb, se) that lies in segment [lo, hi) of
         // the static region (seg = c) or of the dynamic region (seg = C + k).
-        int cbuf = 0;  // FP8: the batch-scale buffer of the current batch (the next one uses cbuf ^ 1)
+        int cbuf = 0;  // C8: the batch-scale buffer of the current batch (the next one uses cbuf ^ 1)
         auto describe = [&](int64_t sb, int64_t se, int64_t lo, int64_t hi, int seg, int &b, int &hg,
                             int &meta, int &id, int &slot_of_piece, int buf) {
             b = hg = meta = slot_of_piece = 0;
@@ -942,7 +943,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
             if (new_k && st == n - 1) flags |= kFlagAppend;  // position ctx - 1 is in this stage
             meta = min(kStageTokens, ctx - pos0) | flags | in_blk << 16;
-            if constexpr (FP8) {  // this stage's (block, head) scales, 0 for a block that will be skipped
+            if constexpr (C8) {  // this stage's (block, head) scales, 0 for a block that will be skipped
                 float *dst = bscl + (buf * 32 + lane) * 2 * HPC;
                 const bool ok_id = id >= 0 && id < num_blocks;
                 const int64_t base = (static_cast<int64_t>(id) * HG + hg) * HPC;
@@ -1067,7 +1068,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         meta &= ~0xff;
                     }
                     info[slot] = make_int4(b, hg, meta & 0xffff, pslot);
-                    if constexpr (FP8) {
+                    if constexpr (C8) {
                         const float *srcs = bscl + (cbuf * 32 + j) * 2 * HPC;
 #pragma unroll
                         for (int e = 0; e < 2 * HPC; ++e) scl[slot * 2 * HPC + e] = srcs[e];
@@ -1077,7 +1078,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     } else if (id >= 0) {
                         const int slot_row = id * bs + (meta >> 16);
                         const uint32_t dst = tiles + slot * L::kStageBytes;
-                        const int z = FP8 ? hg * HPC : 2 * hg * HPC;  // first head (FP8) or half-row of the box
+                        const int z = C8 ? hg * HPC : 2 * hg * HPC;  // first head (C8) or half-row of the box
                         mbar_arrive_expect_tx(full, L::kStageBytes);
                         if (kKvEvictFirst) {
                             tma_load_3d_hint(dst, &tm_k, 0, slot_row, z, full, kv_policy);
@@ -1135,12 +1136,12 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     // ---------------------------------------------------------------- consumer warp
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, r = lane & 7;
-    // 16-bit caches: this head's rows of the stage tile; FP8: the warp's own
+    // 16-bit caches: this head's rows of the stage tile; C8: the warp's own
     // widened tile (the same [2 halves][16 tokens][128 B] swizzled layout)
-    const uint32_t head_off = FP8 ? 0u : static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
+    const uint32_t head_off = C8 ? 0u : static_cast<uint32_t>(warp) * 2 * kStageTokens * 128;
     uint32_t k_off[8], v_off[8], v8_off[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // FP8 V: lane l addresses row (l & 7) + 8((l >> 3) & 1), chunk 2j + (l >> 4)
+    for (int j = 0; j < 4; ++j) {  // C8 V: lane l addresses row (l & 7) + 8((l >> 3) & 1), chunk 2j + (l >> 4)
         const int tok = r + 8 * (mi & 1);
         v8_off[j] = static_cast<uint32_t>(tok) * 128 + (((2 * j + (mi >> 1)) ^ (tok & 7)) << 4);
     }
@@ -1164,8 +1165,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const bool live = g < G;
         const uint32_t *q32 = reinterpret_cast<const uint32_t *>(
             q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(hk) * G + (live ? g : 0)) * kFastHeadDim);
-        if constexpr (FP8) {
-            // The E4M3 score MMAs take K fragments straight from the codes: in
+        if constexpr (C8) {
+            // The 8-bit score MMAs take K fragments straight from the codes: in
             // MMA kc, lane t's k positions {2t, 2t+1, 2t+8, 2t+9} stand for dims
             // 32t + 4kc + {0, 1, 2, 3}, so q is read in that order (f16 MMAs).
 #pragma unroll
@@ -1227,8 +1228,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
         uint32_t kt, vt;  // K / V tiles the ldmatrix offsets apply to
         float sl = scale_log2, sv = 1.f;
-        if constexpr (FP8) {
-            // this head's E4M3 rows [16 tokens][128 B] of K and of V, and their scales
+        if constexpr (C8) {
+            // this head's 8-bit rows [16 tokens][128 B] of K and of V, and their scales
             kt = tiles + slot * L::kStageBytes + static_cast<uint32_t>(warp) * kStageTokens * 128;
             vt = kt + L::kTileBytes;
             sl = scale_log2 * scl[slot * 2 * HPC + warp];
@@ -1259,7 +1260,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             }
         }
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (FP8) {
+        if constexpr (C8) {
             // Rows g and g + 8 of this head's codes, bytes 32t .. 32t + 31 (chunks
             // 2t, 2t + 1 at their swizzled places): word kc of a row gives MMA
             // kc's k positions (2t, 2t+1) and (2t+8, 2t+9).
@@ -1278,8 +1279,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
             for (int kc = 0; kc < 8; ++kc) {
                 uint32_t a[4];
-                e4m3x4_to_f16x4(wr[0][kc], a[0], a[2]);
-                e4m3x4_to_f16x4(wr[1][kc], a[1], a[3]);
+                codes4_to_f16x4<FMT, false>(wr[0][kc], a[0], a[2]);
+                codes4_to_f16x4<FMT, false>(wr[1][kc], a[1], a[3]);
                 H::mma(sc, a, qf[kc][0], qf[kc][1]);
             }
         } else {
@@ -1318,10 +1319,10 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             o[dc][2] *= a0;
             o[dc][3] *= a1;
         }
-        // FP8: the V scale rides on P (sv = 1 for 16-bit caches); the sums l use P itself
+        // C8: the V scale rides on P (sv = 1 for 16-bit caches); the sums l use P itself
         const uint32_t pb0 = movmatrix_trans(H::pack(p0 * sv, p1 * sv));
         const uint32_t pb1 = movmatrix_trans(H::pack(p2 * sv, p3 * sv));
-        if constexpr (FP8) {
+        if constexpr (C8) {
             // V^T fragments straight from the codes: ldmatrix.trans of the tile
             // read as b16 gives lane (g, t) the bytes (V[2t][2g], V[2t][2g+1],
             // V[2t+1][2g], V[2t+1][2g+1]) of a 16-dim chunk; a byte permute
@@ -1334,8 +1335,8 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     uint32_t a[4];
-                    e4m3x4_to_f16x4(byte_pairs(w[2 * e]), a[0], a[1]);
-                    e4m3x4_to_f16x4(byte_pairs(w[2 * e + 1]), a[2], a[3]);
+                    codes4_to_f16x4<FMT, true>(w[2 * e], a[0], a[1]);
+                    codes4_to_f16x4<FMT, true>(w[2 * e + 1], a[2], a[3]);
                     H::mma(o[2 * j + e], a, pb0, pb1);
                 }
             }
@@ -1363,7 +1364,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
                 for (int dc = 0; dc < 8; ++dc) {
-                    const int d0 = FP8 ? dc * 16 + 2 * g : dc * 16 + g, d1 = FP8 ? d0 + 1 : d0 + 8;
+                    const int d0 = C8 ? dc * 16 + 2 * g : dc * 16 + g, d1 = C8 ? d0 + 1 : d0 + 8;
                     if (hA < G) {
                         T *dst = out + (qhead0 + hA) * kFastHeadDim;
                         dst[d0] = from_f32<T>(o[dc][0] * inv0);
@@ -1379,7 +1380,7 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 const int64_t piece = static_cast<int64_t>(pslot) * HPC + warp;  // * G + head
 #pragma unroll
                 for (int dc = 0; dc < 8; ++dc) {
-                    const int d0 = FP8 ? dc * 16 + 2 * g : dc * 16 + g, d1 = FP8 ? d0 + 1 : d0 + 8;
+                    const int d0 = C8 ? dc * 16 + 2 * g : dc * 16 + g, d1 = C8 ? d0 + 1 : d0 + 8;
                     if (hA < G) {
                         float *dst = o_piece + (piece * G + hA) * kFastHeadDim;
                         dst[d0] = o[dc][0];
@@ -1585,9 +1586,9 @@ append_kv_kernel(const char *__restrict__ key, const char *__restrict__ value, c
 }
 
 // ----------------------------------------------------------------------------- host side
-// E4M3 pool [num_slots, Hkv, 128] of bytes viewed as (128 codes, num_slots,
-// Hkv heads): one 128-byte row per (token, head), HPC heads per box.
-pkv_status make_kv_map_fp8(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int hpc) {
+// 8-bit code pool [num_slots, Hkv, 128] of bytes viewed as (128 codes,
+// num_slots, Hkv heads): one 128-byte row per (token, head), HPC heads per box.
+pkv_status make_kv_map_8bit(CUtensorMap *map, const void *pool, int64_t num_slots, int Hkv, int hpc) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return set_error(PKV_ERR_CUDA, "decode: cuTensorMapEncodeTiled entry point unavailable");
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kFastHeadDim), static_cast<cuuint64_t>(num_slots),
@@ -1630,9 +1631,10 @@ struct DecodeArgs {
     int32_t *ws_meta;
     uint32_t *chunk_ctr;
     const void *new_k, *new_v;  // the step's new K/V rows [B, Hkv, d] to append first, or null
-    const float *k_scale, *v_scale;  // E4M3 caches: scales [num_blocks, Hkv]; null for 16-bit caches
+    const float *k_scale, *v_scale;  // 8-bit caches: scales [num_blocks, Hkv]; null for 16-bit caches
     int32_t *err;
     cudaStream_t stream;
+    int32_t codes = kCode16;  // the cache's code format (CacheCode)
 };
 
 pkv_status launch_append(const DecodeArgs &a, int64_t es) {
@@ -1681,19 +1683,19 @@ int stream_ctas(K kernel, int threads, int smem, std::atomic<int> *per_device) {
     return c;
 }
 
-template <typename T, int HPC, int STAGES, bool FP8>
+template <typename T, int HPC, int STAGES, int FMT>
 struct StreamLaunch {
     static std::atomic<int> ctas[64];
     static std::atomic<uint64_t> configured;
     static int grid() {
-        using L = StreamSmem<HPC, STAGES, FP8>;
-        if (ensure_smem(decode_stream_kernel<T, HPC, STAGES, FP8>, L::kAlloc, configured) != cudaSuccess) return 0;
-        return stream_ctas(decode_stream_kernel<T, HPC, STAGES, FP8>, (HPC + 1) * 32, L::kAlloc, ctas);
+        using L = StreamSmem<HPC, STAGES, FMT != kCode16>;
+        if (ensure_smem(decode_stream_kernel<T, HPC, STAGES, FMT>, L::kAlloc, configured) != cudaSuccess) return 0;
+        return stream_ctas(decode_stream_kernel<T, HPC, STAGES, FMT>, (HPC + 1) * 32, L::kAlloc, ctas);
     }
 };
-template <typename T, int HPC, int STAGES, bool FP8> std::atomic<int> StreamLaunch<T, HPC, STAGES, FP8>::ctas[64];
-template <typename T, int HPC, int STAGES, bool FP8>
-std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES, FP8>::configured{0};
+template <typename T, int HPC, int STAGES, int FMT> std::atomic<int> StreamLaunch<T, HPC, STAGES, FMT>::ctas[64];
+template <typename T, int HPC, int STAGES, int FMT>
+std::atomic<uint64_t> StreamLaunch<T, HPC, STAGES, FMT>::configured{0};
 
 // Warps per merge row: as many as keep the merge grid within about one wave.
 inline int merge_warps_per_row(int64_t rows) {
@@ -1719,21 +1721,21 @@ cudaError_t launch_stream_combine(const DecodeArgs &a, const Plan &p, int C, int
                       static_cast<int64_t>(p.max_segments), rows);
 }
 
-template <typename T, int HPC, int STAGES, bool FP8>
+template <typename T, int HPC, int STAGES, int FMT>
 pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
-    using L = StreamSmem<HPC, STAGES, FP8>;
+    using L = StreamSmem<HPC, STAGES, FMT != kCode16>;
     CUtensorMap mk, mv;
     const int64_t slots = static_cast<int64_t>(a.num_blocks) * a.bs;
-    pkv_status st = FP8 ? make_kv_map_fp8(&mk, a.k_cache, slots, a.Hkv, HPC)
+    pkv_status st = FMT != kCode16 ? make_kv_map_8bit(&mk, a.k_cache, slots, a.Hkv, HPC)
                         : make_kv_map(&mk, a.k_cache, Half16<T>::kTmaType, slots, a.Hkv, HPC);
     if (st != PKV_OK) return st;
-    st = FP8 ? make_kv_map_fp8(&mv, a.v_cache, slots, a.Hkv, HPC)
+    st = FMT != kCode16 ? make_kv_map_8bit(&mv, a.v_cache, slots, a.Hkv, HPC)
              : make_kv_map(&mv, a.v_cache, Half16<T>::kTmaType, slots, a.Hkv, HPC);
     if (st != PKV_OK) return st;
-    const int C = StreamLaunch<T, HPC, STAGES, FP8>::grid();
+    const int C = StreamLaunch<T, HPC, STAGES, FMT>::grid();
     if (C <= 0) return set_error(PKV_ERR_CUDA, "decode: no resident CTA fits the work-balanced kernel");
     const int HG = a.Hkv / HPC, G = a.Hq / a.Hkv;
-    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES, FP8>, dim3(C), dim3((HPC + 1) * 32),
+    cudaError_t e = launch_pdl(kPdlDecode, decode_stream_kernel<T, HPC, STAGES, FMT>, dim3(C), dim3((HPC + 1) * 32),
                                L::kAlloc, a.stream, mk, mv, static_cast<T *>(a.out), static_cast<const T *>(a.q),
                                a.block_tables, a.max_blocks, a.context_lens, a.B, a.Hq, G, HG, a.bs, a.num_blocks,
                                a.max_ctx, a.scale * kLog2e, a.o_part, a.ml_part, a.unit_info, a.ws_meta,
@@ -1748,36 +1750,43 @@ pkv_status launch_stream(const DecodeArgs &a, const Plan &p) {
 
 // Pipeline depth per (heads per CTA, cache format): about 96 KB of stages and
 // two CTAs per SM for 16-bit caches; 48 KB (32 KB for one head) and three
-// CTAs per SM for E4M3 caches, whose consumers do more work per byte and need
+// CTAs per SM for 8-bit caches, whose consumers do more work per byte and need
 // the extra warps to hide latency (measured: 181 vs 199 us on the LLaMA layer).
 template <typename T>
 pkv_status launch_stream_any(const DecodeArgs &a, const Plan &p) {
-    if (a.k_scale) {
+    if (a.codes == kCodeE4M3) {
         switch (p.hpc) {
-        case 4: return launch_stream<T, 4, 3, true>(a, p);
-        case 2: return launch_stream<T, 2, 6, true>(a, p);
-        default: return launch_stream<T, 1, 8, true>(a, p);
+        case 4: return launch_stream<T, 4, 3, kCodeE4M3>(a, p);
+        case 2: return launch_stream<T, 2, 6, kCodeE4M3>(a, p);
+        default: return launch_stream<T, 1, 8, kCodeE4M3>(a, p);
+        }
+    }
+    if (a.codes == kCodeInt8) {
+        switch (p.hpc) {
+        case 4: return launch_stream<T, 4, 3, kCodeInt8>(a, p);
+        case 2: return launch_stream<T, 2, 6, kCodeInt8>(a, p);
+        default: return launch_stream<T, 1, 8, kCodeInt8>(a, p);
         }
     }
     switch (p.hpc) {
-    case 4: return launch_stream<T, 4, 3, false>(a, p);
-    case 2: return launch_stream<T, 2, 6, false>(a, p);
-    default: return launch_stream<T, 1, 8, false>(a, p);
+    case 4: return launch_stream<T, 4, 3, kCode16>(a, p);
+    case 2: return launch_stream<T, 2, 6, kCode16>(a, p);
+    default: return launch_stream<T, 1, 8, kCode16>(a, p);
     }
 }
 
 int stream_grid_for(pkv_dtype dt, int hpc) {
     if (dt == PKV_BF16) {
         switch (hpc) {
-        case 4: return StreamLaunch<__nv_bfloat16, 4, 3, false>::grid();
-        case 2: return StreamLaunch<__nv_bfloat16, 2, 6, false>::grid();
-        default: return StreamLaunch<__nv_bfloat16, 1, 8, false>::grid();
+        case 4: return StreamLaunch<__nv_bfloat16, 4, 3, kCode16>::grid();
+        case 2: return StreamLaunch<__nv_bfloat16, 2, 6, kCode16>::grid();
+        default: return StreamLaunch<__nv_bfloat16, 1, 8, kCode16>::grid();
         }
     }
     switch (hpc) {
-    case 4: return StreamLaunch<__half, 4, 3, false>::grid();
-    case 2: return StreamLaunch<__half, 2, 6, false>::grid();
-    default: return StreamLaunch<__half, 1, 8, false>::grid();
+    case 4: return StreamLaunch<__half, 4, 3, kCode16>::grid();
+    case 2: return StreamLaunch<__half, 2, 6, kCode16>::grid();
+    default: return StreamLaunch<__half, 1, 8, kCode16>::grid();
     }
 }
 
@@ -1877,9 +1886,10 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
                         int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
                         pkv_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
                         const void *new_k, const void *new_v, const float *k_scale = nullptr,
-                        const float *v_scale = nullptr) {
+                        const float *v_scale = nullptr, int32_t codes = kCode16) {
     const int64_t es = dtype_bytes(dtype);
-    const bool fp8 = k_scale != nullptr;  // E4M3 caches with per-(block, head) scales
+    const bool c8 = codes != kCode16;  // 8-bit caches with per-(block, head) scales
+    const char *fmt = codes == kCodeInt8 ? "int8" : "fp8";
     if (es == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks < 0 || max_context_len < 0 || max_blocks_per_seq < 0)
@@ -1906,14 +1916,14 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
         return set_error(PKV_ERR_INVALID_ARG, "decode: buffers not aligned to the element size");
     // The fast path additionally wants 16-byte aligned pools (TMA) and 4-byte aligned q.
     const bool fast = p.fast && num_blocks > 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4);
-    if (fp8) {
+    if (c8) {
         if (!fast || !p.stream || append || !aligned(q, 16))
             return set_error(PKV_ERR_UNSUPPORTED,
-                             "decode fp8: needs fp16/bf16 q, head_dim 128, Hq/Hkv <= 8, block_size a multiple of "
+                             "decode %s: needs fp16/bf16 q, head_dim 128, Hq/Hkv <= 8, block_size a multiple of "
                              "16, at most %d sequences, 16-byte aligned q and code pools",
-                             kMaxStreamSeqs);
-        if (!v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
-            return set_error(PKV_ERR_INVALID_ARG, "decode fp8: scales NULL or not 4-byte aligned");
+                             fmt, kMaxStreamSeqs);
+        if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+            return set_error(PKV_ERR_INVALID_ARG, "decode %s: scales NULL or not 4-byte aligned", fmt);
     }
     if (p.fast && !fast) {
         // CUDA-core fallback with partitions that fit the workspace sized for the fast plan.
@@ -1940,6 +1950,7 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
     // every other path runs the append kernel first, in stream order.
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.codes = codes;
     const bool fused = append && fast && p.stream && aligned(new_k, 8) && aligned(new_v, 8);
     if (fused) {
         a.new_k = new_k;
@@ -2015,7 +2026,23 @@ extern "C" pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, c
     if (dtype == PKV_F32) return set_error(PKV_ERR_UNSUPPORTED, "decode fp8: q/out must be fp16 or bf16");
     return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                         num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
-                        workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, k_scale, v_scale);
+                        workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, k_scale, v_scale, kCodeE4M3);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_int8(void *out, const void *q, const void *k_cache,
+                                                      const void *v_cache, const float *k_scale, const float *v_scale,
+                                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                      const int32_t *context_lens, int32_t num_seqs,
+                                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                      int32_t block_size, int32_t num_blocks, int32_t max_context_len,
+                                                      float scale, pkv_dtype dtype, void *workspace,
+                                                      size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    if (num_seqs > 0 && (!k_scale || !v_scale))
+        return set_error(PKV_ERR_INVALID_ARG, "decode int8: NULL scales");
+    if (dtype == PKV_F32) return set_error(PKV_ERR_UNSUPPORTED, "decode int8: q/out must be fp16 or bf16");
+    return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
+                        workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, k_scale, v_scale, kCodeInt8);
 }
 
 // ----------------------------------------------------------------------------- no-allocation variant

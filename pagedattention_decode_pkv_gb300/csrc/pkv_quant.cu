@@ -1,14 +1,18 @@
-// E4M3 (fp8) paged caches: quantizing a 16-bit cache and the slot-mapping
-// scatter into an fp8 cache.
+// 8-bit paged caches (E4M3 fp8 or int8 codes): quantizing a 16-bit cache and
+// the slot-mapping scatter into an 8-bit cache.
 //
 // "Block-Paged KV Cache" (Hurray format documentation), Quantization
 // compatibility: per-block-affine scales with block_size == page_size stay per
 // page slot, so a shared page carries its own scales.  The pages fix only that
 // placement; this library keeps one binary32 scale per (physical block, KV
 // head) for K and one for V ([num_blocks, Hkv]), a stored value being
-// scale * decode(code) with OCP E4M3 codes.  Encoding divides by the scale in
-// binary32 and rounds to the nearest even code, saturating at +-448
-// (cvt.rn.satfinite); a zero scale stores +0.
+// scale * decode(code).  E4M3: OCP E4M3 codes, scale = max |x| / 448; encoding
+// divides by the scale in binary32 and rounds to the nearest even code,
+// saturating at +-448 (cvt.rn.satfinite).  int8 (the same page names int8
+// caches beside fp8 ones; symmetric reading): signed codes in [-127, 127],
+// scale = max |x| / 127; encoding rounds x / scale (binary32) to the nearest
+// integer, ties to even, clamps to +-127 and maps NaN to 0.  A zero scale
+// stores code 0 in both formats.
 //
 // "Paged KV Cache - AI infra interview lesson", Step 1: slot_mapping and
 // store_kvcache -- row slot of the [num_slots, Hkv * d] cache view receives the
@@ -28,25 +32,40 @@ template <> __device__ __forceinline__ float widen<float>(float x) { return x; }
 template <> __device__ __forceinline__ float widen<__half>(__half x) { return __half2float(x); }
 template <> __device__ __forceinline__ float widen<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// Two binary32 -> two E4M3 codes (lo in the low byte), round to nearest even,
-// saturating; x / s with a zero scale gives +0.
-__device__ __forceinline__ uint32_t encode2(float lo, float hi, float s) {
+enum CodeFormat { kE4M3 = 0, kInt8 = 1 };
+
+// The largest code magnitude: a (block, head) scale is max |x| / this.
+template <int FMT> constexpr float kCodeMax = FMT == kInt8 ? 127.f : 448.f;
+
+// binary32 -> int8 code: nearest integer, ties to even (cvt.rni); NaN -> 0
+// (the conversion's rule for NaN), then clamped to +-127.
+__device__ __forceinline__ uint32_t int8_code(float y) {
+    const int r = min(max(__float2int_rn(y), -127), 127);
+    return static_cast<uint32_t>(r) & 0xFFu;
+}
+
+// Two binary32 -> two codes (lo in the low byte) of x / s; a zero scale gives 0.
+template <int FMT> __device__ __forceinline__ uint32_t encode2(float lo, float hi, float s) {
     if (s == 0.f) return 0u;
     const float a = __fdiv_rn(lo, s), b = __fdiv_rn(hi, s);
-    uint16_t d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
-    return d;
+    if constexpr (FMT == kInt8) {
+        return int8_code(a) | int8_code(b) << 8;
+    } else {
+        uint16_t d;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
+        return d;
+    }
 }
 
 constexpr int kQuantThreads = 256;
 
 // One CTA per block, one warp per head at a time: the head's bs x d values
-// (bs rows of d at a stride of Hkv * d), max |x| (NaN ignored) -> s = max / 448,
+// (bs rows of d at a stride of Hkv * d), max |x| (NaN ignored) -> s = max / kCodeMax,
 // then every value -> its code.  The second pass re-reads the same bytes
 // (L1/L2 resident).
-template <typename T>
+template <int FMT, typename T>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales, int32_t bs,
+quantize_q8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales, int32_t bs,
                     int32_t Hkv, int32_t d) {
     pdl_wait();
     pdl_trigger();
@@ -64,11 +83,11 @@ quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, floa
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float s = __fdiv_rn(m, 448.f);
+        const float s = __fdiv_rn(m, kCodeMax<FMT>);
         if (lane == 0) scales[blk * Hkv + h] = s;
         for (int p = lane; p < n2; p += 32) {
             const int64_t e = at(2 * p);
-            *reinterpret_cast<uint16_t *>(codes + e) = static_cast<uint16_t>(encode2(widen(src[e]), widen(src[e + 1]), s));
+            *reinterpret_cast<uint16_t *>(codes + e) = static_cast<uint16_t>(encode2<FMT>(widen(src[e]), widen(src[e + 1]), s));
         }
     }
 }
@@ -79,9 +98,9 @@ quantize_fp8_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, floa
 // 16-byte aligned source rows (8-byte aligned code rows follow).
 constexpr int kQuantVecs = 8;  // vectors per lane: 16 tokens x 128 dims of a 16-bit cache
 
-template <typename T>
+template <int FMT, typename T>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_fp8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales,
+quantize_q8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, float *__restrict__ scales,
                         int64_t slices, int32_t bs, int32_t Hkv, int32_t d) {
     constexpr int VEC = 16 / sizeof(T);
     pdl_wait();
@@ -112,7 +131,7 @@ quantize_fp8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, 
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float s = __fdiv_rn(m, 448.f);
+        const float s = __fdiv_rn(m, kCodeMax<FMT>);
         if (lane == 0) scales[sl] = s;
 #pragma unroll
         for (int k = 0; k < kQuantVecs; ++k) {
@@ -121,8 +140,8 @@ quantize_fp8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, 
             uint32_t w[VEC / 4];
 #pragma unroll
             for (int q = 0; q < VEC / 4; ++q)
-                w[q] = encode2(widen(x[4 * q]), widen(x[4 * q + 1]), s) |
-                       encode2(widen(x[4 * q + 2]), widen(x[4 * q + 3]), s) << 16;
+                w[q] = encode2<FMT>(widen(x[4 * q]), widen(x[4 * q + 1]), s) |
+                       encode2<FMT>(widen(x[4 * q + 2]), widen(x[4 * q + 3]), s) << 16;
             if constexpr (VEC == 8) {
                 *reinterpret_cast<uint2 *>(codes + off[k]) = make_uint2(w[0], w[1]);
             } else {
@@ -135,9 +154,9 @@ quantize_fp8_vec_kernel(const T *__restrict__ src, uint8_t *__restrict__ codes, 
 constexpr int kStoreThreads = 256;
 
 // One thread per (token, head, pair of dims).
-template <typename T>
+template <int FMT, typename T>
 __global__ void __launch_bounds__(kStoreThreads)
-store_fp8_kernel(const T *__restrict__ key, const T *__restrict__ value, uint8_t *__restrict__ k_codes,
+store_q8_kernel(const T *__restrict__ key, const T *__restrict__ value, uint8_t *__restrict__ k_codes,
                  uint8_t *__restrict__ v_codes, const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                  const int32_t *__restrict__ slot_mapping, int64_t num_tokens, int32_t Hkv, int32_t d, int32_t bs,
                  int64_t num_slots, int32_t *__restrict__ err_flag) {
@@ -159,8 +178,8 @@ store_fp8_kernel(const T *__restrict__ key, const T *__restrict__ value, uint8_t
         const int64_t sidx = static_cast<int64_t>(slot / bs) * Hkv + h;
         const int64_t src = i * Hkv * static_cast<int64_t>(d) + e;
         const int64_t dst = static_cast<int64_t>(slot) * Hkv * d + e;
-        const uint32_t ck = encode2(widen(key[src]), widen(key[src + 1]), __ldg(k_scale + sidx));
-        const uint32_t cv = encode2(widen(value[src]), widen(value[src + 1]), __ldg(v_scale + sidx));
+        const uint32_t ck = encode2<FMT>(widen(key[src]), widen(key[src + 1]), __ldg(k_scale + sidx));
+        const uint32_t cv = encode2<FMT>(widen(value[src]), widen(value[src + 1]), __ldg(v_scale + sidx));
         *reinterpret_cast<uint16_t *>(k_codes + dst) = static_cast<uint16_t>(ck);
         *reinterpret_cast<uint16_t *>(v_codes + dst) = static_cast<uint16_t>(cv);
     }
@@ -177,22 +196,19 @@ int sm_count() {
     return count;
 }
 
-}  // namespace
-}  // namespace pkv
-
-using namespace pkv;
-
-extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
-                                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                                               pkv_dtype dtype, void *stream) {
-    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: unknown dtype %d", (int)dtype);
+// Quantizes a [num_blocks, bs, Hkv, d] cache into codes + scales (`name` names
+// the format in error messages).
+template <int FMT>
+pkv_status quantize_entry(const char *name, const void *src, void *codes, float *scales, int32_t num_blocks,
+                          int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype, void *stream) {
+    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "quantize %s: unknown dtype %d", name, (int)dtype);
     if (num_blocks < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2)
-        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: bad sizes (head_dim must be even)");
-    if (num_blocks > INT32_MAX / 2) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: too many blocks");
+        return set_error(PKV_ERR_INVALID_ARG, "quantize %s: bad sizes (head_dim must be even)", name);
+    if (num_blocks > INT32_MAX / 2) return set_error(PKV_ERR_INVALID_ARG, "quantize %s: too many blocks", name);
     if (num_blocks == 0) return ok();
-    if (!src || !codes || !scales) return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: NULL pointer");
+    if (!src || !codes || !scales) return set_error(PKV_ERR_INVALID_ARG, "quantize %s: NULL pointer", name);
     if (!aligned(src, dtype_bytes(dtype)) || !aligned(codes, 2) || !aligned(scales, 4))
-        return set_error(PKV_ERR_INVALID_ARG, "quantize fp8: misaligned buffers");
+        return set_error(PKV_ERR_INVALID_ARG, "quantize %s: misaligned buffers", name);
     auto s = static_cast<cudaStream_t>(stream);
     auto c = static_cast<uint8_t *>(codes);
     cudaError_t e;
@@ -204,57 +220,47 @@ extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, flo
         const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
         if (grid > cap) grid = cap;
         const dim3 g(static_cast<unsigned>(grid));
+#define PKV_QUANT_VEC(T)                                                                                    \
+    launch_pdl(kPdlStore, quantize_q8_vec_kernel<FMT, T>, g, dim3(kQuantThreads), 0, s, static_cast<const T *>(src), \
+               c, scales, slices, block_size, num_kv_heads, head_dim)
         switch (dtype) {
-        case PKV_BF16:
-            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<__nv_bfloat16>, g, dim3(kQuantThreads), 0, s,
-                           static_cast<const __nv_bfloat16 *>(src), c, scales, slices, block_size, num_kv_heads,
-                           head_dim);
-            break;
-        case PKV_F16:
-            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<__half>, g, dim3(kQuantThreads), 0, s,
-                           static_cast<const __half *>(src), c, scales, slices, block_size, num_kv_heads, head_dim);
-            break;
-        default:
-            e = launch_pdl(kPdlStore, quantize_fp8_vec_kernel<float>, g, dim3(kQuantThreads), 0, s,
-                           static_cast<const float *>(src), c, scales, slices, block_size, num_kv_heads, head_dim);
-            break;
+        case PKV_BF16: e = PKV_QUANT_VEC(__nv_bfloat16); break;
+        case PKV_F16: e = PKV_QUANT_VEC(__half); break;
+        default: e = PKV_QUANT_VEC(float); break;
         }
-        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize fp8 launch: %s", cudaGetErrorString(e));
+#undef PKV_QUANT_VEC
+        if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize %s launch: %s", name, cudaGetErrorString(e));
         return ok();
     }
     const dim3 grid(static_cast<unsigned>(num_blocks));
+#define PKV_QUANT(T)                                                                                              \
+    launch_pdl(kPdlStore, quantize_q8_kernel<FMT, T>, grid, dim3(kQuantThreads), 0, s, static_cast<const T *>(src), c, \
+               scales, block_size, num_kv_heads, head_dim)
     switch (dtype) {
-    case PKV_BF16:
-        e = launch_pdl(kPdlStore, quantize_fp8_kernel<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, s,
-                       static_cast<const __nv_bfloat16 *>(src), c, scales, block_size, num_kv_heads, head_dim);
-        break;
-    case PKV_F16:
-        e = launch_pdl(kPdlStore, quantize_fp8_kernel<__half>, grid, dim3(kQuantThreads), 0, s,
-                       static_cast<const __half *>(src), c, scales, block_size, num_kv_heads, head_dim);
-        break;
-    default:
-        e = launch_pdl(kPdlStore, quantize_fp8_kernel<float>, grid, dim3(kQuantThreads), 0, s,
-                       static_cast<const float *>(src), c, scales, block_size, num_kv_heads, head_dim);
-        break;
+    case PKV_BF16: e = PKV_QUANT(__nv_bfloat16); break;
+    case PKV_F16: e = PKV_QUANT(__half); break;
+    default: e = PKV_QUANT(float); break;
     }
-    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize fp8 launch: %s", cudaGetErrorString(e));
+#undef PKV_QUANT
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "quantize %s launch: %s", name, cudaGetErrorString(e));
     return ok();
 }
 
-extern "C" pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
-                                            const float *k_scale, const float *v_scale,
-                                            const int32_t *slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
-                                            int32_t head_dim, int64_t num_slots, int32_t block_size,
-                                            pkv_dtype dtype, int32_t *err_flag, void *stream) {
-    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "store fp8: unknown dtype %d", (int)dtype);
+// The slot-mapping scatter into 8-bit caches with the given scales.
+template <int FMT>
+pkv_status store_entry(const char *name, const void *key, const void *value, void *k_cache, void *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *slot_mapping, int64_t num_tokens,
+                       int32_t num_kv_heads, int32_t head_dim, int64_t num_slots, int32_t block_size, pkv_dtype dtype,
+                       int32_t *err_flag, void *stream) {
+    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "store %s: unknown dtype %d", name, (int)dtype);
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2 || num_slots < 0 || block_size <= 0)
-        return set_error(PKV_ERR_INVALID_ARG, "store fp8: bad sizes (head_dim must be even)");
+        return set_error(PKV_ERR_INVALID_ARG, "store %s: bad sizes (head_dim must be even)", name);
     if (num_tokens == 0) return ok();
     if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
-        return set_error(PKV_ERR_INVALID_ARG, "store fp8: NULL pointer");
+        return set_error(PKV_ERR_INVALID_ARG, "store %s: NULL pointer", name);
     if (!aligned(key, dtype_bytes(dtype)) || !aligned(value, dtype_bytes(dtype)) || !aligned(k_cache, 2) ||
         !aligned(v_cache, 2) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
-        return set_error(PKV_ERR_INVALID_ARG, "store fp8: misaligned buffers");
+        return set_error(PKV_ERR_INVALID_ARG, "store %s: misaligned buffers", name);
     const int64_t total = num_tokens * num_kv_heads * head_dim / 2;
     int64_t grid = (total + kStoreThreads - 1) / kStoreThreads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
@@ -263,16 +269,53 @@ extern "C" pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, 
     auto kc = static_cast<uint8_t *>(k_cache);
     auto vc = static_cast<uint8_t *>(v_cache);
     cudaError_t e;
-#define PKV_STORE_FP8(T)                                                                                             \
-    launch_pdl(kPdlStore, store_fp8_kernel<T>, dim3(static_cast<unsigned>(grid)), dim3(kStoreThreads), 0, s,        \
+#define PKV_STORE_Q8(T)                                                                                             \
+    launch_pdl(kPdlStore, store_q8_kernel<FMT, T>, dim3(static_cast<unsigned>(grid)), dim3(kStoreThreads), 0, s,    \
                static_cast<const T *>(key), static_cast<const T *>(value), kc, vc, k_scale, v_scale, slot_mapping, \
                num_tokens, num_kv_heads, head_dim, block_size, num_slots, err_flag)
     switch (dtype) {
-    case PKV_BF16: e = PKV_STORE_FP8(__nv_bfloat16); break;
-    case PKV_F16: e = PKV_STORE_FP8(__half); break;
-    default: e = PKV_STORE_FP8(float); break;
+    case PKV_BF16: e = PKV_STORE_Q8(__nv_bfloat16); break;
+    case PKV_F16: e = PKV_STORE_Q8(__half); break;
+    default: e = PKV_STORE_Q8(float); break;
     }
-#undef PKV_STORE_FP8
-    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "store fp8 launch: %s", cudaGetErrorString(e));
+#undef PKV_STORE_Q8
+    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "store %s launch: %s", name, cudaGetErrorString(e));
     return ok();
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
+                                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                               pkv_dtype dtype, void *stream) {
+    return quantize_entry<kE4M3>("fp8", src, codes, scales, num_blocks, block_size, num_kv_heads, head_dim, dtype,
+                                 stream);
+}
+
+extern "C" pkv_status pkv_quantize_kvcache_int8(const void *src, void *codes, float *scales, int32_t num_blocks,
+                                                int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                                pkv_dtype dtype, void *stream) {
+    return quantize_entry<kInt8>("int8", src, codes, scales, num_blocks, block_size, num_kv_heads, head_dim, dtype,
+                                 stream);
+}
+
+extern "C" pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                            const float *k_scale, const float *v_scale,
+                                            const int32_t *slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                                            int32_t head_dim, int64_t num_slots, int32_t block_size,
+                                            pkv_dtype dtype, int32_t *err_flag, void *stream) {
+    return store_entry<kE4M3>("fp8", key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                              num_kv_heads, head_dim, num_slots, block_size, dtype, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_store_kvcache_int8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                             const float *k_scale, const float *v_scale,
+                                             const int32_t *slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                                             int32_t head_dim, int64_t num_slots, int32_t block_size,
+                                             pkv_dtype dtype, int32_t *err_flag, void *stream) {
+    return store_entry<kInt8>("int8", key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                              num_kv_heads, head_dim, num_slots, block_size, dtype, err_flag, stream);
 }

@@ -127,7 +127,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Two bf16 -> two f16 (round to nearest even; the fp8 path runs its MMAs in f16).
+// Two bf16 -> two f16 (round to nearest even; the 8-bit cache paths run their MMAs in f16).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
     uint32_t d;
@@ -152,6 +152,38 @@ __device__ __forceinline__ uint32_t byte_pairs(uint32_t w) {
     uint32_t d;
     asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(d) : "r"(w));
     return d;
+}
+
+// Code formats of the caches the decode kernel reads.
+enum CacheCode { kCode16 = 0, kCodeE4M3 = 1, kCodeInt8 = 2 };
+
+// Four int8 codes -> two f16x2 words, exactly.  Each byte, offset by 128 to an
+// unsigned u (xor of its sign bit), becomes the low mantissa byte of the f16
+// 1024 (0x6400 | u is 1024 + u), and 1152 = 1024 + 128 is subtracted.  The
+// byte selectors SLO / SHI place the bytes: 0x4140 / 0x4342 for (0, 1) and
+// (2, 3), 0x4240 / 0x4341 for (0, 2) and (1, 3).
+template <uint32_t SLO, uint32_t SHI>
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, 0x64646464, %2;" : "=r"(lo) : "r"(u), "n"(SLO));
+    asm("prmt.b32 %0, %1, 0x64646464, %2;" : "=r"(hi) : "r"(u), "n"(SHI));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+// Four 8-bit codes of format FMT -> two f16x2 words holding codes (0, 1) and
+// (2, 3), or (0, 2) and (1, 3) when PAIRS.
+template <int FMT, bool PAIRS>
+__device__ __forceinline__ void codes4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (FMT == kCodeInt8) {
+        if constexpr (PAIRS) {
+            s8x4_to_f16x4<0x4240u, 0x4341u>(w, lo, hi);
+        } else {
+            s8x4_to_f16x4<0x4140u, 0x4342u>(w, lo, hi);
+        }
+    } else {
+        e4m3x4_to_f16x4(PAIRS ? byte_pairs(w) : w, lo, hi);
+    }
 }
 
 template <typename T> struct Half16;

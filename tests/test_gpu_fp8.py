@@ -49,7 +49,8 @@ def test_store_fp8_matches_oracle(pkv, orc, cuda_dev):
     slots = torch.randperm(nb * bs, generator=g)[:n].to(torch.int32)
     slots[5] = -1
     slots[6] = nb * bs + 3  # out of range: skipped, PKV_ERRBIT_SLOT_RANGE
-    slots[7] = 4 * bs + 2   # block 4
+    taken = set(slots.tolist())
+    slots[7] = next(r for r in range(4 * bs, 5 * bs) if r not in taken)  # block 4; slots stay distinct
     err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
     kd, vd = kc.to(cuda_dev), vc.to(cuda_dev)
     pkv.pkv_store_kvcache_fp8(key.to(cuda_dev), value.to(cuda_dev), kd, vd, ks.to(cuda_dev), vs.to(cuda_dev),

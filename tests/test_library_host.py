@@ -194,3 +194,29 @@ def test_quantization_compatibility_matches_the_page_and_the_oracle(pkv, orc):
     with pytest.raises(pkv.PkvError):
         pkv.pkv_validate_quantization_compatibility(pkv.QUANT_PER_BLOCK, 0, 8, 16)
     assert pkv._lib.pkv_validate_quantization_compatibility(3, 0, 4, 0) == pkv.PKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int8"])
+def test_code8_argument_errors_are_synchronous(pkv, fmt):
+    """The 8-bit cache entries (E4M3 and int8) reject bad sizes, NULL pointers
+    and fp32 queries before any CUDA call, and treat empty work as a no-op."""
+    lib = pkv._lib
+    quant = getattr(lib, "pkv_quantize_kvcache_" + fmt)
+    store = getattr(lib, "pkv_store_kvcache_" + fmt)
+    attend = getattr(lib, "pkv_paged_attention_decode_" + fmt)
+    assert quant(None, None, None, 4, 16, 8, 127, pkv.PKV_BF16, None) == pkv.PKV_ERR_INVALID_ARG  # odd head_dim
+    assert b"even" in lib.pkv_last_error_string() and fmt.encode() in lib.pkv_last_error_string()
+    assert quant(None, None, None, 4, 16, 8, 128, 9, None) == pkv.PKV_ERR_INVALID_ARG  # unknown dtype
+    assert quant(None, None, None, 4, 16, 8, 128, pkv.PKV_BF16, None) == pkv.PKV_ERR_INVALID_ARG  # NULL
+    assert quant(None, None, None, 0, 16, 8, 128, pkv.PKV_BF16, None) == pkv.PKV_OK  # no blocks
+    assert store(None, None, None, None, None, None, None, 3, 8, 128, 64, 16, pkv.PKV_BF16, None, None) == \
+        pkv.PKV_ERR_INVALID_ARG
+    assert store(None, None, None, None, None, None, None, 0, 8, 128, 64, 16, pkv.PKV_BF16, None, None) == pkv.PKV_OK
+    args = (None, None, None, None, None, None, None, 4, None, 2, 16, 8, 128, 16, 10, 64, 0.1)
+    assert attend(*args, pkv.PKV_BF16, None, 0, None, None) == pkv.PKV_ERR_INVALID_ARG  # NULL scales
+    assert b"scales" in lib.pkv_last_error_string()
+    P = ctypes.c_void_p(0x10000)
+    args = (None, None, None, None, P, P, None, 4, None, 2, 16, 8, 128, 16, 10, 64, 0.1)
+    assert attend(*args, pkv.PKV_F32, None, 0, None, None) == pkv.PKV_ERR_UNSUPPORTED
+    args = (None, None, None, None, None, None, None, 4, None, 0, 16, 8, 128, 16, 10, 64, 0.1)
+    assert attend(*args, pkv.PKV_BF16, None, 0, None, None) == pkv.PKV_OK  # empty batch
