@@ -47,7 +47,6 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include <cstring>
 #include <type_traits>
 
 #include "pkv_internal.h"
@@ -67,15 +66,20 @@ constexpr uint64_t kPreDeadlineNs = 2000000000ull;
 constexpr float kPreLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: P stays <= 2^8 between rescales
 
-// Sum of the two 16-bit values packed in w (low and high half), in f32.
-template <typename T> __device__ __forceinline__ float pair_sum(uint32_t w);
-template <> __device__ __forceinline__ float pair_sum<__nv_bfloat16>(uint32_t w) {
-    return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+// acc + the low 16-bit value of w (lo) and acc2 + the high one, in f32: the
+// mixed-precision adds take the 16-bit operand as it is (exact widening).
+template <typename T> __device__ __forceinline__ void pair_acc(uint32_t w, float &acc, float &acc2);
+template <> __device__ __forceinline__ void pair_acc<__nv_bfloat16>(uint32_t w, float &acc, float &acc2) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc), "+f"(acc2)
+        : "r"(w));
 }
-template <> __device__ __forceinline__ float pair_sum<__half>(uint32_t w) {
-    __half2 h;
-    memcpy(&h, &w, 4);
-    return __low2float(h) + __high2float(h);
+template <> __device__ __forceinline__ void pair_acc<__half>(uint32_t w, float &acc, float &acc2) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc), "+f"(acc2)
+        : "r"(w));
 }
 
 // Per block size (KEYS keys per block, the S MMA's N) and ring depth: the K/V
@@ -346,20 +350,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             // x = the scaled score (POS: the raw score, scaled inside the exponent
             // below; a positive scale keeps the maximum where it is), -inf if masked
             const float xs = POS ? 1.f : scale_log2;
-            float mx = -INFINITY;
+            // The maximum and the sum below run as four independent chains
+            // (one thread per row has no other work to hide their latency).
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (__all_sync(0xffffffffu, open)) {  // blocks below the diagonal: no mask
 #pragma unroll
                 for (int k = 0; k < kPreKeys; ++k) {
                     if (!POS) x[k] *= xs;
-                    mx = fmaxf(mx, x[k]);
+                    m4[k & 3] = fmaxf(m4[k & 3], x[k]);
                 }
             } else {
 #pragma unroll
                 for (int k = 0; k < kPreKeys; ++k) {
                     x[k] = (k & 15) <= lim[k >> 4] ? x[k] * xs : -INFINITY;
-                    mx = fmaxf(mx, x[k]);
+                    m4[k & 3] = fmaxf(m4[k & 3], x[k]);
                 }
             }
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             if (POS) mx *= scale_log2;
             float a = 1.f;
             bool resc = false;
@@ -371,15 +378,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 m_ref = mx;
             }
             const float base = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum = 0.f;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[kPreKeys / 2];
 #pragma unroll
             for (int i = 0; i < kPreKeys / 2; ++i) {
                 const float e0 = POS ? fmaf(x[2 * i], scale_log2, -base) : x[2 * i] - base;
                 const float e1 = POS ? fmaf(x[2 * i + 1], scale_log2, -base) : x[2 * i + 1] - base;
                 pk[i] = H::pack(fast_exp2(e0), fast_exp2(e1));
-                sum += pair_sum<T>(pk[i]);  // the rounded P the PV MMA uses: the weights sum to 1
+                pair_acc<T>(pk[i], s4[i & 1], s4[2 + (i & 1)]);  // the rounded P the PV MMA uses: weights sum to 1
             }
+            const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
             l_sum = l_sum * a + sum;
             const bool any_resc = __any_sync(0xffffffffu, resc);
             if (any_resc) {  // O changes only after the PV of block j - 1 has added to it
