@@ -82,6 +82,28 @@ template <> __device__ __forceinline__ void pair_acc<__half>(uint32_t w, float &
         : "r"(w));
 }
 
+// max(a, b, c) in one instruction (three-input max; NaN operands are ignored
+// as by fmaxf).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (x0, x1) * s + c per lane, both fused and rounded once (one packed f32x2 FMA);
+// s2 / c2 hold the same value in both halves.
+__device__ __forceinline__ void fma_x2(float x0, float x1, uint64_t s2, uint64_t c2, float &e0, float &e1) {
+    asm("{\n\t.reg .b64 a, d;\n\tmov.b64 a, {%2, %3};\n\t"
+        "fma.rn.f32x2 d, a, %4, %5;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(e0), "=f"(e1)
+        : "f"(x0), "f"(x1), "l"(s2), "l"(c2));
+}
+
+__device__ __forceinline__ uint64_t splat2(float v) {
+    const uint64_t u = __float_as_uint(v);
+    return u | u << 32;
+}
+
 // Per block size (KEYS keys per block, the S MMA's N) and ring depth: the K/V
 // tiles, the shared-memory layout, TMEM columns and mbarrier indices.
 //   KEYS = 128, 3 stages: 230 KB of shared memory, one CTA per SM.
@@ -355,15 +377,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (__all_sync(0xffffffffu, open)) {  // blocks below the diagonal: no mask
 #pragma unroll
-                for (int k = 0; k < kPreKeys; ++k) {
-                    if (!POS) x[k] *= xs;
-                    m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+                for (int k = 0; k < kPreKeys; k += 2) {
+                    if (!POS) {
+                        x[k] *= xs;
+                        x[k + 1] *= xs;
+                    }
+                    m4[(k >> 1) & 3] = max3f(m4[(k >> 1) & 3], x[k], x[k + 1]);
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < kPreKeys; ++k) {
+                for (int k = 0; k < kPreKeys; k += 2) {
                     x[k] = (k & 15) <= lim[k >> 4] ? x[k] * xs : -INFINITY;
-                    m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+                    x[k + 1] = ((k + 1) & 15) <= lim[k >> 4] ? x[k + 1] * xs : -INFINITY;
+                    m4[(k >> 1) & 3] = max3f(m4[(k >> 1) & 3], x[k], x[k + 1]);
                 }
             }
             float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -379,11 +405,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
             const float base = m_ref == -INFINITY ? 0.f : m_ref;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t s2 = splat2(scale_log2), one2 = splat2(1.f), nb2 = splat2(-base);
             uint32_t pk[kPreKeys / 2];
 #pragma unroll
             for (int i = 0; i < kPreKeys / 2; ++i) {
-                const float e0 = POS ? fmaf(x[2 * i], scale_log2, -base) : x[2 * i] - base;
-                const float e1 = POS ? fmaf(x[2 * i + 1], scale_log2, -base) : x[2 * i + 1] - base;
+                float e0, e1;
+                fma_x2(x[2 * i], x[2 * i + 1], POS ? s2 : one2, nb2, e0, e1);  // x * scale - base (POS), x - base
                 pk[i] = H::pack(fast_exp2(e0), fast_exp2(e1));
                 pair_acc<T>(pk[i], s4[i & 1], s4[2 + (i & 1)]);  // the rounded P the PV MMA uses: weights sum to 1
             }
