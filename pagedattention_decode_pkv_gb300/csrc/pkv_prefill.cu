@@ -58,8 +58,6 @@ namespace pkv {
 namespace {
 
 constexpr int kPreRows = 128;        // query rows (position x head) per CTA = TMEM lanes = MMA M
-constexpr int kPreSoftmaxWarps = 4;  // one query row per thread
-constexpr int kPreThreads = (kPreSoftmaxWarps + 2) * 32;  // + producer warp + MMA warp
 constexpr int kQHalf = kPreRows * 128;         // one 64-dim half of the Q tile [128 rows][128 dims]
 constexpr int kQTileBytes = 2 * kQHalf;        // 32 KB
 constexpr uint64_t kPreDeadlineNs = 2000000000ull;
@@ -104,55 +102,64 @@ __device__ __forceinline__ uint64_t splat2(float v) {
     return u | u << 32;
 }
 
-// Per block size (KEYS keys per block, the S MMA's N) and ring depth: the K/V
-// tiles, the shared-memory layout, TMEM columns and mbarrier indices.
-//   KEYS = 128, 3 stages: 230 KB of shared memory, one CTA per SM.
-//   KEYS = 64, 2 stages: 97 KB, two CTAs per SM (eight softmax warps).
-// TMEM: buffers 0 and 1 at columns KEYS b hold S_j (KEYS columns) and then
-// P_j (KEYS / 2 columns of 16-bit pairs, written over the S it came from); O
-// at 2 KEYS.
-template <int KEYS, int STAGES>
+// Per block size (KEYS keys per block, the S MMA's N), ring depth and query
+// tiles per CTA: the K/V tiles, the shared-memory layout, TMEM columns and
+// mbarrier indices.
+//   KEYS = 128, 3 stages, one tile: 230 KB of shared memory, one CTA per SM.
+//   KEYS = 64, 2 stages, one tile: 97 KB, two CTAs per SM (eight softmax warps).
+//   KEYS = 128, 2 stages, two tiles: 198 KB, one CTA per SM, eight softmax
+//     warps (four per tile) sharing every K/V stage.
+// TMEM: tile t owns columns [t kTileCols, (t + 1) kTileCols).  Its kNBuf S / P
+// buffers (two with one tile, one with two tiles) come first: buffer
+// j % kNBuf holds S_j (KEYS columns) and then P_j (KEYS / 2 columns of 16-bit
+// pairs, written over the S it came from); O follows at kTmemO.
+template <int KEYS, int STAGES, int TILES = 1>
 struct PreCfg {
+    static constexpr int kNBuf = TILES == 2 ? 1 : 2;      // S / P buffers per tile
+    static constexpr uint32_t kTmemO = kNBuf * KEYS;       // O's first column within a tile
+    static constexpr uint32_t kTileCols = kNBuf * KEYS + 128;
+    static constexpr uint32_t kTmemCols = KEYS == 64 && TILES == 1 ? 256 : 512;  // a power of two
+    static constexpr int kMinBlocks = KEYS == 64 && TILES == 1 ? 2 : 1;          // CTAs per SM
+    static constexpr int kSoftWarps = 4 * TILES;           // one query row per thread
+    static constexpr int kThreads = (kSoftWarps + 2) * 32;  // + producer warp + MMA warp
     static constexpr int kKvHalf = KEYS * 128;        // one 64-dim half of a K or V tile [KEYS][128 dims]
     static constexpr int kKvTileBytes = 2 * kKvHalf;
     static constexpr int kStageBytes = 2 * kKvTileBytes;  // K then V
-    static constexpr uint32_t kTmemO = 2 * KEYS;
-    static constexpr uint32_t kTmemCols = KEYS == 64 ? 256 : 512;  // the power of two >= 2 KEYS + 128
-    static constexpr int kMinBlocks = KEYS == 64 ? 2 : 1;         // CTAs per SM
     // shared memory
-    static constexpr int kQ = 0;                                   // [2 halves][128 rows][128 B]
-    static constexpr int kKV = kQ + kQTileBytes;                   // stage s: K [2][KEYS][128 B], then V
+    static constexpr int kQ = 0;                                   // [TILES][2 halves][128 rows][128 B]
+    static constexpr int kKV = kQ + TILES * kQTileBytes;           // stage s: K [2][KEYS][128 B], then V
     static constexpr int kKeysOff = kKV + STAGES * kStageBytes;   // int32 [stage][8 chunks] valid keys
     static constexpr int kBar = kKeysOff + 128;                    // mbarriers, 8 bytes each
     static constexpr int kTmemSlot = kBar + 128;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
-    // mbarrier indices
-    static constexpr int kBarKvFull = 0;                      // [STAGES] producer: expect_tx + the copies' bytes
-    static constexpr int kBarKvEmpty = kBarKvFull + STAGES;   // [STAGES] MMA commit after the block's PV
-    static constexpr int kBarSFull = kBarKvEmpty + STAGES;    // [2] MMA commit after S = Q K^T
-    static constexpr int kBarPFull = kBarSFull + 2;           // [2] by block parity: softmax wrote P (rescaled O)
-    static constexpr int kBarODone = kBarPFull + 2;           // [2] by block parity: MMA commit after O += P V
-    static constexpr int kBarQFull = kBarODone + 2;           // 128 softmax threads wrote Q
-    static constexpr int kBarFinal = kBarQFull + 1;           // MMA commit: every MMA of the CTA has completed
+    // mbarrier indices; the per-buffer ones are [TILES][kNBuf] (tile-major)
+    static constexpr int kBarKvFull = 0;                          // [STAGES] producer: expect_tx + the copies' bytes
+    static constexpr int kBarKvEmpty = kBarKvFull + STAGES;       // [STAGES] MMA commit after the block's last PV
+    static constexpr int kBarSFull = kBarKvEmpty + STAGES;        // MMA commit after S = Q K^T
+    static constexpr int kBarPFull = kBarSFull + TILES * kNBuf;   // the tile's 128 softmax threads wrote P
+    static constexpr int kBarODone = kBarPFull + TILES * kNBuf;   // MMA commit after O += P V
+    static constexpr int kBarQFull = kBarODone + TILES * kNBuf;   // [TILES] the tile's 128 threads wrote Q
+    static constexpr int kBarFinal = kBarQFull + TILES;           // MMA commit: every MMA of the CTA has completed
     static constexpr int kNumBars = kBarFinal + 1;
+    static_assert(TILES == 1 || (TILES == 2 && KEYS == 128), "two tiles per CTA take 128-key blocks");
     static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
     static_assert(STAGES * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
-    static_assert(2 * KEYS + 128 <= static_cast<int>(kTmemCols), "S0, S1 and O fit the TMEM allocation");
+    static_assert(TILES * kTileCols <= kTmemCols, "every tile's S buffers and O fit the TMEM allocation");
     static_assert(kAlloc * kMinBlocks <= 227 * 1024 - 1024 * (kMinBlocks - 1), "shared memory per SM");
 };
 
-template <typename T, int KEYS, int STAGES, bool POS>
-__global__ void __launch_bounds__(kPreThreads, (KEYS == 64 ? 2 : 1))
+template <typename T, int KEYS, int STAGES, bool POS, int TILES>
+__global__ void __launch_bounds__(PreCfg<KEYS, STAGES, TILES>::kThreads, PreCfg<KEYS, STAGES, TILES>::kMinBlocks)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                int32_t max_blocks, const int32_t *__restrict__ starts, const int32_t *__restrict__ cu_q,
                int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, int32_t box_rows, float scale_log2,
                int32_t *__restrict__ err_flag) {
-    using L = PreCfg<KEYS, STAGES>;
-    constexpr int kPreKeys = KEYS, kPreStages = STAGES;
+    using L = PreCfg<KEYS, STAGES, TILES>;
+    constexpr int kPreKeys = KEYS, kPreStages = STAGES, kNBuf = L::kNBuf, kSoftWarps = L::kSoftWarps;
     constexpr int kKvHalf = L::kKvHalf, kKvTileBytes = L::kKvTileBytes, kStageBytes = L::kStageBytes;
-    constexpr uint32_t kTmemO = L::kTmemO, kPreTmemCols = L::kTmemCols;
+    constexpr uint32_t kTmemO = L::kTmemO, kTileCols = L::kTileCols, kPreTmemCols = L::kTmemCols;
     constexpr int kBarKvFull = L::kBarKvFull, kBarKvEmpty = L::kBarKvEmpty, kBarSFull = L::kBarSFull;
     constexpr int kBarPFull = L::kBarPFull, kBarODone = L::kBarODone, kBarQFull = L::kBarQFull;
     constexpr int kBarFinal = L::kBarFinal;
@@ -166,17 +173,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t bar0 = smem_u32(smem + L::kBar);
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     const uint32_t sQ = smem_u32(smem + L::kQ), sKV = smem_u32(smem + L::kKV);
-    if (warp == kPreSoftmaxWarps && lane == 0) {
+    if (warp == kSoftWarps && lane == 0) {
         for (int s = 0; s < kPreStages; ++s) {  // per K/V stage
             mbar_init(bar(kBarKvFull + s), 1);
             mbar_init(bar(kBarKvEmpty + s), 1);
         }
-        for (int p = 0; p < 2; ++p) {  // per S / P buffer (block parity)
+        for (int p = 0; p < TILES * kNBuf; ++p) {  // per tile and S / P buffer
             mbar_init(bar(kBarSFull + p), 1);
             mbar_init(bar(kBarPFull + p), kPreRows);
             mbar_init(bar(kBarODone + p), 1);
         }
-        mbar_init(bar(kBarQFull), kPreRows);
+        for (int t = 0; t < TILES; ++t) mbar_init(bar(kBarQFull + t), kPreRows);
         mbar_init(bar(kBarFinal), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tensormap(&tm_k);
@@ -187,15 +194,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int q_begin = cu_q[b], n = cu_q[b + 1] - q_begin, start = starts[b];
     const int positions = kPreRows / G;                       // query positions per tile
     const int tiles_b = n > 0 ? (n + positions - 1) / positions : 0;
-    const int tile = tiles_b - 1 - static_cast<int>(blockIdx.x);  // the last tiles (most keys) launch first
-    if ((n < 0 || tiles_b > static_cast<int>(gridDim.x)) && blockIdx.x == 0 && kh == 0 && threadIdx.x == 0 &&
-        err_flag)  // cu_q decreasing, or more new tokens than max_q_len: rows left unwritten
+    // Tile t of the CTA is tile tiles_b - 1 - (TILES x + t) of the sequence: the
+    // last tiles (most keys) launch first, and tile 0 has at least tile 1's keys.
+    const int tile0 = tiles_b - 1 - static_cast<int>(blockIdx.x) * TILES;
+    if ((n < 0 || tiles_b > static_cast<int>(gridDim.x) * TILES) && blockIdx.x == 0 && kh == 0 &&
+        threadIdx.x == 0 && err_flag)  // cu_q decreasing, or more new tokens than max_q_len: rows left unwritten
         atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
-    if (tile < 0) return;
+    if (tile0 < 0) return;
     const int64_t total = static_cast<int64_t>(start) + n;
     if (start < 0 || (total + bs - 1) / bs > max_blocks) {  // a bad span: zero rows and a flag
-        if (threadIdx.x == 0 && tile == tiles_b - 1 && kh == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
-        const int p0 = tile * positions, p1 = min(n, p0 + positions);
+        if (threadIdx.x == 0 && blockIdx.x == 0 && kh == 0 && err_flag) atomicOr(err_flag, PKV_ERRBIT_CONTEXT);
+        const int p0 = max(tile0 - (TILES - 1), 0) * positions, p1 = min(n, (tile0 + 1) * positions);
         for (int i = threadIdx.x; i < (p1 - p0) * G * kFastHeadDim; i += blockDim.x) {
             const int pi = i / (G * kFastHeadDim), rem = i - pi * G * kFastHeadDim;
             out[(static_cast<int64_t>(q_begin + p0 + pi) * Hq + kh * G) * kFastHeadDim + rem] = from_f32<T>(0.f);
@@ -203,18 +212,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         return;
     }
     // From here on the CTA holds TMEM: every path goes to the common exit below.
-    if (warp == kPreSoftmaxWarps + 1) tmem_alloc(smem_u32(smem + L::kTmemSlot), kPreTmemCols);
+    if (warp == kSoftWarps + 1) tmem_alloc(smem_u32(smem + L::kTmemSlot), kPreTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kTmemSlot);
-    const int q0 = tile * positions;                          // first query index of the tile
-    const int last_pos = start + min(n, q0 + positions) - 1;  // the tile's last position
-    const int nblk = last_pos / kPreKeys + 1;
+    // Keys of each tile: blocks up to its last position (0 for a tile past the sequence's first).
+    int nblk_t[TILES];
+#pragma unroll
+    for (int t = 0; t < TILES; ++t) {
+        const int tt = tile0 - t;
+        nblk_t[t] = tt < 0 ? 0 : (start + min(n, (tt + 1) * positions) - 1) / kPreKeys + 1;
+    }
+    const int nblk = nblk_t[0];
     const uint64_t deadline = global_ns() + kPreDeadlineNs;
     bool timed_out = false;
 
-    if (warp == kPreSoftmaxWarps) {
+    if (warp == kSoftWarps) {
         // ------------------------------------------------------------ producer warp
         // Block j's keys come in chunks of box_rows (= gcd(block_size, 128)) keys:
         // lane l < 128 / box_rows takes chunk l, whose rows are consecutive in one
@@ -264,49 +278,76 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
-            if (bad && err_flag && kh == 0 && tile == tiles_b - 1) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
+            if (bad && err_flag && kh == 0 && blockIdx.x == 0) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
             // no bulk copy may still be writing shared memory when the CTA exits
             for (int j = issued - kPreStages > 0 ? issued - kPreStages : 0; j < issued; ++j)
                 if (!mbar_wait(bar(kBarKvFull + j % kPreStages), (j / kPreStages) & 1, deadline)) timed_out = true;
         }
-    } else if (warp == kPreSoftmaxWarps + 1) {
+    } else if (warp == kSoftWarps + 1) {
         // ------------------------------------------------------------ MMA warp
-        // S_j = Q K_j^T into TMEM columns [128 (j % 2), +128); one block behind,
-        // O (+)= P_{j-1} V_{j-1} into columns [256, 384).
         if (lane == 0) {
             constexpr uint32_t kIdescS = umma_idesc_f16(kBf16, kPreRows, kPreKeys, false);
             constexpr uint32_t kIdescO = umma_idesc_f16(kBf16, kPreRows, kFastHeadDim, true);
-            bool ok = mbar_wait(bar(kBarQFull), 0, deadline);
-            for (int j = 0; ok && j <= nblk; ++j) {
-                if (j < nblk) {
-                    const int s = j % kPreStages;
-                    ok = mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
-                    // buffer j & 1 holds P_{j-2} until the PV of block j - 2 has read it
-                    if (ok && j >= 2) ok = mbar_wait(bar(kBarODone + (j & 1)), ((j - 2) >> 1) & 1, deadline);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t kt = sKV + static_cast<uint32_t>(s) * kStageBytes;
+            // S_j of tile t = Q_t K_j^T into the tile's buffer j % kNBuf, once the
+            // stage has landed and the PV that last read that buffer is done.
+            auto issue_qk = [&](int t, int j) -> bool {
+                const int s = j % kPreStages, bj = j % kNBuf;
+                bool ok = mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
+                if (ok && j >= kNBuf)
+                    ok = mbar_wait(bar(kBarODone + t * kNBuf + bj), ((j - kNBuf) / kNBuf) & 1, deadline);
+                if (!ok) return false;
+                tc_fence_after();
+                const uint32_t kt = sKV + static_cast<uint32_t>(s) * kStageBytes;
+                const uint32_t qt = sQ + static_cast<uint32_t>(t) * kQTileBytes;
 #pragma unroll
-                    for (int k = 0; k < kFastHeadDim / 16; ++k) {  // 16 dims (32 bytes) per step
-                        const uint32_t koff = (k & 3) * 32;
-                        umma_f16(tmem + (j & 1) * kPreKeys, umma_desc_sw128(sQ + (k >> 2) * kQHalf + koff, 16, 1024),
-                                 umma_desc_sw128(kt + (k >> 2) * kKvHalf + koff, 16, 1024), kIdescS, k > 0);
-                    }
-                    umma_commit(bar(kBarSFull + (j & 1)));
+                for (int k = 0; k < kFastHeadDim / 16; ++k) {  // 16 dims (32 bytes) per step
+                    const uint32_t koff = (k & 3) * 32;
+                    umma_f16(tmem + t * kTileCols + bj * kPreKeys,
+                             umma_desc_sw128(qt + (k >> 2) * kQHalf + koff, 16, 1024),
+                             umma_desc_sw128(kt + (k >> 2) * kKvHalf + koff, 16, 1024), kIdescS, k > 0);
                 }
-                if (j >= 1) {
-                    const int pj = j - 1, s = pj % kPreStages;
-                    ok = mbar_wait(bar(kBarPFull + (pj & 1)), (pj >> 1) & 1, deadline);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t vt = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes;
+                umma_commit(bar(kBarSFull + t * kNBuf + bj));
+                return true;
+            };
+            // O_t (+)= P_j V_j once the tile's softmax threads wrote P_j.
+            auto issue_pv = [&](int t, int j) -> bool {
+                const int s = j % kPreStages, bj = j % kNBuf;
+                if (!mbar_wait(bar(kBarPFull + t * kNBuf + bj), (j / kNBuf) & 1, deadline)) return false;
+                tc_fence_after();
+                const uint32_t vt = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes;
+                const uint32_t tc = tmem + t * kTileCols;
 #pragma unroll
-                    for (int k = 0; k < kPreKeys / 16; ++k)  // 16 keys per step: 8 P columns, two 8-row V groups
-                        umma_f16_tmem_a(tmem + kTmemO, tmem + (pj & 1) * kPreKeys + 8 * k,
-                                        umma_desc_sw128(vt + k * 2048, kKvHalf, 1024), kIdescO,
-                                        (pj > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(bar(kBarODone + (pj & 1)));
-                    umma_commit(bar(kBarKvEmpty + s));
+                for (int k = 0; k < kPreKeys / 16; ++k)  // 16 keys per step: 8 P columns, two 8-row V groups
+                    umma_f16_tmem_a(tc + kTmemO, tc + bj * kPreKeys + 8 * k,
+                                    umma_desc_sw128(vt + k * 2048, kKvHalf, 1024), kIdescO,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(kBarODone + t * kNBuf + bj));
+                return true;
+            };
+            bool ok = true;
+            for (int t = 0; t < TILES; ++t)
+                if (ok && nblk_t[t] > 0) ok = mbar_wait(bar(kBarQFull + t), 0, deadline);
+            if constexpr (TILES == 1) {
+                // QK_j, then (one block behind) PV_{j-1}: S_{j+1} is computed while
+                // the softmax works on S_j.
+                for (int j = 0; ok && j <= nblk; ++j) {
+                    if (j < nblk) ok = issue_qk(0, j);
+                    if (ok && j >= 1) {
+                        ok = issue_pv(0, j - 1);
+                        if (ok) umma_commit(bar(kBarKvEmpty + (j - 1) % kPreStages));
+                    }
+                }
+            } else {
+                // Two tiles take turns: while one tile's softmax works on S_j, the
+                // tensor core runs the other tile's PV and next QK.
+                if (ok) ok = issue_qk(0, 0);
+                if (ok && nblk_t[1] > 0) ok = issue_qk(1, 0);
+                for (int j = 0; ok && j < nblk; ++j) {
+                    ok = issue_pv(0, j);
+                    if (ok && j + 1 < nblk) ok = issue_qk(0, j + 1);
+                    if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
+                    if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
+                    if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
                 }
             }
             if (!ok) timed_out = true;
@@ -316,30 +357,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- softmax warps
-        // Thread r owns query row r: position index r / G, head r % G of the group.
-        const int r = threadIdx.x;
+        // Warps 4t .. 4t + 3 serve tile t; its thread r owns query row r:
+        // position index r / G, head r % G of the group.
+        const int t = warp >> 2;
+        const int r = threadIdx.x - t * kPreRows;
+        const int my_nblk = t == 0 ? nblk_t[0] : nblk_t[TILES - 1];
+        const int q0 = (tile0 - t) * positions;  // first query index of the tile
         const int pi = r / G, hd = r - pi * G;
-        const bool live = q0 + pi < n;
+        const bool live = my_nblk > 0 && q0 + pi < n;
         const int pos = start + q0 + pi;
         const int64_t qrow = (static_cast<int64_t>(q_begin) + q0 + pi) * Hq + kh * G + hd;
-        {  // Q row into shared memory (zeros past the sequence)
+        if (my_nblk > 0) {  // Q row into shared memory (zeros past the sequence)
+            const uint32_t sQt = sQ + static_cast<uint32_t>(t) * kQTileBytes;
             const int4 *src = reinterpret_cast<const int4 *>(q + qrow * kFastHeadDim);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int4 v = live ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ + (c >> 3) * kQHalf + r * 128 +
-                                                                               (((c & 7) ^ (r & 7)) << 4)),
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQt + (c >> 3) * kQHalf + r * 128 +
+                                                                                (((c & 7) ^ (r & 7)) << 4)),
                              "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                              : "memory");
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(bar(kBarQFull));
+            mbar_arrive(bar(kBarQFull + t));
         }
-        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
+        // this warp's TMEM lanes (32 (warp % 4) ..) in the tile's columns
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + t * kTileCols;
+        const int bar_t = t * kNBuf;  // the tile's first S / P / O barrier
         float m_ref = -INFINITY, l_sum = 0.f;
-        for (int j = 0; j < nblk; ++j) {
-            const int s = j % kPreStages;
-            bool ok = mbar_wait(bar(kBarSFull + (j & 1)), (j >> 1) & 1, deadline) &&
+        for (int j = 0; j < my_nblk; ++j) {
+            const int s = j % kPreStages, bj = j % kNBuf;
+            bool ok = mbar_wait(bar(kBarSFull + bar_t + bj), (j / kNBuf) & 1, deadline) &&
                       mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
             if (!__all_sync(0xffffffffu, ok)) {
                 timed_out = true;
@@ -350,7 +398,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int c0 = 0; c0 < kPreKeys; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld32(trow + (j & 1) * kPreKeys + c0, v);
+                tmem_ld32(trow + bj * kPreKeys + c0, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(v[i]);
             }
@@ -418,7 +466,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             l_sum = l_sum * a + sum;
             const bool any_resc = __any_sync(0xffffffffu, resc);
             if (any_resc) {  // O changes only after the PV of block j - 1 has added to it
-                ok = j == 0 || mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, deadline);
+                ok = j == 0 || mbar_wait(bar(kBarODone + bar_t + (j - 1) % kNBuf), ((j - 1) / kNBuf) & 1, deadline);
                 if (!__all_sync(0xffffffffu, ok)) {
                     timed_out = true;
                     break;
@@ -442,10 +490,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 uint32_t v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = pk[c0 + i];
-                tmem_st32(trow + (j & 1) * kPreKeys + c0, v);
+                tmem_st32(trow + bj * kPreKeys + c0, v);
             }
             tmem_wait_st();
-            if (r < kPreKeys) {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
+            if (t == 0 && r < kPreKeys) {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
                 const int g = r >> 4, ch = (16 * g) / box_rows;
                 if ((r & 15) >= kv_keys[s * 8 + ch] - (16 * g - ch * box_rows)) {
                     const uint32_t vrow = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes + r * 128;
@@ -459,11 +507,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed V rows
             tc_fence_before();
-            mbar_arrive(bar(kBarPFull + (j & 1)));
+            mbar_arrive(bar(kBarPFull + bar_t + bj));
         }
         // Epilogue: O row / row sum once the last PV is done.
-        bool ok = !timed_out && mbar_wait(bar(kBarODone + ((nblk - 1) & 1)), ((nblk - 1) >> 1) & 1, deadline);
-        if (__all_sync(0xffffffffu, ok)) {
+        bool ok = !timed_out && (my_nblk == 0 || mbar_wait(bar(kBarODone + bar_t + (my_nblk - 1) % kNBuf),
+                                                            ((my_nblk - 1) / kNBuf) & 1, deadline));
+        if (my_nblk == 0) {
+            // a second tile past the sequence's first: nothing to write
+        } else if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             T *dst = out + qrow * kFastHeadDim;
@@ -491,23 +542,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kPreSoftmaxWarps + 1) tmem_dealloc(tmem, kPreTmemCols);
+    if (warp == kSoftWarps + 1) tmem_dealloc(tmem, kPreTmemCols);
 }
 
-template <typename T, int KEYS, int STAGES, bool POS>
+template <typename T, int KEYS, int STAGES, bool POS, int TILES>
 cudaError_t prefill_smem_once() {  // one flag per instantiation (they share a function type)
     static int done_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_dev == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(prefill_kernel<T, KEYS, STAGES, POS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PreCfg<KEYS, STAGES>::kAlloc);
+    e = cudaFuncSetAttribute(prefill_kernel<T, KEYS, STAGES, POS, TILES>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PreCfg<KEYS, STAGES, TILES>::kAlloc);
     if (e == cudaSuccess) done_dev = dev;
     return e;
 }
 
-template <typename T, int KEYS, int STAGES, bool POS>
+template <typename T, int KEYS, int STAGES, bool POS, int TILES>
 pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
                           const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
@@ -521,12 +572,13 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     if (st != PKV_OK) return st;
     st = make_kv_map_box(&mv, v_cache, Half16<T>::kTmaType, slots, Hkv, box_rows, 1);
     if (st != PKV_OK) return st;
-    cudaError_t e = prefill_smem_once<T, KEYS, STAGES, POS>();
+    cudaError_t e = prefill_smem_once<T, KEYS, STAGES, POS, TILES>();
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
     const int G = Hq / Hkv, positions = kPreRows / G;
     const int tiles = (max_q_len + positions - 1) / positions;
-    e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES, POS>, dim3(tiles, Hkv, B), dim3(kPreThreads),
-                   PreCfg<KEYS, STAGES>::kAlloc, stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q),
+    using L = PreCfg<KEYS, STAGES, TILES>;
+    e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES, POS, TILES>, dim3((tiles + TILES - 1) / TILES, Hkv, B),
+                   dim3(L::kThreads), L::kAlloc, stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q),
                    block_tables, max_blocks, starts, cu_q, Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PKV_OK;
@@ -550,16 +602,16 @@ pkv_status launch_prefill_any(void *out, const void *q, const void *k_cache, con
     const int positions = kPreRows / (Hq / Hkv);
     const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((max_q_len + positions - 1) / positions);
     // A positive scale (the usual 1/sqrt(d)) moves into the exponent's argument.
-#define PKV_PREFILL_LAUNCH(KEYS, STAGES)                                                                            \
-    (scale > 0.f ? launch_prefill<T, KEYS, STAGES, true>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, \
-                                                         cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, scale, err,    \
-                                                         stream)                                                     \
-                 : launch_prefill<T, KEYS, STAGES, false>(out, q, k_cache, v_cache, block_tables, max_blocks, starts,\
-                                                          cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, scale, err,   \
-                                                          stream))
+#define PKV_PREFILL_LAUNCH(KEYS, STAGES, TILES)                                                                     \
+    (scale > 0.f ? launch_prefill<T, KEYS, STAGES, true, TILES>(out, q, k_cache, v_cache, block_tables, max_blocks,  \
+                                                                starts, cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, \
+                                                                scale, err, stream)                                  \
+                 : launch_prefill<T, KEYS, STAGES, false, TILES>(out, q, k_cache, v_cache, block_tables, max_blocks, \
+                                                                 starts, cu_q, B, max_q_len, Hq, Hkv, bs,            \
+                                                                 num_blocks, scale, err, stream))
     const pkv_status st = static_cast<int64_t>(max_blocks) * bs >= kLongContextTokens || ctas < kManyCtas
-                              ? PKV_PREFILL_LAUNCH(128, 3)
-                              : PKV_PREFILL_LAUNCH(64, 2);
+                              ? PKV_PREFILL_LAUNCH(128, 2, 2)
+                              : PKV_PREFILL_LAUNCH(64, 2, 1);
 #undef PKV_PREFILL_LAUNCH
     return st;
 }
