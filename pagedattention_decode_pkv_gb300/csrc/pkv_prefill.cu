@@ -109,13 +109,14 @@ __device__ __forceinline__ uint64_t splat2(float v) {
 //   KEYS = 64, 2 stages, one tile: 97 KB, two CTAs per SM (eight softmax warps).
 //   KEYS = 128, 2 stages, two tiles: 198 KB, one CTA per SM, eight softmax
 //     warps (four per tile) sharing every K/V stage.
+//   KEYS = 64, 4 stages, two tiles: 198 KB, one CTA per SM, eight softmax warps.
 // TMEM: tile t owns columns [t kTileCols, (t + 1) kTileCols).  Its kNBuf S / P
-// buffers (two with one tile, one with two tiles) come first: buffer
+// buffers (one for two tiles of 128-key blocks, two otherwise) come first: buffer
 // j % kNBuf holds S_j (KEYS columns) and then P_j (KEYS / 2 columns of 16-bit
 // pairs, written over the S it came from); O follows at kTmemO.
 template <int KEYS, int STAGES, int TILES = 1>
 struct PreCfg {
-    static constexpr int kNBuf = TILES == 2 ? 1 : 2;      // S / P buffers per tile
+    static constexpr int kNBuf = TILES == 2 && KEYS == 128 ? 1 : 2;  // S / P buffers per tile
     static constexpr uint32_t kTmemO = kNBuf * KEYS;       // O's first column within a tile
     static constexpr uint32_t kTileCols = kNBuf * KEYS + 128;
     static constexpr uint32_t kTmemCols = KEYS == 64 && TILES == 1 ? 256 : 512;  // a power of two
@@ -130,7 +131,7 @@ struct PreCfg {
     static constexpr int kKV = kQ + TILES * kQTileBytes;           // stage s: K [2][KEYS][128 B], then V
     static constexpr int kKeysOff = kKV + STAGES * kStageBytes;   // int32 [stage][8 chunks] valid keys
     static constexpr int kBar = kKeysOff + 128;                    // mbarriers, 8 bytes each
-    static constexpr int kTmemSlot = kBar + 128;
+    static constexpr int kTmemSlot = kBar + 256;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
     // mbarrier indices; the per-buffer ones are [TILES][kNBuf] (tile-major)
@@ -142,8 +143,8 @@ struct PreCfg {
     static constexpr int kBarQFull = kBarODone + TILES * kNBuf;   // [TILES] the tile's 128 threads wrote Q
     static constexpr int kBarFinal = kBarQFull + TILES;           // MMA commit: every MMA of the CTA has completed
     static constexpr int kNumBars = kBarFinal + 1;
-    static_assert(TILES == 1 || (TILES == 2 && KEYS == 128), "two tiles per CTA take 128-key blocks");
-    static_assert(kNumBars * 8 <= 128, "the mbarriers fit their shared-memory slot");
+    static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
+    static_assert(kNumBars * 8 <= 256, "the mbarriers fit their shared-memory slot");
     static_assert(STAGES * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
     static_assert(TILES * kTileCols <= kTmemCols, "every tile's S buffers and O fit the TMEM allocation");
     static_assert(kAlloc * kMinBlocks <= 227 * 1024 - 1024 * (kMinBlocks - 1), "shared memory per SM");
@@ -339,15 +340,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 }
             } else {
                 // Two tiles take turns: while one tile's softmax works on S_j, the
-                // tensor core runs the other tile's PV and next QK.
+                // tensor core runs the other tile's PV and next QK.  With one S
+                // buffer per tile the next QK follows the PV that frees it; with two
+                // it goes first (its buffer was freed by the PV of block j - 1).
                 if (ok) ok = issue_qk(0, 0);
                 if (ok && nblk_t[1] > 0) ok = issue_qk(1, 0);
                 for (int j = 0; ok && j < nblk; ++j) {
-                    ok = issue_pv(0, j);
-                    if (ok && j + 1 < nblk) ok = issue_qk(0, j + 1);
-                    if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
-                    if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
-                    if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
+                    if constexpr (kNBuf == 1) {
+                        ok = issue_pv(0, j);
+                        if (ok && j + 1 < nblk) ok = issue_qk(0, j + 1);
+                        if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
+                        if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
+                        if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
+                    } else {
+                        if (j + 1 < nblk) ok = issue_qk(0, j + 1);
+                        if (ok) ok = issue_pv(0, j);
+                        if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
+                        if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
+                        if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
+                    }
                 }
             }
             if (!ok) timed_out = true;
@@ -584,36 +595,23 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     return PKV_OK;
 }
 
-// Configuration: 64-key blocks with two CTAs per SM keep eight softmax warps
-// per SM busy and win when the grid is many waves deep; 128-key blocks (three
-// stages, one CTA per SM) halve the per-block costs and the wave tail, and win
-// for contexts that can reach 16k tokens or grids under 16 waves of two-CTA
-// slots.  Measured on GB300 (TFLOP/s, 128 vs 64 keys): LLaMA-shaped layer
-// (8192 CTAs, contexts <= 4k) 425 vs 500, Qwen3-shaped (8192 CTAs, <= 8k) 515 vs
-// 593, 8 x 8192 (1024 CTAs) 524 vs 477, 8 x 32768 635 vs 497.
-constexpr int64_t kLongContextTokens = 16384;
-constexpr int64_t kManyCtas = 16 * 2 * 152;
-
+// Configuration: 128-key blocks, two query tiles per CTA (eight softmax warps
+// sharing each K/V stage), two stages, one CTA per SM.  Measured on GB300
+// against the other configurations the kernel template admits (TFLOP/s; one
+// tile of 64-key blocks with two CTAs per SM / two tiles of 64-key blocks with
+// four stages / two tiles of 128-key blocks): LLaMA-shaped layer 529 / 622 /
+// 722, Qwen3-shaped layer 631 / 667 / 975, 8 x 8192 513 / 612 / 741.
 template <typename T>
 pkv_status launch_prefill_any(void *out, const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks, const int32_t *starts,
                               const int32_t *cu_q, int32_t B, int32_t max_q_len, int32_t Hq, int32_t Hkv, int32_t bs,
                               int32_t num_blocks, float scale, int32_t *err, cudaStream_t stream) {
-    const int positions = kPreRows / (Hq / Hkv);
-    const int64_t ctas = static_cast<int64_t>(B) * Hkv * ((max_q_len + positions - 1) / positions);
     // A positive scale (the usual 1/sqrt(d)) moves into the exponent's argument.
-#define PKV_PREFILL_LAUNCH(KEYS, STAGES, TILES)                                                                     \
-    (scale > 0.f ? launch_prefill<T, KEYS, STAGES, true, TILES>(out, q, k_cache, v_cache, block_tables, max_blocks,  \
-                                                                starts, cu_q, B, max_q_len, Hq, Hkv, bs, num_blocks, \
-                                                                scale, err, stream)                                  \
-                 : launch_prefill<T, KEYS, STAGES, false, TILES>(out, q, k_cache, v_cache, block_tables, max_blocks, \
-                                                                 starts, cu_q, B, max_q_len, Hq, Hkv, bs,            \
-                                                                 num_blocks, scale, err, stream))
-    const pkv_status st = static_cast<int64_t>(max_blocks) * bs >= kLongContextTokens || ctas < kManyCtas
-                              ? PKV_PREFILL_LAUNCH(128, 2, 2)
-                              : PKV_PREFILL_LAUNCH(64, 2, 1);
-#undef PKV_PREFILL_LAUNCH
-    return st;
+    if (scale > 0.f)
+        return launch_prefill<T, 128, 2, true, 2>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B,
+                                                  max_q_len, Hq, Hkv, bs, num_blocks, scale, err, stream);
+    return launch_prefill<T, 128, 2, false, 2>(out, q, k_cache, v_cache, block_tables, max_blocks, starts, cu_q, B,
+                                               max_q_len, Hq, Hkv, bs, num_blocks, scale, err, stream);
 }
 
 }  // namespace

@@ -15,18 +15,19 @@ def _max_err(out, ref):
     return (out.detach().cpu().double() - ref).abs().max().item() if ref.numel() else 0.0
 
 
-# The launch takes 128-key blocks (one CTA per SM) when the block tables can
-# hold 16k tokens or the grid has fewer than 16 * 2 * 152 CTAs, and 64-key
-# blocks (two CTAs per SM) otherwise.  The grid has B * Hkv * ceil(max_q_len /
-# (128 / G)) CTAs, so a generous max_q_len (tiles past a sequence's end exit at
-# once) selects the 64-key blocks on a small case.
+# Launch shapes: every CTA takes two query tiles of one (sequence, KV head), and
+# the grid has B * Hkv * ceil(tiles / 2) CTAs for tiles = ceil(max_q_len /
+# (128 / G)).  'narrow' gives max_q_len its exact bound (a sequence's last CTA
+# may hold a single tile); 'deep' a generous one (many CTAs past a sequence's
+# end, which exit at once: a grid many waves deep); 'wide_deep' adds block
+# tables of 16k tokens.
 WIDE_TABLE_TOKENS = 16384
 DEEP_GRID_CTAS = 16 * 2 * 152
 
 
 def _max_q(mode, mq, B, Hq, Hkv):
-    """max_q_len for a test mode: 'narrow' (the exact bound: 128-key blocks),
-    'deep' / 'wide_deep' (a grid deep enough for 64-key blocks)."""
+    """max_q_len for a test mode: 'narrow' (the exact bound), 'deep' /
+    'wide_deep' (a grid of at least DEEP_GRID_CTAS one-tile slots)."""
     if mode == "narrow":
         return mq
     positions = 128 // (Hq // Hkv)
