@@ -368,8 +368,8 @@ PKV_API pkv_status pkv_block_paged_element_offset(int64_t seq, int64_t token, in
  * values), one rounding of the output to dtype.  fp16 or bf16, head_dim 128,
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}, block_size a multiple of 16,
  * 16-byte aligned pools, q and out; other shapes or alignments return
- * PKV_ERR_UNSUPPORTED.  No workspace.  One CTA per 128 query rows of a KV
- * head, using all 512 tensor-memory columns of its SM.
+ * PKV_ERR_UNSUPPORTED.  No workspace.  One CTA per two tiles of 128 query
+ * rows of a KV head, using all 512 tensor-memory columns of its SM.
  * Device errors: starts[b] < 0 or a span needing more than max_blocks_per_seq
  * blocks gives zero rows and PKV_ERRBIT_CONTEXT; n_b < 0 or n_b > max_q_len
  * sets PKV_ERRBIT_CONTEXT (rows past max_q_len are not written); a used block

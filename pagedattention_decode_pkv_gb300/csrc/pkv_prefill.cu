@@ -10,26 +10,28 @@
 //     out[cu_q[b] + i, h] = softmax_{t <= p}(scale * q . K[t]) . V[t],
 // query head h reading KV head h / (Hq / H_kv).
 //
-// Design (fifth-generation tensor cores, FlashAttention style).  A CTA owns
-// 128 query rows of one KV head: 128 / G positions x the G query heads of the
-// group, so every K/V byte it stages serves all G heads.  Keys go by blocks of
-// KEYS (128, or 64 with two CTAs per SM; see launch_prefill_any).  Per block j:
+// Design (fifth-generation tensor cores, FlashAttention style).  A query tile
+// is 128 query rows of one KV head: 128 / G positions x the G query heads of
+// the group, so every K/V byte staged for it serves all G heads.  A CTA owns
+// two tiles of the same (sequence, KV head), and keys go by blocks of 128 (the
+// template also takes one tile per CTA and 64-key blocks; launch_prefill_any
+// has the measurements).  Per block j:
 //   * a producer warp copies K_j and V_j (the head's rows of the pages that
 //     hold keys KEYS j .. KEYS j + KEYS - 1) into a ring of stages with TMA, in
 //     chunks of gcd(block_size, KEYS) tokens per 64-dim half, 128-byte
-//     swizzled;
-//   * an MMA warp issues S_j = Q K_j^T (M = 128 rows, N = KEYS, eight K = 16
-//     steps over the head dimension) into one of two TMEM buffers, and, one
-//     block behind, O += P_{j-1} V_{j-1} (N = 128 dims, K = 16 steps over the
-//     keys; P is the A operand straight from TMEM, V the MN-major B operand)
-//     into a TMEM accumulator;
-//   * four softmax warps, one query row per thread, read the row of S_j from
-//     TMEM, mask it (causal, keys of missing pages), keep the row's running
-//     maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m) as
-//     16-bit pairs over the S_j they read.  The MMA warp writes S_{j+2} into
-//     that buffer once the PV of block j has read P_j, so the softmax never
-//     waits for a P buffer, and waits for the PV of block j - 1 only when it
-//     has to rescale O.
+//     swizzled; both tiles read every stage;
+//   * an MMA warp issues, per tile, S_j = Q K_j^T (M = 128 rows, N = KEYS,
+//     eight K = 16 steps over the head dimension) into the tile's S buffer in
+//     TMEM, and O += P_j V_j (N = 128 dims, K = 16 steps over the keys; P is
+//     the A operand straight from TMEM, V the MN-major B operand) into the
+//     tile's TMEM accumulator.  The tiles take turns: one tile's PV and next
+//     QK run while the other tile's softmax works;
+//   * four softmax warps per tile, one query row per thread, read the row of
+//     S_j from TMEM, mask it (causal, keys of missing pages), keep the row's
+//     running maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m)
+//     as 16-bit pairs over the S_j they read.  The next S of the tile goes into
+//     that buffer once the PV of block j has read P_j; the softmax waits for
+//     the PV of block j - 1 only when it has to rescale O.
 // The reference maximum m of a row moves only when the block's maximum exceeds
 // it by more than 2^8 (log2 units), and then O's row is rescaled in TMEM;
 // otherwise P is computed against the older m (values up to 256), which keeps
@@ -37,7 +39,7 @@
 // values the PV MMA multiplies, so the weights of the V rows sum to one (a
 // single dominant key gives its V row exactly, wherever m stands).  The last
 // PV's accumulator, divided by the row sum, is the output row.
-// Grid (query tiles, H_kv, B), tiles fastest: the tiles of one (sequence, KV
+// Grid (tile pairs, H_kv, B), pairs fastest: the tiles of one (sequence, KV
 // head) run side by side and read its pages while they are in L2, and the tile
 // index counts from the end of the sequence, so the longest tiles (most keys)
 // launch first.  Every wait is bounded (PKV_ERRBIT_TIMEOUT), and the CTA waits
@@ -57,7 +59,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kPreRows = 128;        // query rows (position x head) per CTA = TMEM lanes = MMA M
+constexpr int kPreRows = 128;        // query rows (position x head) per tile = TMEM lanes = MMA M
 constexpr int kQHalf = kPreRows * 128;         // one 64-dim half of the Q tile [128 rows][128 dims]
 constexpr int kQTileBytes = 2 * kQHalf;        // 32 KB
 constexpr uint64_t kPreDeadlineNs = 2000000000ull;
