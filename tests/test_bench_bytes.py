@@ -52,3 +52,21 @@ def test_decode_step_bytes_count_every_context_row_once():
     T = int(ctx.sum())
     assert b["paged_attention_decode"] == T * 2 * row + 2 * 4 * cfg.num_q_heads * cfg.head_dim * 2 + 259 * 4 + 4 * 4
     assert b["unpack_k"] == b["unpack_v"] == 2 * T * row + 259 * 4 + 5 * 12
+
+
+def test_code8_attention_bytes_count_one_byte_per_element_and_the_scales():
+    """8-bit (E4M3 / int8) attention bytes: each context row's K and V codes
+    once (one byte per element), a K and a V fp32 scale per (table entry, KV
+    head), q and out in the query dtype, the table entries and the lengths."""
+    cfg = wl.LONG_GQA_8K
+    ctx = torch.tensor([5, 0, 17, 4096], dtype=torch.int32)
+    nnz = 1 + 0 + 2 + 256
+    got = bench.code8_attention_bytes(cfg, ctx, nnz)
+    T = int(ctx.sum())
+    codes = T * 2 * cfg.num_kv_heads * cfg.head_dim
+    q_and_out = 2 * 4 * cfg.num_q_heads * cfg.head_dim * 2
+    scales = nnz * cfg.num_kv_heads * 2 * 4
+    assert got == codes + q_and_out + nnz * 4 + 4 * 4 + scales
+    # half the 16-bit attention's K/V bytes, plus the scales
+    b16 = bench.step_bytes(cfg, ctx, nnz)["paged_attention_decode"]
+    assert got - scales == b16 - codes
