@@ -80,6 +80,20 @@ PKV_API const char *pkv_last_error_string(void);
 PKV_API const char *pkv_version(void);
 
 /*
+ * pkv_selftest_wait_timeout -- failure-detection self-test of the bounded
+ * pipeline wait.  Launches one warp on `stream` that waits on an mbarrier
+ * nothing completes, with the deadline mechanism every attention-kernel stage
+ * uses (a wall-clock limit read from %globaltimer).  When the limit passes, the
+ * kernel ORs PKV_ERRBIT_TIMEOUT into *err_flag and returns; nothing faults or
+ * hangs, and the context stays usable.
+ *   err_flag    device int32, 4-byte aligned (required)
+ *   timeout_us  the wait's limit, in (0, 1000000] microseconds
+ * Returns PKV_ERR_INVALID_ARG for a NULL or misaligned flag or a limit out of
+ * range, PKV_ERR_CUDA if the launch fails.
+ */
+PKV_API pkv_status pkv_selftest_wait_timeout(int32_t *err_flag, uint32_t timeout_us, void *stream);
+
+/*
  * pkv_compute_slot_mapping -- "Walk the Shapes First" and "Step 1": the slot
  * of position p of sequence b is block_tables[b][p / block_size] * block_size
  * + p % block_size; the mapping covers only the positions written this step.

@@ -71,6 +71,7 @@ _SIGS = {
                                 _vp], ctypes.c_int),
     "pkv_paged_attention_decode_int8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
+    "pkv_selftest_wait_timeout": ([_vp, ctypes.c_uint32, _vp], ctypes.c_int),
     "pkv_allocator_create": ([_i32, _i32, _vp], ctypes.c_int),
     "pkv_allocator_destroy": ([_vp], None),
     "pkv_allocator_add_sequence": ([_vp, _i64, _i64, _vp], ctypes.c_int),
@@ -446,6 +447,16 @@ def pkv_paged_attention_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block
     """Decode attention over int8 code caches with per-(block, head) scales."""
     return _attention_codes("int8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
                             max_context_len, out, workspace, err_flag, stream)
+
+
+# ----------------------------------------------------------------------------- failure detection
+def pkv_selftest_wait_timeout(err_flag, timeout_us: int, *, stream=None):
+    """Runs the bounded pipeline wait on a barrier nothing completes: after
+    `timeout_us` the kernel sets ERRBIT_TIMEOUT in `err_flag` (device int32)."""
+    dev = _dev(err_flag)
+    _want(err_flag, torch.int32, "err_flag")
+    with torch.cuda.device(dev):
+        _check(_lib.pkv_selftest_wait_timeout(_ptr(err_flag), int(timeout_us), _stream(dev, stream)))
 
 
 # ----------------------------------------------------------------------------- host block allocator

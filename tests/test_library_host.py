@@ -220,3 +220,15 @@ def test_code8_argument_errors_are_synchronous(pkv, fmt):
     assert attend(*args, pkv.PKV_F32, None, 0, None, None) == pkv.PKV_ERR_UNSUPPORTED
     args = (None, None, None, None, None, None, None, 4, None, 0, 16, 8, 128, 16, 10, 64, 0.1)
     assert attend(*args, pkv.PKV_BF16, None, 0, None, None) == pkv.PKV_OK  # empty batch
+
+
+def test_selftest_wait_timeout_argument_errors_are_synchronous(pkv):
+    """The failure-detection self-test refuses a missing flag and limits outside
+    (0, 1 s] before any launch."""
+    lib = pkv._lib
+    P = ctypes.c_void_p(0x10000)
+    assert lib.pkv_selftest_wait_timeout(None, 1000, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_selftest_wait_timeout(ctypes.c_void_p(0x10002), 1000, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_selftest_wait_timeout(P, 0, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_selftest_wait_timeout(P, 1000001, None) == pkv.PKV_ERR_INVALID_ARG
+    assert b"timeout" in lib.pkv_last_error_string()
