@@ -29,6 +29,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -46,7 +47,8 @@ import pkv_workloads as wl  # noqa: E402
 
 METRIC = "paged decode-attention KV GB/s and % of GB300 HBM roofline; decode tokens/s"
 DEFAULT_CONFIG = "llama2-7b-layer-fp16"
-DECODE_CONFIGS = ["llama2-7b-layer-fp16", "qwen3-0.6b-gqa-bf16", "long-gqa-8k-bf16", "long-gqa-32k-bf16"]
+DECODE_CONFIGS = ["llama2-7b-layer-fp16", "qwen3-0.6b-gqa-bf16", "long-gqa-8k-bf16", "long-gqa-32k-bf16",
+                  "qwen3-0.6b-gqa-bf16-b1024"]
 CSR_CONFIGS = ["csr-prefix-bf16"]
 DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
 HBM_FALLBACK_GBS = 6800.0
@@ -62,11 +64,15 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="wall-clock budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="measure only --config (skip the other decode workloads of the per-workload block)")
     ap.add_argument("--skip-cpu-baseline", action="store_true",
                     help="omit the oracle timing (for profiler runs)")
-    ap.add_argument("--profile-calls", choices=["decode", "fp8", "int8", "prefill"], default=None,
-                    help="profiler driver: run --steps decode-attention calls (16-bit or E4M3 caches) of the "
-                         "workload back to back, eagerly, and exit without timing")
+    ap.add_argument("--profile-calls", choices=["decode", "fp8", "int8", "prefill", "unpack", "store"], default=None,
+                    help="profiler driver: run --steps calls of one kernel on the workload back to back, eagerly, "
+                         "and exit without timing (decode attention over 16-bit, E4M3 or int8 caches; the chunked "
+                         "prefill; the unpack of the batch's CSR snapshot (key role); the store of every context "
+                         "token's K/V row, as after a prefill)")
     return ap.parse_args(argv)
 
 
@@ -273,7 +279,12 @@ def packed_inputs(tensors):
 
 
 class DecodeStep:
-    """Device buffers and C-ABI argument tuples of one hot-path step."""
+    """Device buffers and C-ABI argument tuples of one hot-path step.
+
+    `copies` > 1 keeps that many copies of the caches (same block tables, same
+    values) so that a timed loop can rotate over them: consecutive calls then
+    never find the previous call's K/V in L2 when one call reads less than the
+    L2 holds a few times over."""
 
     def __init__(self, pkv, cfg: wl.DecodeConfig, seed: int, device):
         self.pkv, self.cfg, self.device = pkv, cfg, device
@@ -286,18 +297,36 @@ class DecodeStep:
         self.out = torch.empty_like(b.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         H, d = cfg.num_kv_heads, cfg.head_dim
-        self.unpacked_k = torch.empty(self.snap.total_tokens, H, d, dtype=cfg.dtype, device=device)
-        self.unpacked_v = torch.empty_like(self.unpacked_k)
+        self.unpacked_k = None  # allocated on the first step that unpacks
         self.ws_bytes = pkv.pkv_paged_attention_decode_workspace_size(B, cfg.num_q_heads, H, d, bs,
                                                                       b.max_context_len, cfg.dtype)
-        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.workspace = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
         self.plan = pkv.pkv_paged_attention_decode_plan(B, cfg.num_q_heads, H, d, bs, b.max_context_len, cfg.dtype)
         self.dt = pkv._DTYPE[cfg.dtype]
-        self.bytes = step_bytes(cfg, b.context_lens.cpu(), self.snap.nnz)
+        self.ctx_cpu = b.context_lens.cpu()
+        self.bytes = step_bytes(cfg, self.ctx_cpu, self.snap.nnz)
+        self.caches = [(b.k_cache, b.v_cache)]
+        self.codes = []  # per copy: (k codes, v codes, k scales, v scales) of the 8-bit format self.code_fmt
+        self.code_fmt = None
         # attention: main kernel + combine (always in the work-balanced schedule,
         # partition 0; with fixed partitions only when there is more than one)
         combine = self.plan[2] and self.plan[0] == 0 or self.plan[1] > 1
-        self.launches_per_step = 1 + 1 + (2 if combine else 1) + 2
+        self.attention_launches = 2 if combine else 1
+        self.launches_per_step = 1 + 1 + self.attention_launches + 2
+
+    def set_copies(self, n: int):
+        """Keep n copies of the caches (the first is the batch's own)."""
+        b = self.batch
+        self.caches = self.caches[:n]
+        while len(self.caches) < n:
+            self.caches.append((b.k_cache.clone(), b.v_cache.clone()))
+
+    def _unpack_buffers(self):
+        if self.unpacked_k is None:
+            c = self.cfg
+            self.unpacked_k = torch.empty(self.snap.total_tokens, c.num_kv_heads, c.head_dim, dtype=c.dtype,
+                                          device=self.device)
+            self.unpacked_v = torch.empty_like(self.unpacked_k)
 
     def input_sets(self):
         """Two sets of the step's per-step device inputs (and outputs), so a
@@ -311,27 +340,26 @@ class DecodeStep:
             b, s = self.batch, self.snap
             self._sets, self._packed = [], []
             for k in range(2):
-                (q, nk, nv, bt, cl, st, en, cu, sbt, sp, tp), host, dev = packed_inputs(
-                    [b.q, b.new_key, b.new_value, b.block_tables, b.context_lens, b.starts, b.ends, b.cu_new,
-                     s.block_table, s.seq_ptr, s.token_ptr])
+                (q, nk, nv, bt, cl, st, en, cu), host, dev = packed_inputs(
+                    [b.q, b.new_key, b.new_value, b.block_tables, b.context_lens, b.starts, b.ends, b.cu_new])
                 bk = replace(b, q=q, new_key=nk, new_value=nv, block_tables=bt, context_lens=cl, starts=st, ends=en,
                              cu_new=cu)
-                sk = replace(s, block_table=sbt, seq_ptr=sp, token_ptr=tp)
-                self._sets.append((bk, sk, self.out if k == 0 else torch.empty_like(self.out)))
+                self._sets.append((bk, s, self.out if k == 0 else torch.empty_like(self.out)))
                 self._packed.append((host, dev))
         return self._sets
 
-    def run_set(self, stream_ptr, k: int):
+    def run_set(self, stream_ptr, k: int, unpack: bool = True):
         """Enqueue one step on input set k (see input_sets)."""
         keep = (self.batch, self.snap, self.out)
         self.batch, self.snap, self.out = self.input_sets()[k]
         try:
-            self.run(stream_ptr)
+            self.run(stream_ptr, unpack=unpack)
         finally:
             self.batch, self.snap, self.out = keep
 
-    def run(self, stream_ptr, events=None):
-        """Enqueue one step; events (6 per step) bracket the kernels if given."""
+    def run(self, stream_ptr, events=None, unpack: bool = True):
+        """Enqueue one step; events (6 per step) bracket the kernels if given.
+        unpack=False stops after the attention (a decode step)."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
         ok = 0
@@ -346,62 +374,74 @@ class DecodeStep:
         rec(2)
         ok |= self.attention(stream_ptr)
         rec(3)
-        s = self.snap
-        for pool, dst in ((b.k_cache, self.unpacked_k), (b.v_cache, self.unpacked_v)):
-            ok |= L.pkv_unpack_block_paged(p(dst), p(pool), p(s.block_table), p(s.seq_ptr), self.pkv.PKV_U32,
-                                           p(s.token_ptr), self.B, s.nnz, c.block_size, self.nb, c.num_kv_heads,
-                                           c.head_dim, s.total_tokens, self.dt, p(self.err), stream_ptr)
-            rec(4 if dst is self.unpacked_k else 5)
+        if unpack:
+            self._unpack_buffers()
+            s = self.snap
+            for pool, dst in ((b.k_cache, self.unpacked_k), (b.v_cache, self.unpacked_v)):
+                ok |= L.pkv_unpack_block_paged(p(dst), p(pool), p(s.block_table), p(s.seq_ptr), self.pkv.PKV_U32,
+                                               p(s.token_ptr), self.B, s.nnz, c.block_size, self.nb, c.num_kv_heads,
+                                               c.head_dim, s.total_tokens, self.dt, p(self.err), stream_ptr)
+                rec(4 if dst is self.unpacked_k else 5)
         if ok != 0:
             raise RuntimeError("pkv call failed: " + L.pkv_last_error_string().decode())
 
-    def attention(self, stream_ptr) -> int:
-        """Enqueue the decode-attention call alone; returns its status."""
+    def attention(self, stream_ptr, k: int = 0) -> int:
+        """Enqueue the decode-attention call alone on cache copy k; returns its status."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
-        return L.pkv_paged_attention_decode(p(self.out), p(b.q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
+        kc, vc = self.caches[k] if k else (b.k_cache, b.v_cache)
+        return L.pkv_paged_attention_decode(p(self.out), p(b.q), p(kc), p(vc), p(b.block_tables),
                                             b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads,
                                             c.num_kv_heads, c.head_dim, c.block_size, self.nb, b.max_context_len,
                                             b.scale, self.dt, p(self.workspace), self.workspace.numel(),
                                             p(self.err), stream_ptr)
 
     def make_codes(self, fmt: str):
-        """8-bit copies of the caches (fmt "fp8" = E4M3 or "int8"; per-(block,
-        head) scales) for the 8-bit passes; one format is held at a time."""
-        self.kq = self.vq = None
+        """8-bit copies (fmt "fp8" = E4M3 or "int8"; per-(block, head) scales)
+        of every cache copy, for the 8-bit passes; one format is held at a time."""
+        self.codes = []
         quant = getattr(self.pkv, "pkv_quantize_kvcache_" + fmt)
-        self.kq, self.ks = quant(self.batch.k_cache)
-        self.vq, self.vs = quant(self.batch.v_cache)
+        kq, ks = quant(self.caches[0][0])
+        vq, vs = quant(self.caches[0][1])
+        self.codes.append((kq, vq, ks, vs))
+        for _ in range(1, len(self.caches)):
+            self.codes.append((kq.clone(), vq.clone(), ks, vs))
         self.code_fmt = fmt
 
-    def code8_attention(self, stream_ptr) -> int:
-        """Enqueue the decode-attention call over the 8-bit caches of make_codes."""
+    def drop_codes(self):
+        self.codes, self.code_fmt = [], None
+
+    def code8_attention(self, stream_ptr, k: int = 0) -> int:
+        """Enqueue the decode-attention call over the 8-bit caches of make_codes (copy k)."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        kq, vq, ks, vs = self.codes[k]
         fn = getattr(L, "pkv_paged_attention_decode_" + self.code_fmt)
-        return fn(p(self.out), p(b.q), p(self.kq), p(self.vq), p(self.ks), p(self.vs), p(b.block_tables),
+        return fn(p(self.out), p(b.q), p(kq), p(vq), p(ks), p(vs), p(b.block_tables),
                   b.block_tables.shape[1], p(b.context_lens), self.B, c.num_q_heads, c.num_kv_heads, c.head_dim,
                   c.block_size, self.nb, b.max_context_len, b.scale, self.dt, p(self.workspace),
                   self.workspace.numel(), p(self.err), stream_ptr)
 
-    def fused_step(self, stream_ptr) -> int:
-        """Enqueue the fused decode step (append the new K/V rows, then attend)."""
+    def fused_step(self, stream_ptr, k: int = 0) -> int:
+        """Enqueue the fused decode step (append the new K/V rows, then attend) on cache copy k."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
-        return L.pkv_paged_attention_decode_append(p(self.out), p(b.q), p(b.new_key), p(b.new_value), p(b.k_cache),
-                                                   p(b.v_cache), p(b.block_tables), b.block_tables.shape[1],
+        kc, vc = self.caches[k] if k else (b.k_cache, b.v_cache)
+        return L.pkv_paged_attention_decode_append(p(self.out), p(b.q), p(b.new_key), p(b.new_value), p(kc), p(vc),
+                                                   p(b.block_tables), b.block_tables.shape[1],
                                                    p(b.context_lens), self.B, c.num_q_heads, c.num_kv_heads,
                                                    c.head_dim, c.block_size, self.nb, b.max_context_len, b.scale,
                                                    self.dt, p(self.workspace), self.workspace.numel(), p(self.err),
                                                    stream_ptr)
 
-    def separate_step(self, stream_ptr) -> int:
-        """Enqueue the same step as three calls: slot mapping, store, attention."""
+    def separate_step(self, stream_ptr, k: int = 0) -> int:
+        """Enqueue the same decode step as three calls: slot mapping, store, attention (cache copy k)."""
         L, b, c, p = self.pkv._lib, self.batch, self.cfg, lambda t: t.data_ptr()
+        kc, vc = self.caches[k] if k else (b.k_cache, b.v_cache)
         st = L.pkv_compute_slot_mapping(p(b.block_tables), b.block_tables.shape[1], p(b.starts), p(b.ends),
                                         p(b.cu_new), self.B, c.block_size, self.nb, p(self.slots), self.B,
                                         p(self.err), stream_ptr)
-        st |= L.pkv_store_kvcache(p(b.new_key), p(b.new_value), p(b.k_cache), p(b.v_cache), p(self.slots), self.B,
+        st |= L.pkv_store_kvcache(p(b.new_key), p(b.new_value), p(kc), p(vc), p(self.slots), self.B,
                                   c.num_kv_heads, c.head_dim, self.nb * c.block_size, self.dt, p(self.err),
                                   stream_ptr)
-        return st | self.attention(stream_ptr)
+        return st | self.attention(stream_ptr, k)
 
     # per-step host inputs for the end-to-end measurement
     def host_inputs(self, k: int = 0):
@@ -411,6 +451,9 @@ class DecodeStep:
 
 
 STEPS_PER_GRAPH = 10
+MIN_WINDOW_S = 1.0      # device time of every throughput window (clock samples every 100 ms fall inside)
+GRAPH_TARGET_MS = 2.0   # calls per graph: about this much device time, so graph boundaries are rare
+COLD_CALLS = 20         # per-call (cold) timings per workload
 
 
 def capture_step_graph(step: DecodeStep, n_steps: int):
@@ -424,7 +467,7 @@ def capture_step_graph(step: DecodeStep, n_steps: int):
     return g
 
 
-def capture_pipelined_io_graph(step: DecodeStep, n_steps: int, io):
+def capture_pipelined_io_graph(step, n_steps: int, io, unpack: bool = True):
     """CUDA graph of n_steps steps as a decode loop with host inputs runs them:
     step i reads input set i % 2, whose host->device copies run on a second
     stream as soon as step i - 2 is done with that set (overlapping step
@@ -453,7 +496,10 @@ def capture_pipelined_io_graph(step: DecodeStep, n_steps: int, io):
             comp.wait_event(ready[i])
             if i >= 2:
                 comp.wait_event(drained[i - 2])  # output k has been read back
-            step.run_set(ptr, k)
+            if unpack:
+                step.run_set(ptr, k)
+            else:
+                step.run_set(ptr, k, unpack=False)
             done[i].record(comp)
             with torch.cuda.stream(side):
                 side.wait_event(done[i])
@@ -464,7 +510,7 @@ def capture_pipelined_io_graph(step: DecodeStep, n_steps: int, io):
     return g
 
 
-def time_graphs(step: DecodeStep, steps: int, world: int, io=None):
+def time_graphs(step, steps: int, world: int, io=None):
     """Replays graphs of STEPS_PER_GRAPH steps (and single steps for the
     remainder) so that exactly `steps` steps run between the two events; with
     io, the graphs are the pipelined end-to-end loop."""
@@ -493,19 +539,116 @@ def time_graphs(step: DecodeStep, steps: int, world: int, io=None):
     return e0.elapsed_time(e1), (t_wall0, t_wall1)
 
 
+def replay_window(g, units_per_replay: int, world: int, min_s: float = MIN_WINDOW_S, min_units: int = 0):
+    """Replays graph g back to back until at least min_s seconds of device time
+    (and min_units units) have run between two CUDA events.  Returns (ms per
+    unit, units timed, (wall start, wall end))."""
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1), 1e-3)
+    n = max(1, math.ceil(min_s * 1e3 / est), math.ceil(min_units / units_per_replay))
+    barrier(world)
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    barrier(world)
+    return e0.elapsed_time(e1) / (n * units_per_replay), n * units_per_replay, (tw0, tw1)
+
+
+def capture_calls(step, what, n_calls: int, ncopies: int = 1):
+    """CUDA graph of n_calls calls of what(stream_ptr, copy), copy = i % ncopies
+    (launches chained by programmatic dependent launch)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for i in range(n_calls):
+            if what(ptr, i % ncopies) != 0:
+                raise RuntimeError("pkv call failed: " + step.pkv._lib.pkv_last_error_string().decode())
+    return g
+
+
+def calls_per_graph(est_ms: float, ncopies: int) -> int:
+    """About GRAPH_TARGET_MS of calls per graph (8 to 64), a multiple of ncopies."""
+    n = min(64, max(8, math.ceil(GRAPH_TARGET_MS / max(est_ms, 1e-3))))
+    return (n + ncopies - 1) // ncopies * ncopies
+
+
+def time_sustained(step, what, world: int, est_ms: float, ncopies: int = 1, min_s: float = MIN_WINDOW_S,
+                   min_calls: int = 0):
+    """Calls of `what` back to back, as a decode loop issues them, rotating
+    over ncopies cache copies, for at least min_s seconds of device time.
+    Returns (ms per call, calls timed, calls per graph, wall window)."""
+    per = calls_per_graph(est_ms, ncopies)
+    g = capture_calls(step, what, per, ncopies)
+    ms, calls, win = replay_window(g, per, world, min_s, min_calls)
+    return ms, calls, per, win
+
+
+_EVICT = {}
+
+
+def evict_buffer(device):
+    """A 512 MB buffer whose read evicts the L2 (and writes back its dirty lines)."""
+    if device not in _EVICT:
+        _EVICT[device] = (torch.ones(L2_EVICT_BYTES // 4, dtype=torch.float32, device=device),
+                          torch.empty((), dtype=torch.float32, device=device))
+    return _EVICT[device]
+
+
+def time_cold_calls(step, what, n: int, world: int, stream):
+    """One call at a time between two CUDA events on the launching stream,
+    each after a 512 MB read (outside the events) that evicts the L2: launch
+    latency and a cold L2 included.  Returns (median ms, mean ms)."""
+    evict, sink = evict_buffer(step.device)
+    ptr = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            what(ptr, 0)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        barrier(world)
+        for a, b in evs:
+            torch.sum(evict, dim=0, out=sink)
+            a.record()
+            if what(ptr, 0) != 0:
+                raise RuntimeError("pkv call failed: " + step.pkv._lib.pkv_last_error_string().decode())
+            b.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    t = [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(t), statistics.fmean(t)
+
+
 L2_EVICT_BYTES = 512 << 20  # > 4x the 129 MB L2
 
 
+def l2_bytes(device) -> int:
+    try:
+        return int(torch.cuda.get_device_properties(device).L2_cache_size) or 129 * 10 ** 6
+    except Exception:
+        return 129 * 10 ** 6
+
+
 def time_kernels(step: DecodeStep, steps: int, world: int, stream):
-    """Second pass: eager launches with CUDA events between the kernels on the
-    launching stream.  Before every step (outside the events) a 512 MB buffer
-    is read, which evicts the L2 and writes back the previous step's dirty
-    lines, so no kernel is charged for another kernel's deferred writes.  The
-    events cut the launch chaining, so these per-kernel times are slightly
+    """Per-kernel pass: eager launches with CUDA events between the kernels on
+    the launching stream.  Before every step (outside the events) a 512 MB
+    buffer is read, which evicts the L2 and writes back the previous step's
+    dirty lines, so no kernel is charged for another kernel's deferred writes.
+    The events cut the launch chaining, so these per-kernel times are slightly
     pessimistic."""
     ptr = ctypes.c_void_p(stream.cuda_stream)
-    evict = torch.ones(L2_EVICT_BYTES // 4, dtype=torch.float32, device=step.device)
-    sink = torch.empty((), dtype=torch.float32, device=step.device)
+    evict, sink = evict_buffer(step.device)
     with torch.cuda.stream(stream):
         for _ in range(3):
             step.run(ptr)
@@ -521,40 +664,6 @@ def time_kernels(step: DecodeStep, steps: int, world: int, stream):
     return {n: statistics.fmean(e[k].elapsed_time(e[k + 1]) for e in evs) for k, n in enumerate(names)}
 
 
-ATTN_PER_GRAPH = 10
-
-
-def time_attention_sustained(step: DecodeStep, calls: int, world: int, what=None):
-    """Third pass: decode-attention calls back to back, as a decode loop issues
-    them, in CUDA graphs of ATTN_PER_GRAPH calls (launches chained by
-    programmatic dependent launch); `calls` calls (rounded up to whole graphs)
-    between two CUDA events.  Every bench workload reads more K/V per call than
-    the 129 MB L2 holds, and the K/V loads carry an evict-first L2 policy, so no
-    flush is needed.  `what` (default step.attention) enqueues one call.
-    Returns (ms per call, calls timed)."""
-    what = what or step.attention
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        for _ in range(ATTN_PER_GRAPH):
-            if what(ptr) != 0:
-                raise RuntimeError("pkv call failed: " + step.pkv._lib.pkv_last_error_string().decode())
-    for _ in range(2):
-        g.replay()
-    torch.cuda.synchronize()
-    n = max(1, (calls + ATTN_PER_GRAPH - 1) // ATTN_PER_GRAPH)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    return e0.elapsed_time(e1) / (n * ATTN_PER_GRAPH), n * ATTN_PER_GRAPH
-
-
 def time_host_allocator(pkv, step: DecodeStep, steps: int = 200):
     """Host block allocator on the workload's pool: the batch's sequences are
     admitted with their context lengths, then every step appends one token to
@@ -563,7 +672,7 @@ def time_host_allocator(pkv, step: DecodeStep, steps: int = 200):
     small for the extra tokens."""
     cfg = step.cfg
     a = pkv.pkv_allocator_create(step.nb, cfg.block_size)
-    for i, n in enumerate(step.batch.context_lens.cpu().tolist()):
+    for i, n in enumerate(step.ctx_cpu.tolist()):
         pkv.pkv_allocator_add_sequence(a, i, n)
     if pkv.pkv_allocator_stats(a)["free"] < step.B * (steps // cfg.block_size + 1):
         return None
@@ -583,10 +692,11 @@ def prefill_call(step: DecodeStep):
     """Chunked prefill on the workload's own cache: every sequence's last
     min(ctx, 512) positions are taken as the new tokens of a prefill chunk
     (fresh random queries) and attend causally over their whole context.
-    Returns (enqueue function, algorithmic FLOPs per call, queries): 2 d flops
-    for q.k and 2 d for p.v per (query, key) pair and query head."""
+    Returns (enqueue function (stream_ptr, copy), algorithmic FLOPs per call,
+    queries): 2 d flops for q.k and 2 d for p.v per (query, key) pair and
+    query head."""
     pkv, b, c = step.pkv, step.batch, step.cfg
-    ctx = b.context_lens.cpu().to(torch.int64)
+    ctx = step.ctx_cpu.to(torch.int64)
     ns = ctx.clamp(max=PREFILL_NEW_TOKENS)
     starts = (ctx - ns).to(torch.int32)
     cu = torch.zeros(step.B + 1, dtype=torch.int32)
@@ -601,7 +711,7 @@ def prefill_call(step: DecodeStep):
     L, p = pkv._lib, lambda t: t.data_ptr()
     mq = int(ns.max())
 
-    def call(ptr):
+    def call(ptr, k=0):
         return L.pkv_paged_attention_prefill(p(out), p(q), p(b.k_cache), p(b.v_cache), p(b.block_tables),
                                              b.block_tables.shape[1], p(st), p(cud), step.B, mq, c.num_q_heads,
                                              c.num_kv_heads, c.head_dim, c.block_size, step.nb, b.scale, step.dt,
@@ -611,14 +721,7 @@ def prefill_call(step: DecodeStep):
     return call, flops, nq
 
 
-def time_prefill(step: DecodeStep, calls: int, world: int):
-    """prefill_call back to back in CUDA graphs: (ms per call, FLOPs per call, queries)."""
-    call, flops, nq = prefill_call(step)
-    ms, _ = time_attention_sustained(step, calls, world, call)
-    return ms, flops, nq
-
-
-def e2e_io(step: DecodeStep):
+def e2e_io(step):
     """Pinned host buffers of the end-to-end pass, per input set."""
     pairs = [step.host_inputs(0), step.host_inputs(1)]
     out_host = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
@@ -631,8 +734,8 @@ def e2e_io(step: DecodeStep):
 # ----------------------------------------------------------------------------- oracle sample
 def oracle_sample_inputs(batch: wl.DecodeBatch, seqs):
     """The chosen sequences with only the blocks they use, on the CPU (block
-    ids renumbered into a compact pool); plus their CSR view."""
-    cfg, bs = batch.cfg, batch.cfg.block_size
+    ids renumbered into a compact pool)."""
+    bs = batch.cfg.block_size
     ctx = batch.context_lens.cpu()[seqs]
     tables = batch.block_tables.cpu()[seqs]
     nblk = [(int(c) + bs - 1) // bs for c in ctx]
@@ -643,29 +746,19 @@ def oracle_sample_inputs(batch: wl.DecodeBatch, seqs):
         new_tables[i, :n] = torch.tensor([remap[int(x)] for x in tables[i, :n]], dtype=torch.int32)
     kc = batch.k_cache[used.to(batch.k_cache.device)].cpu()
     vc = batch.v_cache[used.to(batch.v_cache.device)].cpu()
-    seq_ptr = torch.zeros(len(seqs) + 1, dtype=torch.int64)
-    seq_ptr[1:] = torch.cumsum(torch.tensor(nblk), 0)
-    token_ptr = torch.zeros(len(seqs) + 1, dtype=torch.int64)
-    token_ptr[1:] = torch.cumsum(ctx.to(torch.int64), 0)
-    csr_bt = torch.cat([new_tables[i, :n] for i, n in enumerate(nblk)])
-    return dict(q=batch.q.cpu()[seqs], kc=kc, vc=vc, tables=new_tables, ctx=ctx,
-                starts=batch.starts.cpu()[seqs], ends=batch.ends.cpu()[seqs],
-                key=batch.new_key.cpu()[seqs], value=batch.new_value.cpu()[seqs], nb=len(used),
-                seq_ptr=seq_ptr.to(torch.int32), token_ptr=token_ptr, csr_bt=csr_bt, nnz=len(used))
+    return dict(q=batch.q.cpu()[seqs], kc=kc, vc=vc, tables=new_tables, ctx=ctx, nnz=len(used))
 
 
-def oracle_step(orc, s, cfg, scale):
-    """The step's computations, done by the oracle on one sample."""
-    slots, _ = orc.compute_slot_mapping(s["tables"], s["starts"], s["ends"], cfg.block_size, s["nb"])
-    kc, vc, _ = orc.store_kvcache(s["key"], s["value"], s["kc"], s["vc"], slots)
-    orc.paged_attention_decode(s["q"], kc, vc, s["tables"], s["ctx"], scale)
-    for pool in (kc, vc):
-        orc.unpack_block_paged(pool, s["csr_bt"], s["seq_ptr"], s["token_ptr"], index_dtype=torch.int32)
+def oracle_attention(orc, s, scale):
+    """The decode attention of one sample, computed by the oracle."""
+    orc.paged_attention_decode(s["q"], s["kc"], s["vc"], s["tables"], s["ctx"], scale)
 
 
 def cpu_sample_run(batch, budget_s: float, start_seq: int = 0, max_seqs: int | None = None):
-    """Run the oracle over sequences start_seq, start_seq+1, ... until the
-    budget is spent; returns (GB/s, seconds, number of sequences, bytes)."""
+    """Decode attention by the oracle over sequences start_seq, start_seq+1, ...
+    (one at a time, inputs gathered outside the clock) until the budget is
+    spent; returns (KV GB/s, seconds, number of sequences, bytes), bytes being
+    the attention's algorithmic bytes of those sequences."""
     import oracle as orc
 
     orc.build()
@@ -675,18 +768,18 @@ def cpu_sample_run(batch, budget_s: float, start_seq: int = 0, max_seqs: int | N
         seq = [(start_seq + done) % B]
         s = oracle_sample_inputs(batch, seq)
         t0 = time.perf_counter()
-        oracle_step(orc, s, cfg, batch.scale)
+        oracle_attention(orc, s, batch.scale)
         t_total += time.perf_counter() - t0
-        nbytes += sum(step_bytes(cfg, s["ctx"], s["nnz"]).values())
+        nbytes += step_bytes(cfg, s["ctx"], s["nnz"])["paged_attention_decode"]
         done += 1
     return nbytes / t_total / 1e9, t_total, done, nbytes
 
 
 def cpu_all_cores_run(batch, max_seqs: int):
-    """The same oracle step on the first max_seqs sequences, one sequence per
-    task on a pool of host threads (the C oracle runs outside the GIL); inputs
-    are prepared before the clock starts.  Returns (GB/s, seconds, sequences,
-    bytes, threads)."""
+    """The same oracle attention on the first max_seqs sequences, one sequence
+    per task on a pool of host threads (the C oracle runs outside the GIL);
+    inputs are prepared before the clock starts.  Returns (GB/s, seconds,
+    sequences, bytes, threads)."""
     import oracle as orc
     from concurrent.futures import ThreadPoolExecutor
 
@@ -697,15 +790,114 @@ def cpu_all_cores_run(batch, max_seqs: int):
     threads = max(1, min(len(os.sched_getaffinity(0)), n))
     with ThreadPoolExecutor(max_workers=threads) as pool:
         t0 = time.perf_counter()
-        list(pool.map(lambda smp: oracle_step(orc, smp, cfg, batch.scale), samples))
+        list(pool.map(lambda smp: oracle_attention(orc, smp, batch.scale), samples))
         secs = time.perf_counter() - t0
-    nbytes = sum(sum(step_bytes(cfg, smp["ctx"], smp["nnz"]).values()) for smp in samples)
+    nbytes = sum(step_bytes(cfg, smp["ctx"], smp["nnz"])["paged_attention_decode"] for smp in samples)
     return nbytes / secs / 1e9, secs, n, nbytes, threads
+
+
+# ----------------------------------------------------------------------------- the workload description
+def workload_config(cfg: wl.DecodeConfig, ctx: torch.Tensor, world: int) -> dict:
+    """The `config` object of a decode workload: the same dict on both arms."""
+    es = torch.tensor([], dtype=cfg.dtype).element_size()
+    tokens = int(ctx.to(torch.int64).sum())
+    kv = tokens * 2 * cfg.num_kv_heads * cfg.head_dim * es
+    return {
+        "workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
+        "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
+        "block_size": cfg.block_size, "context_tokens": tokens, "max_context_len": int(ctx.max()),
+        "kv_bytes_per_call": kv,
+        "l2": f"{kv / 1e9:.2f} GB of K/V per decode-attention call vs the 129 MB L2: no flush; workloads under "
+              "4x L2 rotate over cache copies",
+        "parallelism": f"replicas x{world} (independent sequences per rank, no data-path collective)",
+    }
+
+
+DEFAULT_SWEEP = ["llama2-7b-layer-fp16", "qwen3-0.6b-gqa-bf16", "long-gqa-8k-bf16", "long-gqa-32k-bf16",
+                 "qwen3-0.6b-gqa-bf16-b1024"]
+
+
+def _clk(summary: dict) -> dict:
+    return {k: summary.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples_in_timed_region", "power_w_max")}
+
+
+def measure_decode_workload(pkv, step: DecodeStep, world: int, device, stream, sampler) -> dict:
+    """Decode attention on one workload: cold per-call latency, sustained
+    calls (rotating over cache copies when a call reads under 4x L2), the
+    fused decode step and the 8-bit caches, each sustained window at least
+    MIN_WINDOW_S of device time."""
+    cfg = step.cfg
+    peak, _ = measured_hbm_peak()
+    l2 = l2_bytes(device)
+    kv_alg = step.bytes["paged_attention_decode"]
+    ncopies = 1 if kv_alg >= 4 * l2 else max(4, math.ceil(4 * l2 / kv_alg))
+    step.set_copies(ncopies)
+    rmax = lambda x: reduce_max(x, world, device)  # noqa: E731
+    rsum = lambda x: reduce_sum(x, world, device)  # noqa: E731
+    all_bytes = rsum(kv_alg)
+    B_all = rsum(cfg.batch)
+
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9
+
+    res = {"workload": cfg.name, "batch": cfg.batch, "context_tokens": int(step.ctx_cpu.to(torch.int64).sum()),
+           "attention_bytes_per_call": kv_alg, "cache_copies": ncopies,
+           "plan": {"partition_tokens": step.plan[0], "partitions_or_ctas": step.plan[1],
+                    "tensor_core_path": step.plan[2],
+                    "schedule": "work-balanced" if step.plan[2] and step.plan[0] == 0 else "fixed partitions"}}
+    cold_med, cold_mean = time_cold_calls(step, step.attention, COLD_CALLS, world, stream)
+    cold_med, cold_mean = rmax(cold_med), rmax(cold_mean)
+    ms, calls, per, (t0, t1) = time_sustained(step, step.attention, world, cold_med, ncopies)
+    clk = sampler.summary(t0, t1)
+    ms = rmax(ms)
+    a = gbs(all_bytes, ms)
+    c = gbs(all_bytes, cold_med)
+    res["attention"] = {
+        "sustained": {"us": round(ms * 1e3, 2), "gbs": round(a, 1), "frac": round(a / peak, 4),
+                      "frac_of_8000_nominal": round(a / 8000.0, 4), "calls": calls, "calls_per_graph": per,
+                      "clocks": _clk(clk)},
+        "per_call": {"us": round(cold_med * 1e3, 2), "us_mean": round(cold_mean * 1e3, 2), "gbs": round(c, 1),
+                     "frac": round(c / peak, 4), "frac_of_8000_nominal": round(c / 8000.0, 4),
+                     "calls": COLD_CALLS},
+        "tokens_per_s": round(B_all / (ms * 1e-3), 1)}
+    fms, fcalls, _, (t0, t1) = time_sustained(step, step.fused_step, world, ms, ncopies)
+    fms = rmax(fms)
+    res["decode_step_fused"] = {"us": round(fms * 1e3, 2), "tokens_per_s": round(B_all / (fms * 1e-3), 1),
+                                "kv_gbs": round(gbs(all_bytes, fms), 1), "calls": fcalls,
+                                "clocks": _clk(sampler.summary(t0, t1))}
+    c8_bytes = rsum(code8_attention_bytes(cfg, step.ctx_cpu, step.snap.nnz))
+    for fmt in ("fp8", "int8"):
+        step.make_codes(fmt)
+        ptr = ctypes.c_void_p(stream.cuda_stream)
+        with torch.cuda.stream(stream):
+            st = step.code8_attention(ptr, 0)
+        torch.cuda.synchronize()
+        if st != 0:
+            res[fmt] = {"unsupported": pkv._lib.pkv_last_error_string().decode()}
+            step.drop_codes()
+            continue
+        c8_local = code8_attention_bytes(cfg, step.ctx_cpu, step.snap.nnz)
+        n8 = 1 if c8_local >= 4 * l2 else max(4, math.ceil(4 * l2 / c8_local))
+        m8, calls8, _, (t0, t1) = time_sustained(step, step.code8_attention, world, ms / 2, min(n8, len(step.codes)))
+        m8 = rmax(m8)
+        g8 = gbs(c8_bytes, m8)
+        res[fmt] = {"us": round(m8 * 1e3, 2), "gbs": round(g8, 1), "frac": round(g8 / peak, 4),
+                    "frac_of_8000_nominal": round(g8 / 8000.0, 4), "tokens_per_s": round(B_all / (m8 * 1e-3), 1),
+                    "speedup_vs_16bit": round(ms / m8, 3), "calls": calls8,
+                    "clocks": _clk(sampler.summary(t0, t1))}
+        step.drop_codes()
+    step.set_copies(1)
+    torch.cuda.synchronize()
+    err = int(step.err.item())
+    if err:
+        raise RuntimeError(f"device error bits {err:#x} during the {cfg.name} passes")
+    return res
 
 
 # ----------------------------------------------------------------------------- arms
 def run_reference(args, world, rank):
-    """The oracle as it stands, on the host cores, one bounded sample per step."""
+    """The oracle as it stands, on the host cores: decode attention of a
+    bounded sample of the workload's sequences per step."""
     if rank != 0:
         return 0
     cfg = wl.CONFIGS[args.config]
@@ -721,15 +913,14 @@ def run_reference(args, world, rank):
         t += dt
         nbytes += nb
     value = nbytes / t / 1e9
-    sample = (f"{seqs_per_step} sequences of the {cfg.name} batch per step (slot mapping, store, decode "
-              f"attention, K/V unpack of those sequences), single-threaded C oracle in binary64")
+    sample = (f"{seqs_per_step} sequences of the {cfg.name} batch per step, decode attention of each over its "
+              "whole paged context; single-threaded C oracle in binary64")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
-        "data": "synthetic (seeded N(0,1), random block permutation)",
-        "config": {"workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
-                   "l2": "bounded CPU sample; no GPU work"},
+        "data": "synthetic (seeded N(0,1) K/V/q, random non-contiguous block permutation)",
+        "config": workload_config(cfg, batch.context_lens.cpu(), world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -745,6 +936,8 @@ def run_ours(args, world, rank, local):
     cfg = wl.CONFIGS[args.config]
     step = DecodeStep(pkv, cfg, seed=args.seed + rank, device=device)
     stream = torch.cuda.Stream(device)
+    rmax = lambda x: reduce_max(x, world, device)  # noqa: E731
+    rsum = lambda x: reduce_sum(x, world, device)  # noqa: E731
 
     # eager warm-up: first-use set-up of the library, then the graphs
     ptr = ctypes.c_void_p(stream.cuda_stream)
@@ -756,118 +949,106 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    total_ms, (tw0, tw1) = time_graphs(step, args.steps, world)
-    clocks = sampler.summary(tw0, tw1)
-    sampler.stop()
+    try:
+        # 1. exactly `steps` hot-path steps (slot mapping, store, attention, unpack K and V)
+        total_ms, (tw0, tw1) = time_graphs(step, args.steps, world)
+        clocks_steps = sampler.summary(tw0, tw1)
+        torch.cuda.synchronize()
+        if int(step.err.item()):
+            raise RuntimeError(f"device error bits {int(step.err.item()):#x} during the benchmark")
+        # 2. the headline: decode-attention calls back to back for >= 1 s
+        headline = measure_decode_workload(pkv, step, world, device, stream, sampler)
+        # 3. the other decode workloads, the same passes
+        sweep = {cfg.name: headline}
+        if not args.no_sweep:
+            for name in DEFAULT_SWEEP:
+                if name == cfg.name:
+                    continue
+                other = DecodeStep(pkv, wl.CONFIGS[name], seed=args.seed + rank, device=device)
+                with torch.cuda.stream(stream):
+                    other.attention(ptr)
+                torch.cuda.synchronize()
+                sweep[name] = measure_decode_workload(pkv, other, world, device, stream, sampler)
+                del other
+                torch.cuda.empty_cache()
+        # 4. per-kernel times of the headline step, the separate decode step,
+        #    the prefill, the end-to-end decode loop
+        per = time_kernels(step, max(args.steps, COLD_CALLS), world, stream)
+        sep_ms, _, _, _ = time_sustained(step, step.separate_step, world, per["paged_attention_decode"])
+        sep_ms = rmax(sep_ms)
+        call, pre_flops, pre_q = prefill_call(step)
+        pre_ms, pre_calls, _, (t0, t1) = time_sustained(step, call, world, 1.5)
+        pre_clk = sampler.summary(t0, t1)
+        pre_ms = rmax(pre_ms)
+        io, h2d, d2h = e2e_io(step)
+        g_e2e = capture_pipelined_io_graph(step, STEPS_PER_GRAPH, io, unpack=False)
+        e2e_ms, e2e_steps, (t0, t1) = replay_window(g_e2e, STEPS_PER_GRAPH, world)
+        e2e_clk = sampler.summary(t0, t1)
+        e2e_ms = rmax(e2e_ms)
+    finally:
+        sampler.stop()
     torch.cuda.synchronize()
-    err = int(step.err.item())
-    if err:
-        raise RuntimeError(f"device error bits {err:#x} during the benchmark")
-
-    per = time_kernels(step, args.steps, world, stream)
-    sus_ms, sus_calls = time_attention_sustained(step, args.steps, world)
-    fused_ms, _ = time_attention_sustained(step, args.steps, world, step.fused_step)
-    sep_ms, _ = time_attention_sustained(step, args.steps, world, step.separate_step)
-    code8_bytes = code8_attention_bytes(cfg, step.batch.context_lens.cpu(), step.snap.nnz)
-    code8 = {}
-    for fmt in ("fp8", "int8"):
-        step.make_codes(fmt)
-        ms, _ = time_attention_sustained(step, args.steps, world, step.code8_attention)
-        code8[fmt] = (reduce_max(ms, world, device), reduce_sum(cfg.batch / (ms * 1e-3), world, device))
-    step.kq = step.vq = None
-    pre_ms, pre_flops, pre_q = time_prefill(step, max(10, args.steps // 20), world)
-    pre_ms = reduce_max(pre_ms, world, device)
+    if int(step.err.item()):
+        raise RuntimeError(f"device error bits {int(step.err.item()):#x} during the benchmark")
     alloc_us = time_host_allocator(pkv, step)
-    fused_tok_s = reduce_sum(cfg.batch / (fused_ms * 1e-3), world, device)
-    fused_ms = reduce_max(fused_ms, world, device)
-    sep_ms = reduce_max(sep_ms, world, device)
-    io, h2d, d2h = e2e_io(step)
-    e2e_ms, _ = time_graphs(step, args.steps, world, io)
-
-    step_total_bytes = sum(step.bytes.values())
-    total_ms_max = reduce_max(total_ms, world, device)
-    e2e_ms_max = reduce_max(e2e_ms, world, device)
-    all_bytes = reduce_sum(step_total_bytes * args.steps, world, device)
-    value = all_bytes / (total_ms_max * 1e-3) / 1e9
-    e2e_value = all_bytes / (e2e_ms_max * 1e-3) / 1e9
 
     peak, peak_kind = measured_hbm_peak()
     bf16_peak, bf16_kind = measured_bf16_peak()
-    attn_ms = per["paged_attention_decode"]
-    attn_percall_gbs = step.bytes["paged_attention_decode"] / (attn_ms * 1e-3) / 1e9
-    sus_ms = reduce_max(sus_ms, world, device)
-    attn_gbs = step.bytes["paged_attention_decode"] / (sus_ms * 1e-3) / 1e9
-    units = int(step.batch.context_lens.to(torch.int64).sum())  # tokens of context per launch
+    attn_bytes = step.bytes["paged_attention_decode"]
+    all_attn_bytes = rsum(attn_bytes)
+    h_sus = headline["attention"]["sustained"]
+    value = h_sus["gbs"]
+    step_total_bytes = sum(step.bytes.values())
+    total_ms_max = rmax(total_ms)
+    step_gbs = rsum(step_total_bytes * args.steps) / (total_ms_max * 1e-3) / 1e9
+    e2e_value = all_attn_bytes / (e2e_ms * 1e-3) / 1e9
+    units = int(step.ctx_cpu.to(torch.int64).sum())  # tokens of context per launch
     traffic = profiled_traffic("paged_attention_decode", units)
-    decode_ms = per["slot_mapping"] + per["store_kvcache"] + attn_ms
-    decode_tok_s = reduce_sum(cfg.batch / (decode_ms * 1e-3), world, device)
+    roof_calls = h_sus["calls"]
 
     cpu_baseline = None
     if world == 1 and not args.skip_cpu_baseline:
         gbs, secs, nseq, nbytes = cpu_sample_run(step.batch, args.cpu_budget_s)
         cpu_baseline = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                        "sample": f"first {nseq} of {cfg.batch} sequences of the batch, whole step per sequence "
-                                  f"({nbytes / 1e9:.3f} GB of step bytes in {secs:.1f} s), single-threaded C "
-                                  f"oracle in binary64"}
+                        "sample": f"decode attention of the first {nseq} of {cfg.batch} sequences of the batch, one "
+                                  f"sequence at a time ({nbytes / 1e9:.3f} GB of attention bytes in {secs:.1f} s), "
+                                  "single-threaded C oracle in binary64"}
         mgbs, msecs, mseq, mbytes, threads = cpu_all_cores_run(step.batch, max(nseq, 1))
         cpu_baseline["all_cores"] = {
             "value": round(mgbs, 4), "unit": "GB/s", "cores": threads,
-            "sample": f"the same {mseq} sequences ({mbytes / 1e9:.3f} GB of step bytes in {msecs:.2f} s), one "
-                      f"sequence per task on {threads} host threads"}
+            "sample": f"the same {mseq} sequences ({mbytes / 1e9:.3f} GB in {msecs:.2f} s), one sequence per task "
+                      f"on {threads} host threads"}
 
     if rank != 0:
         return 0
     kernel_us = {k: round(v * 1e3, 2) for k, v in per.items()}
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(total_ms_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
         "data": "synthetic (seeded N(0,1) K/V/q, random non-contiguous block permutation)",
-        "config": {
-            "workload": cfg.name, "description": cfg.description, "batch": cfg.batch,
-            "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads, "head_dim": cfg.head_dim,
-            "block_size": cfg.block_size, "context_tokens": units, "max_context_len": step.batch.max_context_len,
-            "decode_partition_tokens": step.plan[0], "decode_partitions": step.plan[1],
-            "tensor_core_path": step.plan[2],
-            "step": "slot mapping + store_kvcache + paged_attention_decode (+combine) + unpack K and V",
-            "step_bytes": step_total_bytes,
-            "l2": f"inputs larger than L2: {step.bytes['paged_attention_decode'] / 1e9:.2f} GB of KV per step "
-                  f"vs 129 MB L2; no flush",
-            "parallelism": f"replicas x{world} (independent sequences per rank, no data-path collective)",
-        },
-        "decode_tokens_per_s": round(decode_tok_s, 1),
+        "config": workload_config(cfg, step.ctx_cpu, world),
+        "plan": headline["plan"],
+        "decode_tokens_per_s": headline["decode_step_fused"]["tokens_per_s"],
+        "attention_tokens_per_s": headline["attention"]["tokens_per_s"],
+        "step_gbs": round(step_gbs, 2),
+        "step_bytes": step_total_bytes,
         "kernel_us": kernel_us,
         "kernel_gbs": {k: round(step.bytes[k] / (per[k] * 1e-3) / 1e9, 1) for k in per},
-        "roofline": {"kernel": "pkv_paged_attention_decode (main pass + combine)", "bound": "hbm",
-                     "achieved": round(attn_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(attn_gbs / peak, 4), "peak_kind": peak_kind,
-                     "frac_of_8000_nominal": round(attn_gbs / 8000.0, 4),
+        "roofline": {"kernel": "pkv_paged_attention_decode (main pass + merge)", "bound": "hbm",
+                     "achieved": value, "peak": peak, "unit": "GB/s", "frac": round(value / peak, 4),
+                     "peak_kind": peak_kind, "frac_of_8000_nominal": round(value / 8000.0, 4),
                      "traffic": None if traffic is None else round(traffic),
-                     "us_per_call": round(sus_ms * 1e3, 2), "calls_timed": sus_calls,
-                     "per_call_latency": {"us": round(attn_ms * 1e3, 2), "achieved": round(attn_percall_gbs, 1),
-                                          "frac": round(attn_percall_gbs / peak, 4),
-                                          "frac_of_8000_nominal": round(attn_percall_gbs / 8000.0, 4)}},
-        "decode_step_fused": {
-            "what": "one decode step (append every sequence's new K/V row at position ctx-1, then attention over "
-                    "the whole context) back to back in CUDA graphs, as pkv_paged_attention_decode_append vs "
-                    "pkv_compute_slot_mapping + pkv_store_kvcache + pkv_paged_attention_decode",
-            "fused_us": round(fused_ms * 1e3, 2),
-            "separate_us": round(sep_ms * 1e3, 2),
-            "fused_tokens_per_s": round(fused_tok_s, 1),
-            "fused_kv_gbs": round(step.bytes["paged_attention_decode"] / (fused_ms * 1e-3) / 1e9, 1)},
-        **{f"decode_{fmt}": {
-            "what": f"pkv_paged_attention_decode_{fmt} over {name} copies of the caches (one fp32 scale per block "
-                    "and KV head), back to back in CUDA graphs like the roofline pass",
-            "us_per_call": round(code8[fmt][0] * 1e3, 2),
-            "gbs": round(code8_bytes / (code8[fmt][0] * 1e-3) / 1e9, 1),
-            "frac_of_peak": round(code8_bytes / (code8[fmt][0] * 1e-3) / 1e9 / peak, 4),
-            "tokens_per_s": round(code8[fmt][1], 1),
-            "speedup_vs_16bit": round(sus_ms / code8[fmt][0], 3)}
-           for fmt, name in (("fp8", "E4M3"), ("int8", "int8"))},
+                     "algorithmic_bytes_per_call": attn_bytes,
+                     "us_per_call": h_sus["us"], "calls_timed": roof_calls,
+                     "per_call_latency": headline["attention"]["per_call"]},
+        "configs": sweep,
+        "decode_step_separate_us": round(sep_ms * 1e3, 2),
         "prefill": {
             "what": f"pkv_paged_attention_prefill: each sequence's last min(ctx, {PREFILL_NEW_TOKENS}) positions as a "
                     "prefill chunk over its own paged context (causal), back to back in CUDA graphs",
-            "queries": pre_q, "us_per_call": round(pre_ms * 1e3, 2),
+            "queries": pre_q, "us_per_call": round(pre_ms * 1e3, 2), "calls": pre_calls,
+            "clocks": _clk(pre_clk),
             "roofline": {"bound": "tensor", "achieved": round(pre_flops / (pre_ms * 1e-3) / 1e12, 2),
                          "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": round(pre_flops / (pre_ms * 1e-3) / 1e12 / bf16_peak, 4),
@@ -875,21 +1056,30 @@ def run_ours(args, world, rank, local):
         "host_allocator_us_per_step": None if alloc_us is None else round(alloc_us, 1),
         "cpu_baseline": cpu_baseline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
-        "gpu_launches": step.launches_per_step * args.steps,
-        "timing": {"value": f"CUDA graphs of {STEPS_PER_GRAPH} steps (kernels chained by programmatic dependent "
-                            "launch) replayed until `steps` steps ran between two CUDA events",
-                   "kernel_us": "second pass of `steps` eager steps with CUDA events between the kernels on the "
-                                "launching stream; a 512 MB read before each step (outside the events) evicts L2",
-                   "roofline": "third pass: `steps` decode-attention calls back to back in CUDA graphs of "
-                               f"{ATTN_PER_GRAPH} calls between two CUDA events (K/V read per call > L2; no flush); "
-                               "per_call_latency is the attention figure of the second pass (one call between "
-                               "two events after an L2 eviction, launch latency included)",
-                   "e2e": "graphs of the same steps as a pipelined decode loop runs them: every step copies "
-                          "its inputs from pinned host memory in one copy (each of the two device input sets is "
-                          "one packed buffer; step i+1's copy on a second stream overlaps step i) and reads its "
-                          "attention output and error flag back"},
-        "clocks": clocks,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "clocks": _clk(e2e_clk)},
+        "gpu_launches": step.launches_per_step * args.steps + step.attention_launches * roof_calls,
+        "timing": {
+            "value": "decode-attention KV GB/s: algorithmic bytes of one pkv_paged_attention_decode call (K and V "
+                     "once, q, out, tables) over the sustained time per call (main pass + merge); calls back to back "
+                     f"in CUDA graphs (PDL-chained), graphs replayed for >= {MIN_WINDOW_S:.0f} s of device time "
+                     "between two CUDA events; = roofline.achieved",
+            "ms_per_step": f"exactly `steps` whole hot-path steps (slot mapping, store, attention, unpack K and V) in "
+                           f"CUDA graphs of {STEPS_PER_GRAPH} steps between two CUDA events; step_gbs = their "
+                           "algorithmic bytes over that time",
+            "configs": "every decode workload: per_call = one call between two CUDA events after a 512 MB "
+                       "L2-evicting read (median of 20, launch latency included); sustained = calls back to back for "
+                       f">= {MIN_WINDOW_S:.0f} s, rotating over `cache_copies` copies of the caches when one call reads "
+                       "under 4x L2; fp8/int8 = the same over E4M3/int8 caches (code bytes); decode_step_fused = "
+                       "append + attention (pkv_paged_attention_decode_append), tokens/s = batch / its time",
+            "kernel_us": "eager steps with CUDA events between the kernels on the launching stream; a 512 MB read "
+                         "before each step (outside the events) evicts L2",
+            "e2e": "decode steps (slot mapping, store, attention) as a pipelined loop runs them, for >= 1 s: every "
+                   "step copies its inputs from pinned host memory in one copy (two device input sets, step i+1's "
+                   "copy on a second stream overlaps step i) and reads its attention output and error flag back; "
+                   "value = attention KV bytes per step over the step time",
+            "gpu_launches": "kernels launched in the two timed regions value and ms_per_step come from"},
+        "clocks": dict(h_sus["clocks"], steps_pass=_clk(clocks_steps)),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -1208,7 +1398,7 @@ def csr_sub_snapshot(snap, first: int, count: int):
                    q=snap.q[first:first + count])
 
 def run_profile_calls(args, local):
-    """The workload's attention calls only, for an ncu capture of one launch."""
+    """One kernel's calls on the workload (--profile-calls), for an ncu capture of a few launches."""
     import pagedattention_decode_pkv_gb300 as pkv
 
     device = torch.device("cuda", local)
@@ -1220,6 +1410,29 @@ def run_profile_calls(args, local):
         call = step.code8_attention
     elif args.profile_calls == "prefill":
         call = prefill_call(step)[0]
+    elif args.profile_calls == "unpack":
+        step._unpack_buffers()
+        L, s, c, p = pkv._lib, step.snap, step.cfg, (lambda t: t.data_ptr())
+
+        def call(ptr):
+            return L.pkv_unpack_block_paged(p(step.unpacked_k), p(step.batch.k_cache), p(s.block_table),
+                                            p(s.seq_ptr), pkv.PKV_U32, p(s.token_ptr), step.B, s.nnz, c.block_size,
+                                            step.nb, c.num_kv_heads, c.head_dim, s.total_tokens, step.dt,
+                                            p(step.err), ptr)
+    elif args.profile_calls == "store":
+        # every context token's row, scattered to its own slot (a prefill's store)
+        L, b, c, p = pkv._lib, step.batch, step.cfg, (lambda t: t.data_ptr())
+        bt, ctx, bs = b.block_tables.cpu(), step.ctx_cpu, c.block_size
+        slots = torch.cat([bt[i, torch.arange(int(n)) // bs].to(torch.int64) * bs + torch.arange(int(n)) % bs
+                           for i, n in enumerate(ctx)]).to(torch.int32).to(device)
+        T = slots.numel()
+        key = torch.randn(T, c.num_kv_heads, c.head_dim, device=device).to(c.dtype)
+        value = torch.randn_like(key)
+        step.profile_buffers = (slots, key, value)
+
+        def call(ptr):
+            return L.pkv_store_kvcache(p(key), p(value), p(b.k_cache), p(b.v_cache), p(slots), T, c.num_kv_heads,
+                                       c.head_dim, step.nb * bs, step.dt, p(step.err), ptr)
     ptr = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for _ in range(args.steps):
         if call(ptr) != 0:

@@ -75,6 +75,10 @@ LLAMA2_7B_LAYER = DecodeConfig(
 QWEN3_GQA = DecodeConfig(
     "qwen3-0.6b-gqa-bf16", torch.bfloat16, 16, 8, 128, 256, 128, 256, 8192, 4096,
     "Qwen3-0.6B-shaped GQA layer: Hq=16, Hkv=8, d=128, bs=256, B=128, ctx~U[256,8192]")
+QWEN3_GQA_B1024 = DecodeConfig(
+    "qwen3-0.6b-gqa-bf16-b1024", torch.bfloat16, 16, 8, 128, 256, 1024, 256, 8192, None,
+    "Qwen3-0.6B-shaped GQA layer at a serving batch of 1024 sequences: Hq=16, Hkv=8, d=128, bs=256, "
+    "ctx~U[256,8192], pool of exactly the blocks the batch needs")
 LONG_GQA_8K = DecodeConfig(
     "long-gqa-8k-bf16", torch.bfloat16, 32, 8, 128, 16, 8, 8192, 8192, None,
     "long-context GQA: Hq=32, Hkv=8, d=128, bs=16, 8 sequences x 8192 tokens")
@@ -86,7 +90,7 @@ CSR_PREFIX = CsrConfig(
     "CSR snapshot: page_size=16, H=8, d=128, 256 seqs, half share a 1024-token aliased prefix, "
     "suffix~U[1,2048], u32 index buffers")
 
-CONFIGS = {c.name: c for c in (TINY, LLAMA2_7B_LAYER, QWEN3_GQA, LONG_GQA_8K, LONG_GQA_32K,
+CONFIGS = {c.name: c for c in (TINY, LLAMA2_7B_LAYER, QWEN3_GQA, QWEN3_GQA_B1024, LONG_GQA_8K, LONG_GQA_32K,
                                 CSR_PREFIX)}
 
 

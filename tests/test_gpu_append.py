@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import pkv_workloads as wl
+from conftest import attn_error
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +22,7 @@ def _bits(t):
 
 
 def _max_err(out, ref):
-    return (out.detach().cpu().double() - ref).abs().max().item() if ref.numel() else 0.0
+    return attn_error(out, ref)
 
 
 def _append(pkv, batch, max_ctx, err=None, key=None, value=None):

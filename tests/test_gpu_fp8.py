@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import pkv_workloads as wl
+from conftest import attn_error
 
 pytestmark = pytest.mark.gpu
 
@@ -13,7 +14,7 @@ ATOL_16 = 2e-2
 
 
 def _max_err(out, ref):
-    return (out.detach().cpu().double() - ref).abs().max().item() if ref.numel() else 0.0
+    return attn_error(out, ref)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])

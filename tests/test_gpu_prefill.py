@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import pkv_workloads as wl
+from conftest import attn_error
 
 pytestmark = pytest.mark.gpu
 
@@ -12,7 +13,7 @@ ATOL_16 = 2e-2
 
 
 def _max_err(out, ref):
-    return (out.detach().cpu().double() - ref).abs().max().item() if ref.numel() else 0.0
+    return attn_error(out, ref)
 
 
 # Launch shapes: every CTA takes two query tiles of one (sequence, KV head), and

@@ -8,13 +8,14 @@ Common Pitfalls) and "Block-Paged KV Cache" (Element lookup through the block
 table; Validating the storage invariants).
 """
 import math
+import os
 
 import numpy as np
 import pytest
 import torch
 import torch.nn.functional as F
 
-from conftest import load_golden
+from conftest import ROOT, load_golden
 
 
 # --------------------------------------------------------------------------- widening
@@ -636,3 +637,17 @@ def test_quantization_compatibility_each_rule(orc):
     assert orc.quantization_compatible(0x01, 0, 1, 4) == 0   # per-tensor
     assert orc.quantization_compatible(0x00, 0, 1, 4) == 0   # none
     assert orc.quantization_compatible(0x07, 0, 4, 4) == 4   # unknown tag
+
+
+def test_walk_trace_golden_is_what_its_script_derives():
+    """walk_trace.json's derived steps are written by tests/golden/make_walk_trace.py,
+    which calls only the oracle (allocator model and slot mapping)."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "tests", "golden", "make_walk_trace.py")
+    spec = importlib.util.spec_from_file_location("_make_walk_trace", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert mod.main(["--check"]) == 0
+    steps = load_golden("walk_trace.json")["derived_by_the_page_rules"]["steps"]
+    assert steps[0]["slots"][:6] == load_golden("walk_trace.json")["printed_on_page"]["A_prefill"]
