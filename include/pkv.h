@@ -244,10 +244,14 @@ PKV_API pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num
  * every GPU loading the library holds until the process exits.  Sizes whose
  * pkv_paged_attention_decode_workspace_size exceeds it are rejected with
  * PKV_ERR_WORKSPACE before anything is enqueued; use the workspace variant
- * for those.
+ * for those.  Argument errors (bad sizes, NULL pointers) are reported as
+ * PKV_ERR_INVALID_ARG first, exactly as by pkv_paged_attention_decode.  The
+ * decode workloads of the benchmark fit: 8 x 32768 tokens at Hq 32 / Hkv 8
+ * needs about 15.9 MB, 64 x 4096 at Hq = Hkv = 32 about 14.4 MB.
  *
- * The first call on each device looks up the region's device address
- * (cudaGetSymbolAddress) with that device current.  Make that first call
+ * Every call looks up the region's device address (cudaGetSymbolAddress)
+ * with the calling thread's current device; the lookup allocates nothing.
+ * The first call on a device may load the library's device code, so make it
  * before any stream capture.
  *
  * All calls share the one region, and it keeps whatever the last call left
@@ -424,8 +428,20 @@ PKV_API pkv_status pkv_paged_attention_prefill(void *out, const void *q, const v
  *   and the products run on f16 tensor cores (q is rounded to f16 once;
  *   values beyond 65504 overflow).  Only the tensor-core, work-balanced
  *   shapes run: head_dim 128, num_q_heads / num_kv_heads <= 8, block_size a
- *   multiple of 16, at most 512 sequences, 16-byte aligned q and code pools;
- *   others return PKV_ERR_UNSUPPORTED.
+ *   multiple of 16, 16-byte aligned q and code pools; others return
+ *   PKV_ERR_UNSUPPORTED.  Batches of more than 512 sequences run as
+ *   consecutive launches over groups of at most 512 (one workspace, reused in
+ *   stream order).
+ * pkv_paged_attention_decode_append_fp8: the fused decode step over fp8
+ *   caches ("Step 1" then "Step 2" for one new token per sequence): key[b]
+ *   and value[b] ([num_seqs, num_kv_heads, head_dim], the q dtype, 8-byte
+ *   aligned) are encoded as by pkv_store_kvcache_fp8, under the scales
+ *   already in k_scale / v_scale, into the cache row of position
+ *   context_lens[b] - 1, and the attention of pkv_paged_attention_decode_fp8
+ *   runs over the whole context, the new token included.  The scales are not
+ *   changed.  Arguments, workspace, limits and errors as
+ *   pkv_paged_attention_decode_fp8; a block id out of range at position
+ *   ctx - 1 skips the append and sets PKV_ERRBIT_BLOCK_RANGE.
  */
 PKV_API pkv_status pkv_quantize_kvcache_fp8(const void *src, void *codes, float *scales, int32_t num_blocks,
                                             int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
@@ -443,6 +459,16 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, cons
                                                   int32_t block_size, int32_t num_blocks, int32_t max_context_len,
                                                   float scale, pkv_dtype dtype, void *workspace,
                                                   size_t workspace_bytes, int32_t *err_flag, void *stream);
+PKV_API pkv_status pkv_paged_attention_decode_append_fp8(void *out, const void *q, const void *key,
+                                                         const void *value, void *k_cache, void *v_cache,
+                                                         const float *k_scale, const float *v_scale,
+                                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                         const int32_t *context_lens, int32_t num_seqs,
+                                                         int32_t num_q_heads, int32_t num_kv_heads,
+                                                         int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                                         int32_t max_context_len, float scale, pkv_dtype dtype,
+                                                         void *workspace, size_t workspace_bytes,
+                                                         int32_t *err_flag, void *stream);
 
 /*
  * int8 paged caches -- "Block-Paged KV Cache", Quantization compatibility
@@ -454,11 +480,11 @@ PKV_API pkv_status pkv_paged_attention_decode_fp8(void *out, const void *q, cons
  * Encoding divides by the scale in binary32, rounds to the nearest integer
  * (ties to even), clamps to +-127 and stores NaN as 0; a zero scale stores 0.
  *
- * pkv_quantize_kvcache_int8, pkv_store_kvcache_int8 and
- * pkv_paged_attention_decode_int8 take the arguments, and have the
- * ownership, shape limits, errors and device error bits, of their fp8
- * counterparts above; only the code format differs.  Codes are widened
- * exactly to f16 for the products.
+ * pkv_quantize_kvcache_int8, pkv_store_kvcache_int8,
+ * pkv_paged_attention_decode_int8 and pkv_paged_attention_decode_append_int8
+ * take the arguments, and have the ownership, shape limits, errors and
+ * device error bits, of their fp8 counterparts above; only the code format
+ * differs.  Codes are widened exactly to f16 for the products.
  */
 PKV_API pkv_status pkv_quantize_kvcache_int8(const void *src, void *codes, float *scales, int32_t num_blocks,
                                              int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
@@ -476,6 +502,16 @@ PKV_API pkv_status pkv_paged_attention_decode_int8(void *out, const void *q, con
                                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len,
                                                    float scale, pkv_dtype dtype, void *workspace,
                                                    size_t workspace_bytes, int32_t *err_flag, void *stream);
+PKV_API pkv_status pkv_paged_attention_decode_append_int8(void *out, const void *q, const void *key,
+                                                          const void *value, void *k_cache, void *v_cache,
+                                                          const float *k_scale, const float *v_scale,
+                                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                          const int32_t *context_lens, int32_t num_seqs,
+                                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                                          int32_t max_context_len, float scale, pkv_dtype dtype,
+                                                          void *workspace, size_t workspace_bytes,
+                                                          int32_t *err_flag, void *stream);
 
 /*
  * Host block allocator -- which physical block of the pool each sequence

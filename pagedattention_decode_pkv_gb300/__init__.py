@@ -71,6 +71,12 @@ _SIGS = {
                                 _vp], ctypes.c_int),
     "pkv_paged_attention_decode_int8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp], ctypes.c_int),
+    "pkv_paged_attention_decode_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                               _i32, _i32, _i32, _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp],
+                                              ctypes.c_int),
+    "pkv_paged_attention_decode_append_int8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                                _i32, _i32, _i32, _i32, _i32, _f32, ctypes.c_int, _vp, _sz, _vp, _vp],
+                                               ctypes.c_int),
     "pkv_selftest_wait_timeout": ([_vp, ctypes.c_uint32, _vp], ctypes.c_int),
     "pkv_allocator_create": ([_i32, _i32, _vp], ctypes.c_int),
     "pkv_allocator_destroy": ([_vp], None),
@@ -385,8 +391,9 @@ def _store_codes(fmt, key, value, k_cache, v_cache, k_scale, v_scale, slot_mappi
 
 
 def _attention_codes(fmt, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
-                     max_context_len, out, workspace, err_flag, stream):
-    dev = _dev(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, workspace, err_flag)
+                     max_context_len, out, workspace, err_flag, stream, key=None, value=None):
+    dev = _dev(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out, workspace, err_flag, key,
+               value)
     _want(k_cache, _CODES[fmt], "k_cache")
     _want(v_cache, _CODES[fmt], "v_cache")
     _want(k_scale, torch.float32, "k_scale")
@@ -400,12 +407,20 @@ def _attention_codes(fmt, q, k_cache, v_cache, k_scale, v_scale, block_tables, c
     ws = pkv_paged_attention_decode_workspace_size(B, Hq, Hkv, d, bs, max_context_len, q.dtype) if B else 0
     if ws and workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-    fn = getattr(_lib, "pkv_paged_attention_decode_" + fmt)
+    tail = (block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale),
+            _DTYPE[q.dtype], _ptr(workspace) if ws else None,
+            workspace.numel() * workspace.element_size() if ws else 0, _ptr(err_flag), _stream(dev, stream))
     with torch.cuda.device(dev):
-        _check(fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
-                  block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, d, bs, nb, max_context_len, float(scale),
-                  _DTYPE[q.dtype], _ptr(workspace) if ws else None,
-                  workspace.numel() * workspace.element_size() if ws else 0, _ptr(err_flag), _stream(dev, stream)))
+        if key is None:
+            fn = getattr(_lib, "pkv_paged_attention_decode_" + fmt)
+            _check(fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                      _ptr(block_tables), *tail))
+        else:
+            if key.dtype != q.dtype or value.dtype != q.dtype or key.shape != (B, Hkv, d) or value.shape != key.shape:
+                raise ValueError("key/value must be [num_seqs, num_kv_heads, head_dim] of the q dtype")
+            fn = getattr(_lib, "pkv_paged_attention_decode_append_" + fmt)
+            _check(fn(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(k_cache),
+                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), *tail))
     return out
 
 
@@ -429,6 +444,17 @@ def pkv_paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_
                             max_context_len, out, workspace, err_flag, stream)
 
 
+def pkv_paged_attention_decode_append_fp8(q, key, value, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                          context_lens, scale: float, max_context_len: int, *, out=None,
+                                          workspace=None, err_flag=None, stream=None):
+    """One decode step over E4M3 code caches: key[b] / value[b] are encoded
+    under the existing (block, head) scales into the row of position
+    context_lens[b] - 1 (in place), then the attention of
+    pkv_paged_attention_decode_fp8 runs over the whole context."""
+    return _attention_codes("fp8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                            max_context_len, out, workspace, err_flag, stream, key, value)
+
+
 def pkv_quantize_kvcache_int8(cache, *, codes=None, scales=None, stream=None):
     """[num_blocks, bs, Hkv, d] cache -> (int8 codes of the same shape, float32
     scales [num_blocks, Hkv]); per (block, head) s = max|x| / 127."""
@@ -447,6 +473,14 @@ def pkv_paged_attention_decode_int8(q, k_cache, v_cache, k_scale, v_scale, block
     """Decode attention over int8 code caches with per-(block, head) scales."""
     return _attention_codes("int8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
                             max_context_len, out, workspace, err_flag, stream)
+
+
+def pkv_paged_attention_decode_append_int8(q, key, value, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                           context_lens, scale: float, max_context_len: int, *, out=None,
+                                           workspace=None, err_flag=None, stream=None):
+    """One decode step over int8 code caches (see pkv_paged_attention_decode_append_fp8)."""
+    return _attention_codes("int8", q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                            max_context_len, out, workspace, err_flag, stream, key, value)
 
 
 # ----------------------------------------------------------------------------- failure detection

@@ -40,11 +40,11 @@
 
 #include <atomic>
 #include <cstdlib>
-#include <mutex>
 #include <type_traits>
 
 #include "pkv_internal.h"
 #include "pkv_pdl.cuh"
+#include "pkv_q8.cuh"
 #include "pkv_tma.cuh"
 
 namespace pkv {
@@ -67,6 +67,8 @@ constexpr bool kKvEvictFirst = true;   // K/V tiles are read once: mark them fir
 struct Plan {
     bool fast = false;
     bool stream = false;  // fast path with the work-balanced one-wave schedule
+    int groups = 1;       // work-balanced launches, one per group of <= kMaxStreamSeqs sequences
+    int group_seqs = 0;   // sequences per group (the last may hold fewer)
     int64_t units = 0;    // (sequence, head group) units of the work-balanced schedule
     int64_t max_chunks = 0, max_segments = 0;  // dynamic-tail chunks / piece slots (bounds)
     size_t unit_bytes = 0;
@@ -91,7 +93,7 @@ int env_partition_override() {
 // alignment does not hold at call time); max_parts > 0 caps the partitions so
 // that the partials fit a workspace sized for another plan.
 Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt, bool generic_only = false,
-               int64_t max_parts = 0) {
+               int64_t max_parts = 0, bool codes8 = false) {
     Plan p;
     const int G = Hq / Hkv;
     p.fast = !generic_only && (dt == PKV_F16 || dt == PKV_BF16) && d == kFastHeadDim && G >= 1 && G <= 8 &&
@@ -101,12 +103,20 @@ Plan make_plan(int B, int Hq, int Hkv, int d, int bs, int max_ctx, pkv_dtype dt,
     p.stages = 98304 / stage_bytes;
     if (p.stages > 8) p.stages = 8;
     if (p.stages < 2) p.stages = 2;
-    p.stream = p.fast && B <= kMaxStreamSeqs;
+    // Past kMaxStreamSeqs sequences, 16-bit caches take the fixed-partition
+    // kernel (a many-wave grid: measured 7.33 TB/s on 1024 Qwen3-shaped
+    // sequences); 8-bit caches, which only the work-balanced kernel reads,
+    // run it as consecutive launches over groups of near-equal size that reuse
+    // one scratch region in stream order (each launch's first global access
+    // waits for the previous grid to complete).
+    p.stream = p.fast && (B <= kMaxStreamSeqs || codes8);
     if (p.stream) {
+        p.groups = B > kMaxStreamSeqs ? (B + kMaxStreamSeqs - 1) / kMaxStreamSeqs : 1;
+        p.group_seqs = (B + p.groups - 1) / p.groups;
         // Pieces: at most one per (unit, segment) boundary; segments are the
         // static slices (at most kMaxStreamCtas) and the dynamic-tail chunks.
         const int64_t HG = Hkv / p.hpc, HU = Hq / HG;
-        p.units = static_cast<int64_t>(B) * HG;
+        p.units = static_cast<int64_t>(p.group_seqs) * HG;
         const int64_t w_max = p.units * ((static_cast<int64_t>(max_ctx) + kStageTokens - 1) / kStageTokens);
         p.max_chunks = w_max / kTailDenominator / kChunkStages + 1;
         // static slots [0, kMaxStreamCtas + units), dynamic slots after them
@@ -1032,24 +1042,49 @@ decode_stream_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     // Append: the step's new K/V rows of these HPC heads go to the
                     // cache row of position ctx - 1 before the bulk copy reads it
                     // back (the generic-proxy stores are ordered before the
-                    // async-proxy load by fence.proxy.async).
+                    // async-proxy load by fence.proxy.async).  Lane l moves dims
+                    // 4l .. 4l + 3 of every head (8 bytes of the 16-bit row).
                     const int64_t row = static_cast<int64_t>(id) * bs + (meta >> 16) + ((meta & 0xff) - 1);
                     const int64_t src = (static_cast<int64_t>(b) * HG + hg) * HPC * kFastHeadDim;
-                    const int64_t dst = (row * HG + hg) * HPC * kFastHeadDim;
+                    const int64_t dst = (row * HG + hg) * HPC * kFastHeadDim;  // elements (16-bit) or codes
                     const int2 *sk = reinterpret_cast<const int2 *>(new_k + src);
                     const int2 *sv = reinterpret_cast<const int2 *>(new_v + src);
-                    int2 *dk = reinterpret_cast<int2 *>(k_cache_w + dst);
-                    int2 *dv = reinterpret_cast<int2 *>(v_cache_w + dst);
                     int2 tk[HPC], tv[HPC];  // HPC heads x 256 bytes = HPC x 32 lanes x 8 bytes
 #pragma unroll
                     for (int e = 0; e < HPC; ++e) {
                         tk[e] = __ldg(sk + e * 32 + lane);
                         tv[e] = __ldg(sv + e * 32 + lane);
                     }
+                    if constexpr (C8) {
+                        // 8-bit cache: each head's four values become four codes
+                        // under that head's existing (block, head) scale, loaded
+                        // with this stage's description (the store kernels'
+                        // encoding: x / s in binary32, round to nearest even).
+                        __syncwarp();  // the describing lane wrote the scales
+                        const float *sc = bscl + (cbuf * 32 + j) * 2 * HPC;  // [K: HPC][V: HPC]
+                        uint8_t *dk = reinterpret_cast<uint8_t *>(k_cache_w) + dst;
+                        uint8_t *dv = reinterpret_cast<uint8_t *>(v_cache_w) + dst;
 #pragma unroll
-                    for (int e = 0; e < HPC; ++e) {
-                        dk[e * 32 + lane] = tk[e];
-                        dv[e * 32 + lane] = tv[e];
+                        for (int e = 0; e < HPC; ++e) {
+                            const T *xk = reinterpret_cast<const T *>(&tk[e]);
+                            const T *xv = reinterpret_cast<const T *>(&tv[e]);
+                            const float s_k = sc[e], s_v = sc[HPC + e];
+                            constexpr bool I8 = FMT == kCodeInt8;
+                            const uint32_t ck = q8_encode2<I8>(to_f32(xk[0]), to_f32(xk[1]), s_k) |
+                                                q8_encode2<I8>(to_f32(xk[2]), to_f32(xk[3]), s_k) << 16;
+                            const uint32_t cv = q8_encode2<I8>(to_f32(xv[0]), to_f32(xv[1]), s_v) |
+                                                q8_encode2<I8>(to_f32(xv[2]), to_f32(xv[3]), s_v) << 16;
+                            *reinterpret_cast<uint32_t *>(dk + e * kFastHeadDim + 4 * lane) = ck;
+                            *reinterpret_cast<uint32_t *>(dv + e * kFastHeadDim + 4 * lane) = cv;
+                        }
+                    } else {
+                        int2 *dk = reinterpret_cast<int2 *>(k_cache_w + dst);
+                        int2 *dv = reinterpret_cast<int2 *>(v_cache_w + dst);
+#pragma unroll
+                        for (int e = 0; e < HPC; ++e) {
+                            dk[e * 32 + lane] = tk[e];
+                            dv[e * 32 + lane] = tv[e];
+                        }
                     }
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     __syncwarp();
@@ -1706,7 +1741,8 @@ inline int merge_warps_per_row(int64_t rows) {
 
 template <typename T>
 cudaError_t launch_stream_combine(const DecodeArgs &a, const Plan &p, int C, int HG, int HU) {
-    const int64_t rows = p.units * HU;
+    const int64_t units = static_cast<int64_t>(a.B) * HG;  // this launch's group (<= p.units)
+    const int64_t rows = units * HU;
     const int wpr = merge_warps_per_row(rows);
     const int64_t rpc = kMergeWarps / wpr;
     const dim3 grid(static_cast<unsigned>((rows + rpc - 1) / rpc));
@@ -1717,7 +1753,7 @@ cudaError_t launch_stream_combine(const DecodeArgs &a, const Plan &p, int C, int
     return launch_pdl(kPdlCombine, kern, grid, dim3(kMergeThreads), 0, a.stream, static_cast<T *>(a.out),
                       static_cast<const float *>(a.o_part), static_cast<const float2 *>(a.ml_part),
                       static_cast<const int4 *>(a.unit_info), a.context_lens, a.Hq, HG, HU, a.bs, a.max_blocks,
-                      a.max_ctx, C, static_cast<int64_t>(kMaxStreamCtas + p.units),
+                      a.max_ctx, C, static_cast<int64_t>(kMaxStreamCtas + units),
                       static_cast<int64_t>(p.max_segments), rows);
 }
 
@@ -1857,7 +1893,11 @@ extern "C" size_t pkv_paged_attention_decode_workspace_size(int32_t num_seqs, in
     if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
         head_dim <= 0 || block_size <= 0 || max_context_len < 0 || dtype_bytes(dtype) == 0)
         return 0;
-    return make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype).ws_bytes;
+    // one size for 16-bit and 8-bit caches (their plans differ past 512 sequences)
+    const size_t a = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype).ws_bytes;
+    const size_t b = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype,
+                               false, 0, true).ws_bytes;
+    return a > b ? a : b;
 }
 
 extern "C" pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num_q_heads,
@@ -1878,6 +1918,29 @@ extern "C" pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t 
 namespace pkv {
 namespace {
 
+// Sizes, dtype and pointers of a decode call, checked before anything else
+// (the workspace is checked later, against the plan these sizes give).
+pkv_status check_decode_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, int32_t max_context_len, pkv_dtype dtype) {
+    if (dtype_bytes(dtype) == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks < 0 || max_context_len < 0 || max_blocks_per_seq < 0)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: bad sizes");
+    if (num_q_heads % num_kv_heads)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                         num_q_heads, num_kv_heads);
+    if (head_dim > 1024) return set_error(PKV_ERR_UNSUPPORTED, "decode: head_dim > 1024");
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+        return set_error(PKV_ERR_INVALID_ARG, "decode: num_blocks * block_size >= 2^31");
+    if (num_seqs > 65535) return set_error(PKV_ERR_UNSUPPORTED, "decode: more than 65535 sequences in one call");
+    if (num_seqs > 0 && (!out || !q || !context_lens || (max_blocks_per_seq > 0 && !block_tables) ||
+                         (num_blocks > 0 && (!k_cache || !v_cache))))
+        return set_error(PKV_ERR_INVALID_ARG, "decode: NULL pointer");
+    return PKV_OK;
+}
+
 // Decode attention, with the step's new K/V rows appended first when new_k is
 // not null (the fused decode step).
 pkv_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -1890,25 +1953,15 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
     const int64_t es = dtype_bytes(dtype);
     const bool c8 = codes != kCode16;  // 8-bit caches with per-(block, head) scales
     const char *fmt = codes == kCodeInt8 ? "int8" : "fp8";
-    if (es == 0) return set_error(PKV_ERR_INVALID_ARG, "decode: unknown dtype %d", (int)dtype);
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-        num_blocks < 0 || max_context_len < 0 || max_blocks_per_seq < 0)
-        return set_error(PKV_ERR_INVALID_ARG, "decode: bad sizes");
-    if (num_q_heads % num_kv_heads)
-        return set_error(PKV_ERR_INVALID_ARG, "decode: num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
-                         num_q_heads, num_kv_heads);
-    if (head_dim > 1024) return set_error(PKV_ERR_UNSUPPORTED, "decode: head_dim > 1024");
-    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
-        return set_error(PKV_ERR_INVALID_ARG, "decode: num_blocks * block_size >= 2^31");
-    if (num_seqs > 65535) return set_error(PKV_ERR_UNSUPPORTED, "decode: more than 65535 sequences in one call");
+    pkv_status chk = check_decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                       max_context_len, dtype);
+    if (chk != PKV_OK) return chk;
     if (num_seqs == 0) return ok();
-    if (!out || !q || !context_lens || (max_blocks_per_seq > 0 && !block_tables) ||
-        (num_blocks > 0 && (!k_cache || !v_cache)))
-        return set_error(PKV_ERR_INVALID_ARG, "decode: NULL pointer");
     const bool append = new_k != nullptr || new_v != nullptr;
     if (append && (!new_k || !new_v || !aligned(new_k, es) || !aligned(new_v, es)))
         return set_error(PKV_ERR_INVALID_ARG, "decode append: key/value NULL or not aligned to the element size");
-    Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype);
+    Plan p = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, dtype, false, 0, c8);
     if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
         return set_error(PKV_ERR_WORKSPACE, "decode: workspace needs %zu bytes (256-byte aligned), got %zu",
                          p.ws_bytes, workspace_bytes);
@@ -1917,11 +1970,11 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
     // The fast path additionally wants 16-byte aligned pools (TMA) and 4-byte aligned q.
     const bool fast = p.fast && num_blocks > 0 && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(q, 4);
     if (c8) {
-        if (!fast || !p.stream || append || !aligned(q, 16))
+        if (!fast || !p.stream || !aligned(q, 16) || (append && (!aligned(new_k, 8) || !aligned(new_v, 8))))
             return set_error(PKV_ERR_UNSUPPORTED,
                              "decode %s: needs fp16/bf16 q, head_dim 128, Hq/Hkv <= 8, block_size a multiple of "
-                             "16, at most %d sequences, 16-byte aligned q and code pools",
-                             fmt, kMaxStreamSeqs);
+                             "16, 16-byte aligned q and code pools (and 8-byte aligned key/value to append)",
+                             fmt);
         if (!k_scale || !v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4))
             return set_error(PKV_ERR_INVALID_ARG, "decode %s: scales NULL or not 4-byte aligned", fmt);
     }
@@ -1963,7 +2016,24 @@ pkv_status decode_entry(void *out, const void *q, const void *k_cache, const voi
         a.new_k = a.new_v = nullptr;
     }
     if (fast && p.stream) {
-        st = dtype == PKV_BF16 ? launch_stream_any<__nv_bfloat16>(a, p) : launch_stream_any<__half>(a, p);
+        // one work-balanced launch (and merge) per group of sequences
+        const int64_t q_row = static_cast<int64_t>(num_q_heads) * head_dim * es;
+        const int64_t kv_row = static_cast<int64_t>(num_kv_heads) * head_dim * es;
+        for (int g = 0; g < p.groups; ++g) {
+            const int b0 = g * p.group_seqs;
+            DecodeArgs ag = a;
+            ag.B = min(p.group_seqs, num_seqs - b0);
+            ag.out = static_cast<char *>(out) + b0 * q_row;
+            ag.q = static_cast<const char *>(q) + b0 * q_row;
+            ag.block_tables = block_tables ? block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq : nullptr;
+            ag.context_lens = context_lens + b0;
+            if (a.new_k) {
+                ag.new_k = static_cast<const char *>(a.new_k) + b0 * kv_row;
+                ag.new_v = static_cast<const char *>(a.new_v) + b0 * kv_row;
+            }
+            st = dtype == PKV_BF16 ? launch_stream_any<__nv_bfloat16>(ag, p) : launch_stream_any<__half>(ag, p);
+            if (st != PKV_OK) return st;
+        }
     } else if (fast) {
         st = dtype == PKV_BF16 ? launch_fast_any<__nv_bfloat16>(a, p) : launch_fast_any<__half>(a, p);
         if (st != PKV_OK) return st;
@@ -2045,6 +2115,51 @@ extern "C" pkv_status pkv_paged_attention_decode_int8(void *out, const void *q, 
                         workspace, workspace_bytes, err_flag, stream, nullptr, nullptr, k_scale, v_scale, kCodeInt8);
 }
 
+// The fused decode step over 8-bit caches: key[b] / value[b] are encoded
+// under the (block, head) scales already in k_scale / v_scale and written to
+// the cache row of position context_lens[b] - 1 by the attention kernel's
+// producer warp, then the attention runs over the whole context.
+namespace pkv {
+namespace {
+pkv_status decode_append_q8(void *out, const void *q, const void *key, const void *value, void *k_cache,
+                            void *v_cache, const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, int32_t max_context_len, float scale, pkv_dtype dtype, void *workspace,
+                            size_t workspace_bytes, int32_t *err_flag, void *stream, int32_t codes) {
+    const char *fmt = codes == kCodeInt8 ? "int8" : "fp8";
+    if (num_seqs > 0 && (!k_scale || !v_scale || !key || !value))
+        return set_error(PKV_ERR_INVALID_ARG, "decode append %s: NULL key, value or scales", fmt);
+    if (dtype == PKV_F32) return set_error(PKV_ERR_UNSUPPORTED, "decode append %s: q/out must be fp16 or bf16", fmt);
+    return decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, dtype,
+                        workspace, workspace_bytes, err_flag, stream, key, value, k_scale, v_scale, codes);
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_attention_decode_append_fp8(
+    void *out, const void *q, const void *key, const void *value, void *k_cache, void *v_cache, const float *k_scale,
+    const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, int32_t max_context_len, float scale, pkv_dtype dtype, void *workspace,
+    size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    return decode_append_q8(out, q, key, value, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                            context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                            max_context_len, scale, dtype, workspace, workspace_bytes, err_flag, stream, kCodeE4M3);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_append_int8(
+    void *out, const void *q, const void *key, const void *value, void *k_cache, void *v_cache, const float *k_scale,
+    const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, int32_t max_context_len, float scale, pkv_dtype dtype, void *workspace,
+    size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    return decode_append_q8(out, q, key, value, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                            context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                            max_context_len, scale, dtype, workspace, workspace_bytes, err_flag, stream, kCodeInt8);
+}
+
 // ----------------------------------------------------------------------------- no-allocation variant
 // Decode attention for callers that cannot allocate device memory where they
 // run (an engine plugin that may only use memory it was handed, a service with
@@ -2058,27 +2173,16 @@ static __device__ __align__(256) unsigned char g_pkv_static_workspace[PKV_STATIC
 namespace pkv {
 namespace {
 
-constexpr int kMaxStaticDevices = 64;
-std::mutex g_static_ws_mutex;
-void *g_static_ws_addr[kMaxStaticDevices] = {};
-
-// Device address of the region on the current device, looked up once per
-// device with that device current (host code cannot use the symbol itself).
+// Device address of the region on the current device.  Host code cannot use
+// the symbol itself (it names a host-side shadow), so the address is looked up
+// with the device current, on every call: the lookup allocates nothing, and a
+// fresh one stays right after a cudaDeviceReset reloads the module.
 pkv_status static_workspace_address(void **addr) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "static workspace: cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxStaticDevices)
-        return set_error(PKV_ERR_UNSUPPORTED, "static workspace: device index %d >= %d", dev, kMaxStaticDevices);
-    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
-    if (!g_static_ws_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_pkv_static_workspace);
-        if (e != cudaSuccess || !p)
-            return set_error(PKV_ERR_CUDA, "static workspace: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_static_ws_addr[dev] = p;
-    }
-    *addr = g_static_ws_addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_pkv_static_workspace);
+    if (e != cudaSuccess || !p)
+        return set_error(PKV_ERR_CUDA, "static workspace: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    *addr = p;
     return PKV_OK;
 }
 
@@ -2090,6 +2194,11 @@ extern "C" pkv_status pkv_paged_attention_decode_static_ws(
     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, int32_t max_context_len,
     float scale, pkv_dtype dtype, int32_t *err_flag, void *stream) {
+    // the same argument errors as the workspace variant, before the size check
+    const pkv_status chk = check_decode_args(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                             context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             block_size, num_blocks, max_context_len, dtype);
+    if (chk != PKV_OK) return chk;
     const size_t need = pkv_paged_attention_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                                   block_size, max_context_len, dtype);
     if (need > PKV_STATIC_WORKSPACE_BYTES)

@@ -23,6 +23,7 @@
 
 #include "pkv_internal.h"
 #include "pkv_pdl.cuh"
+#include "pkv_q8.cuh"
 
 namespace pkv {
 namespace {
@@ -37,24 +38,9 @@ enum CodeFormat { kE4M3 = 0, kInt8 = 1 };
 // The largest code magnitude: a (block, head) scale is max |x| / this.
 template <int FMT> constexpr float kCodeMax = FMT == kInt8 ? 127.f : 448.f;
 
-// binary32 -> int8 code: nearest integer, ties to even (cvt.rni); NaN -> 0
-// (the conversion's rule for NaN), then clamped to +-127.
-__device__ __forceinline__ uint32_t int8_code(float y) {
-    const int r = min(max(__float2int_rn(y), -127), 127);
-    return static_cast<uint32_t>(r) & 0xFFu;
-}
-
 // Two binary32 -> two codes (lo in the low byte) of x / s; a zero scale gives 0.
 template <int FMT> __device__ __forceinline__ uint32_t encode2(float lo, float hi, float s) {
-    if (s == 0.f) return 0u;
-    const float a = __fdiv_rn(lo, s), b = __fdiv_rn(hi, s);
-    if constexpr (FMT == kInt8) {
-        return int8_code(a) | int8_code(b) << 8;
-    } else {
-        uint16_t d;
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
-        return d;
-    }
+    return q8_encode2<FMT == kInt8>(lo, hi, s);
 }
 
 constexpr int kQuantThreads = 256;
