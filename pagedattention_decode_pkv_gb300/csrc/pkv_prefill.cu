@@ -13,14 +13,16 @@
 // Design (fifth-generation tensor cores, FlashAttention style).  A query tile
 // is 128 query rows of one KV head: 128 / G positions x the G query heads of
 // the group, so every K/V byte staged for it serves all G heads.  A CTA owns
-// two tiles of the same (sequence, KV head), and keys go by blocks of 128 (the
-// template also takes one tile per CTA and 64-key blocks; launch_prefill_any
-// has the measurements).  Per block j:
+// two tiles of the same (sequence, KV head), and keys go by blocks of 128.
+// Per block j:
 //   * a producer warp copies K_j and V_j (the head's rows of the pages that
-//     hold keys KEYS j .. KEYS j + KEYS - 1) into a ring of stages with TMA, in
-//     chunks of gcd(block_size, KEYS) tokens per 64-dim half, 128-byte
-//     swizzled; both tiles read every stage;
-//   * an MMA warp issues, per tile, S_j = Q K_j^T (M = 128 rows, N = KEYS,
+//     hold keys 128 j .. 128 j + 127) with TMA, in chunks of
+//     gcd(block_size, 128) tokens per 64-dim half, 128-byte swizzled, into two
+//     separate rings of two buffers: K_j as soon as both tiles' QKs of block
+//     j - 2 have read its K buffer, V_j once their PVs of block j - 2 have
+//     read its V buffer, so the K copies run ahead of the V copies and their
+//     latency hides behind the PVs;
+//   * an MMA warp issues, per tile, S_j = Q K_j^T (M = 128 rows, N = 128 keys,
 //     eight K = 16 steps over the head dimension) into the tile's S buffer in
 //     TMEM, and O += P_j V_j (N = 128 dims, K = 16 steps over the keys; P is
 //     the A operand straight from TMEM, V the MN-major B operand) into the
@@ -30,8 +32,10 @@
 //     S_j from TMEM, mask it (causal, keys of missing pages), keep the row's
 //     running maximum and sum, and write P_j = exp2(S_j * scale * log2 e - m)
 //     as 16-bit pairs over the S_j they read.  The next S of the tile goes into
-//     that buffer once the PV of block j has read P_j; the softmax waits for
-//     the PV of block j - 1 only when it has to rescale O.
+//     that buffer right after the PV of block j that reads P_j: one thread's
+//     tcgen05.mma operations run in issue order, so the MMA warp does not wait
+//     for that PV.  The softmax waits for the PV of block j - 1 only when it
+//     has to rescale O.
 // The reference maximum m of a row moves only when the block's maximum exceeds
 // it by more than 2^8 (log2 units), and then O's row is rescaled in TMEM;
 // otherwise P is computed against the older m (values up to 256), which keeps
@@ -106,16 +110,14 @@ __device__ __forceinline__ uint64_t splat2(float v) {
 
 // Per block size (KEYS keys per block, the S MMA's N), ring depth and query
 // tiles per CTA: the K/V tiles, the shared-memory layout, TMEM columns and
-// mbarrier indices.
-//   KEYS = 128, 3 stages, one tile: 230 KB of shared memory, one CTA per SM.
-//   KEYS = 64, 2 stages, one tile: 97 KB, two CTAs per SM (eight softmax warps).
-//   KEYS = 128, 2 stages, two tiles: 198 KB, one CTA per SM, eight softmax
-//     warps (four per tile) sharing every K/V stage.
-//   KEYS = 64, 4 stages, two tiles: 198 KB, one CTA per SM, eight softmax warps.
-// TMEM: tile t owns columns [t kTileCols, (t + 1) kTileCols).  Its kNBuf S / P
-// buffers (one for two tiles of 128-key blocks, two otherwise) come first: buffer
-// j % kNBuf holds S_j (KEYS columns) and then P_j (KEYS / 2 columns of 16-bit
-// pairs, written over the S it came from); O follows at kTmemO.
+// mbarrier indices.  The kernel runs KEYS = 128, two buffers per ring and two
+// tiles: 198 KB of shared memory (two Q tiles, K and V rings of two 32 KB
+// buffers each), one CTA per SM, eight softmax warps (four per tile) sharing
+// every K/V buffer.  One tile per CTA and 64-key blocks (two CTAs per SM, or
+// four buffers) measured slower (launch_prefill_any).
+// TMEM: tile t owns columns [t kTileCols, (t + 1) kTileCols): its S / P buffer
+// (S_j in KEYS columns, then P_j in KEYS / 2 columns of 16-bit pairs written
+// over the S it came from) and O at kTmemO.
 template <int KEYS, int STAGES, int TILES = 1>
 struct PreCfg {
     static constexpr int kNBuf = TILES == 2 && KEYS == 128 ? 1 : 2;  // S / P buffers per tile
@@ -131,15 +133,18 @@ struct PreCfg {
     // shared memory
     static constexpr int kQ = 0;                                   // [TILES][2 halves][128 rows][128 B]
     static constexpr int kKV = kQ + TILES * kQTileBytes;           // stage s: K [2][KEYS][128 B], then V
-    static constexpr int kKeysOff = kKV + STAGES * kStageBytes;   // int32 [stage][8 chunks] valid keys
-    static constexpr int kBar = kKeysOff + 128;                    // mbarriers, 8 bytes each
+    static constexpr int kKeySlots = 4;                            // blocks whose chunk key counts are kept
+    static constexpr int kKeysOff = kKV + STAGES * kStageBytes;   // int32 [kKeySlots][8 chunks] valid keys
+    static constexpr int kBar = kKeysOff + kKeySlots * 8 * 4;      // mbarriers, 8 bytes each
     static constexpr int kTmemSlot = kBar + 256;
     static constexpr int kBytes = kTmemSlot + 16;
     static constexpr int kAlloc = kBytes + 1024;
     // mbarrier indices; the per-buffer ones are [TILES][kNBuf] (tile-major)
-    static constexpr int kBarKvFull = 0;                          // [STAGES] producer: expect_tx + the copies' bytes
-    static constexpr int kBarKvEmpty = kBarKvFull + STAGES;       // [STAGES] MMA commit after the block's last PV
-    static constexpr int kBarSFull = kBarKvEmpty + STAGES;        // MMA commit after S = Q K^T
+    static constexpr int kBarKFull = 0;                           // [STAGES] producer: expect_tx + the K copies' bytes
+    static constexpr int kBarKEmpty = kBarKFull + STAGES;         // [STAGES] MMA commit after the block's last QK
+    static constexpr int kBarVFull = kBarKEmpty + STAGES;         // [STAGES] producer: expect_tx + the V copies' bytes
+    static constexpr int kBarVEmpty = kBarVFull + STAGES;         // [STAGES] MMA commit after the block's last PV
+    static constexpr int kBarSFull = kBarVEmpty + STAGES;         // MMA commit after S = Q K^T
     static constexpr int kBarPFull = kBarSFull + TILES * kNBuf;   // the tile's 128 softmax threads wrote P
     static constexpr int kBarODone = kBarPFull + TILES * kNBuf;   // MMA commit after O += P V
     static constexpr int kBarQFull = kBarODone + TILES * kNBuf;   // [TILES] the tile's 128 threads wrote Q
@@ -147,7 +152,7 @@ struct PreCfg {
     static constexpr int kNumBars = kBarFinal + 1;
     static_assert(TILES == 1 || TILES == 2, "one or two query tiles per CTA");
     static_assert(kNumBars * 8 <= 256, "the mbarriers fit their shared-memory slot");
-    static_assert(STAGES * 8 * 4 <= 128, "the per-stage chunk key counts fit their shared-memory slot");
+    static_assert(kKeySlots >= 2 * STAGES, "a block's key counts outlive both tiles' softmax of it");
     static_assert(TILES * kTileCols <= kTmemCols, "every tile's S buffers and O fit the TMEM allocation");
     static_assert(kAlloc * kMinBlocks <= 227 * 1024 - 1024 * (kMinBlocks - 1), "shared memory per SM");
 };
@@ -157,13 +162,15 @@ __global__ void __launch_bounds__(PreCfg<KEYS, STAGES, TILES>::kThreads, PreCfg<
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                T *__restrict__ out, const T *__restrict__ q, const int32_t *__restrict__ block_tables,
                int32_t max_blocks, const int32_t *__restrict__ starts, const int32_t *__restrict__ cu_q,
-               int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, int32_t box_rows, float scale_log2,
+               int32_t Hq, int32_t G, int32_t bs, int32_t num_blocks, int32_t box_lg, float scale_log2,
                int32_t *__restrict__ err_flag) {
     using L = PreCfg<KEYS, STAGES, TILES>;
     constexpr int kPreKeys = KEYS, kPreStages = STAGES, kNBuf = L::kNBuf, kSoftWarps = L::kSoftWarps;
     constexpr int kKvHalf = L::kKvHalf, kKvTileBytes = L::kKvTileBytes, kStageBytes = L::kStageBytes;
     constexpr uint32_t kTmemO = L::kTmemO, kTileCols = L::kTileCols, kPreTmemCols = L::kTmemCols;
-    constexpr int kBarKvFull = L::kBarKvFull, kBarKvEmpty = L::kBarKvEmpty, kBarSFull = L::kBarSFull;
+    constexpr int kBarKFull = L::kBarKFull, kBarKEmpty = L::kBarKEmpty, kBarSFull = L::kBarSFull;
+    constexpr int kBarVFull = L::kBarVFull, kBarVEmpty = L::kBarVEmpty, kKeySlots = L::kKeySlots;
+    static_assert(TILES == 2 && KEYS == 128, "the kernel runs two query tiles of 128-key blocks");
     constexpr int kBarPFull = L::kBarPFull, kBarODone = L::kBarODone, kBarQFull = L::kBarQFull;
     constexpr int kBarFinal = L::kBarFinal;
     using H = Half16<T>;
@@ -178,8 +185,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t sQ = smem_u32(smem + L::kQ), sKV = smem_u32(smem + L::kKV);
     if (warp == kSoftWarps && lane == 0) {
         for (int s = 0; s < kPreStages; ++s) {  // per K/V stage
-            mbar_init(bar(kBarKvFull + s), 1);
-            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+            mbar_init(bar(kBarVFull + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
         }
         for (int p = 0; p < TILES * kNBuf; ++p) {  // per tile and S / P buffer
             mbar_init(bar(kBarSFull + p), 1);
@@ -233,21 +242,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
     if (warp == kSoftWarps) {
         // ------------------------------------------------------------ producer warp
-        // Block j's keys come in chunks of box_rows (= gcd(block_size, 128)) keys:
-        // lane l < 128 / box_rows takes chunk l, whose rows are consecutive in one
+        // Block j's keys come in chunks of box_rows = 2^box_lg (= gcd(block_size, 128))
+        // keys: lane l < 128 / box_rows takes chunk l, whose rows are consecutive in one
         // page.  Chunks at or past the end of the span, or of a page whose id is
         // out of range, are not copied; kv_keys[stage][l] gives the consumers the
         // chunk's number of valid keys.
         const int32_t *row = block_tables + static_cast<int64_t>(b) * max_blocks;
+        const int box_rows = 1 << box_lg;
         const int nch = kPreKeys / box_rows;
         const uint32_t chunk_bytes = static_cast<uint32_t>(box_rows) * 128;  // one 64-dim half of a chunk
         bool bad = false;
-        int issued = 0;
+        int issued_k = 0, issued_v = 0;
+        // Block j's K and V go to buffers j % STAGES of two separate rings: K_j
+        // once both tiles' QKs of block j - STAGES have read that K buffer, V_j
+        // once their PVs of block j - STAGES have read that V buffer, so the K
+        // copies run a QK ahead of what one K+V stage would allow.
+        auto wait_free = [&](int empty, int j) -> bool {
+            int ok = 1;
+            if (lane == 0 && j >= kPreStages) ok = mbar_wait(bar(empty + j % kPreStages), ((j / kPreStages) - 1) & 1, deadline);
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
         for (int j = 0; j < nblk; ++j) {
             const int s = j % kPreStages;
-            int ok = 1;
-            if (lane == 0 && j >= kPreStages) ok = mbar_wait(bar(kBarKvEmpty + s), ((j / kPreStages) - 1) & 1, deadline);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            if (!wait_free(kBarKEmpty, j)) {
                 timed_out = true;
                 break;
             }
@@ -262,42 +279,53 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     keys = left < box_rows ? static_cast<int>(left) : box_rows;
                 }
             }
-            if (lane < nch) kv_keys[s * 8 + lane] = keys;
-            const uint32_t full = bar(kBarKvFull + s);
+            if (lane < nch) kv_keys[(j % kKeySlots) * 8 + lane] = keys;
             const unsigned loaded = __ballot_sync(0xffffffffu, keys > 0);
+            const uint32_t tile_bytes = static_cast<uint32_t>(__popc(loaded)) * 2u * chunk_bytes;  // K (or V) of the block
+            const int slot_row = keys > 0 ? id * bs + key0 % bs : 0;
+            const uint32_t kdst = sKV + static_cast<uint32_t>(s) * kStageBytes + lane * chunk_bytes;
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(loaded)) * 4u * chunk_bytes);
+            if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + s), tile_bytes);
             __syncwarp();
             if (keys > 0) {
-                const int slot_row = id * bs + key0 % bs;
-                const uint32_t kdst = sKV + static_cast<uint32_t>(s) * kStageBytes + lane * chunk_bytes;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tma_load_3d(kdst + h * kKvHalf, &tm_k, 0, slot_row, 2 * kh + h, full);
-                    tma_load_3d(kdst + kKvTileBytes + h * kKvHalf, &tm_v, 0, slot_row, 2 * kh + h, full);
-                }
+                for (int h = 0; h < 2; ++h) tma_load_3d(kdst + h * kKvHalf, &tm_k, 0, slot_row, 2 * kh + h, bar(kBarKFull + s));
             }
-            issued = j + 1;
+            issued_k = j + 1;
+            if (!wait_free(kBarVEmpty, j)) {
+                timed_out = true;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + s), tile_bytes);  // after the key counts (release)
+            __syncwarp();
+            if (keys > 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(kdst + kKvTileBytes + h * kKvHalf, &tm_v, 0, slot_row, 2 * kh + h, bar(kBarVFull + s));
+            }
+            issued_v = j + 1;
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
             if (bad && err_flag && kh == 0 && blockIdx.x == 0) atomicOr(err_flag, PKV_ERRBIT_BLOCK_RANGE);
             // no bulk copy may still be writing shared memory when the CTA exits
-            for (int j = issued - kPreStages > 0 ? issued - kPreStages : 0; j < issued; ++j)
-                if (!mbar_wait(bar(kBarKvFull + j % kPreStages), (j / kPreStages) & 1, deadline)) timed_out = true;
+            for (int j = issued_k - kPreStages > 0 ? issued_k - kPreStages : 0; j < issued_k; ++j)
+                if (!mbar_wait(bar(kBarKFull + j % kPreStages), (j / kPreStages) & 1, deadline)) timed_out = true;
+            for (int j = issued_v - kPreStages > 0 ? issued_v - kPreStages : 0; j < issued_v; ++j)
+                if (!mbar_wait(bar(kBarVFull + j % kPreStages), (j / kPreStages) & 1, deadline)) timed_out = true;
         }
     } else if (warp == kSoftWarps + 1) {
         // ------------------------------------------------------------ MMA warp
         if (lane == 0) {
             constexpr uint32_t kIdescS = umma_idesc_f16(kBf16, kPreRows, kPreKeys, false);
             constexpr uint32_t kIdescO = umma_idesc_f16(kBf16, kPreRows, kFastHeadDim, true);
-            // S_j of tile t = Q_t K_j^T into the tile's buffer j % kNBuf, once the
-            // stage has landed and the PV that last read that buffer is done.
+            // S_j of tile t = Q_t K_j^T into the tile's S / P buffer once K_j has
+            // landed.  The buffer's previous P (block j - 1) is read by a PV this
+            // thread issued earlier: tcgen05.mma operations of one thread run in
+            // issue order, so S_j may be issued without waiting for that PV.
             auto issue_qk = [&](int t, int j) -> bool {
                 const int s = j % kPreStages, bj = j % kNBuf;
-                bool ok = mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
-                if (ok && j >= kNBuf)
-                    ok = mbar_wait(bar(kBarODone + t * kNBuf + bj), ((j - kNBuf) / kNBuf) & 1, deadline);
+                bool ok = mbar_wait(bar(kBarKFull + s), (j / kPreStages) & 1, deadline);
                 if (!ok) return false;
                 tc_fence_after();
                 const uint32_t kt = sKV + static_cast<uint32_t>(s) * kStageBytes;
@@ -312,10 +340,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 umma_commit(bar(kBarSFull + t * kNBuf + bj));
                 return true;
             };
-            // O_t (+)= P_j V_j once the tile's softmax threads wrote P_j.
+            // O_t (+)= P_j V_j once the tile's softmax threads wrote P_j and V_j has landed.
             auto issue_pv = [&](int t, int j) -> bool {
                 const int s = j % kPreStages, bj = j % kNBuf;
-                if (!mbar_wait(bar(kBarPFull + t * kNBuf + bj), (j / kNBuf) & 1, deadline)) return false;
+                if (!mbar_wait(bar(kBarPFull + t * kNBuf + bj), (j / kNBuf) & 1, deadline) ||
+                    !mbar_wait(bar(kBarVFull + s), (j / kPreStages) & 1, deadline))
+                    return false;
                 tc_fence_after();
                 const uint32_t vt = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes;
                 const uint32_t tc = tmem + t * kTileCols;
@@ -330,38 +360,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             bool ok = true;
             for (int t = 0; t < TILES; ++t)
                 if (ok && nblk_t[t] > 0) ok = mbar_wait(bar(kBarQFull + t), 0, deadline);
-            if constexpr (TILES == 1) {
-                // QK_j, then (one block behind) PV_{j-1}: S_{j+1} is computed while
-                // the softmax works on S_j.
-                for (int j = 0; ok && j <= nblk; ++j) {
-                    if (j < nblk) ok = issue_qk(0, j);
-                    if (ok && j >= 1) {
-                        ok = issue_pv(0, j - 1);
-                        if (ok) umma_commit(bar(kBarKvEmpty + (j - 1) % kPreStages));
-                    }
-                }
-            } else {
-                // Two tiles take turns: while one tile's softmax works on S_j, the
-                // tensor core runs the other tile's PV and next QK.  With one S
-                // buffer per tile the next QK follows the PV that frees it; with two
-                // it goes first (its buffer was freed by the PV of block j - 1).
-                if (ok) ok = issue_qk(0, 0);
-                if (ok && nblk_t[1] > 0) ok = issue_qk(1, 0);
-                for (int j = 0; ok && j < nblk; ++j) {
-                    if constexpr (kNBuf == 1) {
-                        ok = issue_pv(0, j);
-                        if (ok && j + 1 < nblk) ok = issue_qk(0, j + 1);
-                        if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
-                        if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
-                        if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
-                    } else {
-                        if (j + 1 < nblk) ok = issue_qk(0, j + 1);
-                        if (ok) ok = issue_pv(0, j);
-                        if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
-                        if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
-                        if (ok) umma_commit(bar(kBarKvEmpty + j % kPreStages));  // both tiles' PVs read stage j
-                    }
-                }
+            // The tiles take turns: while one tile's softmax works on S_j, the
+            // tensor core runs the other tile's PV and next QK.  A K buffer is
+            // released once both tiles' QKs of its block are issued, a V buffer
+            // once both PVs are (the commits arrive when those MMAs complete).
+            if (ok) ok = issue_qk(0, 0);
+            if (ok && nblk_t[1] > 0) ok = issue_qk(1, 0);
+            if (ok) umma_commit(bar(kBarKEmpty + 0));
+            for (int j = 0; ok && j < nblk; ++j) {
+                ok = issue_pv(0, j);
+                if (ok && j + 1 < nblk) ok = issue_qk(0, j + 1);
+                if (ok && j < nblk_t[1]) ok = issue_pv(1, j);
+                if (ok) umma_commit(bar(kBarVEmpty + j % kPreStages));
+                if (ok && j + 1 < nblk_t[1]) ok = issue_qk(1, j + 1);
+                if (ok && j + 1 < nblk) umma_commit(bar(kBarKEmpty + (j + 1) % kPreStages));
             }
             if (!ok) timed_out = true;
             umma_commit(bar(kBarFinal));  // arrives once every MMA issued above has completed
@@ -400,8 +412,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         float m_ref = -INFINITY, l_sum = 0.f;
         for (int j = 0; j < my_nblk; ++j) {
             const int s = j % kPreStages, bj = j % kNBuf;
+            // S_j, then V_j: the block's key counts were written before V_j's copy
+            // was armed, and tile 0 zeroes V rows of keys that were not copied.
             bool ok = mbar_wait(bar(kBarSFull + bar_t + bj), (j / kNBuf) & 1, deadline) &&
-                      mbar_wait(bar(kBarKvFull + s), (j / kPreStages) & 1, deadline);
+                      mbar_wait(bar(kBarVFull + s), (j / kPreStages) & 1, deadline);
             if (!__all_sync(0xffffffffu, ok)) {
                 timed_out = true;
                 break;
@@ -421,8 +435,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 const int causal = live ? pos - j * kPreKeys : -1;  // keys k <= causal are visible
 #pragma unroll
                 for (int g = 0; g < kPreKeys / 16; ++g) {
-                    const int ch = (16 * g) / box_rows, off = 16 * g - ch * box_rows;
-                    const int copied = kv_keys[s * 8 + ch] - off;  // valid keys of the group, from its first
+                    const int ch = (16 * g) >> box_lg, off = 16 * g - (ch << box_lg);
+                    const int copied = kv_keys[(j % kKeySlots) * 8 + ch] - off;  // valid keys of the group, from its first
                     const int c = causal - 16 * g;
                     lim[g] = min(c, min(copied, 16) - 1);      // keys 16g + i valid for i <= lim[g]
                 }
@@ -507,8 +521,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
             tmem_wait_st();
             if (t == 0 && r < kPreKeys) {  // V row of key r: zeros where nothing valid was copied (0 * NaN would poison O)
-                const int g = r >> 4, ch = (16 * g) / box_rows;
-                if ((r & 15) >= kv_keys[s * 8 + ch] - (16 * g - ch * box_rows)) {
+                const int g = r >> 4, ch = (16 * g) >> box_lg;
+                if ((r & 15) >= kv_keys[(j % kKeySlots) * 8 + ch] - (16 * g - (ch << box_lg))) {
                     const uint32_t vrow = sKV + static_cast<uint32_t>(s) * kStageBytes + kKvTileBytes + r * 128;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
@@ -592,7 +606,8 @@ pkv_status launch_prefill(void *out, const void *q, const void *k_cache, const v
     using L = PreCfg<KEYS, STAGES, TILES>;
     e = launch_pdl(kPdlDecode, prefill_kernel<T, KEYS, STAGES, POS, TILES>, dim3((tiles + TILES - 1) / TILES, Hkv, B),
                    dim3(L::kThreads), L::kAlloc, stream, mk, mv, static_cast<T *>(out), static_cast<const T *>(q),
-                   block_tables, max_blocks, starts, cu_q, Hq, G, bs, num_blocks, box_rows, scale * kPreLog2e, err);
+                   block_tables, max_blocks, starts, cu_q, Hq, G, bs, num_blocks, __builtin_ctz(box_rows),
+                   scale * kPreLog2e, err);
     if (e != cudaSuccess) return set_error(PKV_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
