@@ -246,8 +246,10 @@ PKV_API pkv_status pkv_paged_attention_decode_plan(int32_t num_seqs, int32_t num
  * PKV_ERR_WORKSPACE before anything is enqueued; use the workspace variant
  * for those.  Argument errors (bad sizes, NULL pointers) are reported as
  * PKV_ERR_INVALID_ARG first, exactly as by pkv_paged_attention_decode.  The
- * decode workloads of the benchmark fit: 8 x 32768 tokens at Hq 32 / Hkv 8
- * needs about 15.9 MB, 64 x 4096 at Hq = Hkv = 32 about 14.4 MB.
+ * size bound assumes every sequence holds max_context_len tokens: 8 x 32768
+ * tokens at Hq 32 / Hkv 8 needs about 15.9 MB and fits, as do 64 x 4096 at
+ * Hq = Hkv = 32 (14.6 MB) and 8 x 8192 (7.4 MB); 128 sequences of up to 8192
+ * tokens at Hq 16 / Hkv 8 need about 27 MB and do not.
  *
  * Every call looks up the region's device address (cudaGetSymbolAddress)
  * with the calling thread's current device; the lookup allocates nothing.

@@ -394,7 +394,7 @@ def test_full_size_decode_step(pkv, orc, cuda_dev, name):
     assert torch.equal(_bits(batch.k_cache), _bits(kr)) and torch.equal(_bits(batch.v_cache), _bits(vr))
     ws = pkv.pkv_paged_attention_decode_workspace_size(B, cfg.num_q_heads, cfg.num_kv_heads, 128, bs,
                                                        batch.max_context_len, cfg.dtype)
-    workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=cuda_dev)
+    workspace = torch.zeros(max(ws, 1), dtype=torch.uint8, device=cuda_dev)
     out = pkv.pkv_paged_attention_decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
                                          batch.context_lens, batch.scale, batch.max_context_len,
                                          workspace=workspace, err_flag=err)
