@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0,
                     help="wall-clock budget of the oracle CPU-baseline sample")
+    ap.add_argument("--window-s", type=float, default=1.0,
+                    help="device time of every throughput window (profiler runs pass 0: one graph replay each)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="measure only --config (skip the other decode workloads of the per-workload block)")
     ap.add_argument("--skip-cpu-baseline", action="store_true",
@@ -539,10 +541,11 @@ def time_graphs(step, steps: int, world: int, io=None):
     return e0.elapsed_time(e1), (t_wall0, t_wall1)
 
 
-def replay_window(g, units_per_replay: int, world: int, min_s: float = MIN_WINDOW_S, min_units: int = 0):
+def replay_window(g, units_per_replay: int, world: int, min_s: float | None = None, min_units: int = 0):
     """Replays graph g back to back until at least min_s seconds of device time
-    (and min_units units) have run between two CUDA events.  Returns (ms per
-    unit, units timed, (wall start, wall end))."""
+    (and min_units units) have run between two CUDA events (min_s defaults to
+    MIN_WINDOW_S).  Returns (ms per unit, units timed, (wall start, wall end))."""
+    min_s = MIN_WINDOW_S if min_s is None else min_s
     for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
@@ -584,7 +587,7 @@ def calls_per_graph(est_ms: float, ncopies: int) -> int:
     return (n + ncopies - 1) // ncopies * ncopies
 
 
-def time_sustained(step, what, world: int, est_ms: float, ncopies: int = 1, min_s: float = MIN_WINDOW_S,
+def time_sustained(step, what, world: int, est_ms: float, ncopies: int = 1, min_s: float | None = None,
                    min_calls: int = 0):
     """Calls of `what` back to back, as a decode loop issues them, rotating
     over ncopies cache copies, for at least min_s seconds of device time.
@@ -930,6 +933,9 @@ def run_reference(args, world, rank):
 
 def run_ours(args, world, rank, local):
     import pagedattention_decode_pkv_gb300 as pkv
+
+    global MIN_WINDOW_S
+    MIN_WINDOW_S = args.window_s
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
