@@ -75,12 +75,14 @@ def test_append_fused_equal_lengths(pkv, orc, cuda_dev, Hq, Hkv, bs, ctx, B):
     assert _max_err(out, ref) <= ATOL_16
 
 
-def test_append_equals_the_three_calls(pkv, cuda_dev):
-    """Fused step == slot mapping + store + attention through the library, bit for bit."""
+def test_append_equals_the_three_calls(pkv, orc, cuda_dev):
+    """Fused step == slot mapping + store + attention through the library, bit
+    for bit, and both equal the oracle's decode step."""
     cfg = wl.LONG_GQA_8K
     lens = [8192, 5000, 17, 1, 4096, 777, 16, 2048]
     a = wl.decode_batch(cfg, seed=21, device=cuda_dev, ctx_override=lens, nan_tails=True)
     b = wl.decode_batch(cfg, seed=21, device=cuda_dev, ctx_override=lens, nan_tails=True)
+    kc0, vc0 = a.k_cache.cpu(), a.v_cache.cpu()
     out_fused = _append(pkv, a, 8192)
     nb = b.extra["num_blocks"]
     slots = pkv.pkv_compute_slot_mapping(b.block_tables, b.starts, b.ends, b.cu_new, cfg.block_size, nb,
@@ -91,6 +93,10 @@ def test_append_equals_the_three_calls(pkv, cuda_dev):
     torch.cuda.synchronize()
     assert torch.equal(_bits(a.k_cache), _bits(b.k_cache)) and torch.equal(_bits(a.v_cache), _bits(b.v_cache))
     assert torch.equal(_bits(out_fused), _bits(out_sep))
+    ref, kr, vr, nerr = _oracle_step(orc, a, kc0, vc0)
+    assert nerr == 0
+    assert torch.equal(_bits(a.k_cache), _bits(kr)) and torch.equal(_bits(a.v_cache), _bits(vr))
+    assert _max_err(out_fused, ref) <= ATOL_16
 
 
 @pytest.mark.parametrize("case", ["fixed_partitions", "generic_fp32", "generic_fp16_d64", "unaligned_key"])

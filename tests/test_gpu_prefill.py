@@ -94,9 +94,10 @@ def test_prefill_peaky_and_last_row_equals_decode(pkv, orc, cuda_dev, mode):
     torch.testing.assert_close(out[last].float(), dec.float(), rtol=2 ** -7, atol=1e-2)
 
 
-def test_prefill_in_chunks_equals_one_pass(pkv, cuda_dev):
+def test_prefill_in_chunks_equals_one_pass(pkv, orc, cuda_dev):
     """Chunked prefill: the same queries split into two calls (positions
-    [0, 700) then [700, 1000)) give the rows of one call, bit for bit."""
+    [0, 700) then [700, 1000)) give the rows of one call, and both match the
+    oracle's single pass."""
     batch, q, starts, cu, _ = _case(torch.bfloat16, 16, 8, 16, [(0, 1000)], seed=71, cuda_dev=cuda_dev)
     whole = pkv.pkv_paged_attention_prefill(q, batch.k_cache, batch.v_cache, batch.block_tables, starts, cu,
                                             batch.scale, 1000)
@@ -111,6 +112,10 @@ def test_prefill_in_chunks_equals_one_pass(pkv, cuda_dev):
     # of the bf16 output (2^-7 relative covers it in every binade) on top of
     # the 1e-2 absolute noise of a sum of unit-size terms.
     torch.testing.assert_close(torch.cat(parts).float(), whole.float(), rtol=2 ** -7, atol=1e-2)
+    ref, nerr = orc.paged_attention_prefill(q, batch.k_cache, batch.v_cache, batch.block_tables, starts, cu,
+                                            batch.scale)
+    assert nerr == 0
+    assert _max_err(whole, ref) <= ATOL_16 and _max_err(torch.cat(parts), ref) <= ATOL_16
 
 
 def test_prefill_errors(pkv, orc, cuda_dev):
